@@ -1,0 +1,439 @@
+"""Paged decode benchmark: one decode step of a Llama-3-8B-shaped layer.
+
+Workload (the headline configuration): 64 sequences, 32 query / 8 KV heads,
+head_dim 128, bf16 cache, block size 16; context lengths are prompt + output
+of the first 64 requests of the seeded request mix (sum 121,416 tokens,
+732..3360); blocks are a seeded permutation of a pool 1.2x the blocks used.
+One step = the host slot mapping of the 64 new tokens, the cache write of
+their K/V (pa_reshape_and_cache) and paged decode over all 64 sequences
+(pa_decode: paged-decode kernel + split-K combine).
+
+Metric: achieved HBM GB/s on the algorithmic bytes a step must move
+(K and V of every context token once, q, out, block-table entries, lengths,
+the new tokens' K/V write) and microseconds per step.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun every rank runs an independent replica on its own GPU (the
+path has no cross-GPU exchange); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak) and µs/step"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--partition", type=int, default=0, help="split-K partition (0 = auto)")
+    ap.add_argument("--kernel", type=int, default=0, help="decode kernel (0 auto, 1 SIMT, 2 tcgen05)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- workload
+
+class Step:
+    """Device-resident state of the headline decode step."""
+
+    def __init__(self, device, partition=0, kernel=0):
+        import torch
+
+        from paged_kv_cache_108_gb300 import ops, pool, synth
+        self.torch, self.ops, self.pool = torch, ops, pool
+        w = synth.llama8b(with_data=False)
+        self.w = w
+        self.device = device
+        self.partition, self.kernel = partition, kernel
+        B, hkv, d, H = w.block_size, w.num_kv_heads, w.head_dim, w.num_heads
+        gen = torch.Generator(device=device)
+        gen.manual_seed(w.seed)
+        shape = (w.num_blocks, B, hkv, d)
+        self.k_cache = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+        self.v_cache = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+        S = w.num_seqs
+        self.q = torch.randn((S, H, d), generator=gen, device=device).to(torch.bfloat16)
+        self.k_new = torch.randn((S, hkv, d), generator=gen, device=device).to(torch.bfloat16)
+        self.v_new = torch.randn((S, hkv, d), generator=gen, device=device).to(torch.bfloat16)
+        self.positions = (w.context_lens - 1).astype(np.int32)
+        slots = pool.slot_mapping(w.block_tables, B, self.positions)
+        self.slots = torch.from_numpy(slots).to(device)
+        self.block_tables = torch.from_numpy(w.block_tables).to(device)
+        self.context_lens = torch.from_numpy(w.context_lens).to(device)
+        self.out = torch.empty_like(self.q)
+        self.ws = ops.alloc_workspace(S, H, d, w.max_blocks, B, partition, device=device)
+        self.splits = ops.decode_workspace_size(S, H, d, w.max_blocks, B, partition) > 0
+        self.launches_per_step = 2 + (1 if self.splits else 0)
+
+    # algorithmic bytes of one step (what the method must move)
+    def decode_bytes(self) -> int:
+        w = self.w
+        kv = int(np.sum(w.context_lens)) * w.num_kv_heads * w.head_dim * 2 * 2
+        qo = 2 * w.num_seqs * w.num_heads * w.head_dim * 2
+        table = int(sum(math.ceil(n / w.block_size) for n in w.context_lens)) * 4
+        return kv + qo + table + w.num_seqs * 4
+
+    def write_bytes(self) -> int:
+        w = self.w
+        return 2 * (2 * w.num_seqs * w.num_kv_heads * w.head_dim * 2) + w.num_seqs * 4
+
+    def run_write(self, slots=None, k=None, v=None):
+        self.ops.reshape_and_cache(self.k_new if k is None else k, self.v_new if v is None else v,
+                                   self.k_cache, self.v_cache, self.slots if slots is None else slots)
+
+    def run_decode(self, q=None, bt=None, cl=None):
+        w = self.w
+        self.ops.decode(self.out, self.q if q is None else q, self.k_cache, self.v_cache,
+                        self.block_tables if bt is None else bt,
+                        self.context_lens if cl is None else cl, w.scale, workspace=self.ws,
+                        partition_tokens=self.partition, kernel=self.kernel)
+
+
+# ---------------------------------------------------------------- helpers
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:  # noqa: BLE001
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(step_bytes):
+    """ncu DRAM bytes per decode call, if recorded for the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:  # noqa: BLE001
+        return None
+    import hashlib
+    h = hashlib.sha256()
+    for rel in rec.get("sources", []):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != rec.get("sources_sha256"):
+        return None
+    return rec.get("dram_bytes_per_call")
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:  # noqa: BLE001
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:  # noqa: BLE001
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower() in ("active", "1"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline_oracle(step, budget_s=10.0):
+    """Time the fp64 oracle on this step's data on the host cores."""
+    from oracle import core as ocore
+    torch = step.torch
+    w = step.w
+    kc = step.k_cache.view(torch.int16).cpu().numpy().view(np.uint16)
+    vc = step.v_cache.view(torch.int16).cpu().numpy().view(np.uint16)
+    q = step.q.view(torch.int16).cpu().numpy().view(np.uint16)
+    threads = os.cpu_count() or 1
+    units = [(i, g) for i in range(w.num_seqs) for g in range(w.num_kv_heads)]
+    # bounded sample: the first sequences' units until the budget is spent
+    bytes_done, t_total, reps = 0, 0.0, 0
+    per_unit_bytes = {(i, g): int(w.context_lens[i]) * w.head_dim * 2 * 2 for i, g in units}
+    chunk = max(threads, 32)
+    at = 0
+    while t_total < budget_s and reps < 64:
+        sel = units[at:at + chunk]
+        if not sel:
+            at = 0
+            continue
+        t0 = time.perf_counter()
+        ocore.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, units=sel,
+                     nthreads=threads)
+        t_total += time.perf_counter() - t0
+        bytes_done += sum(per_unit_bytes[u] for u in sel)
+        at += chunk
+        reps += 1
+    gbs = bytes_done / t_total / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{reps} batches of {chunk} (sequence, kv-head) units of the llama8b step "
+                      f"({bytes_done / 1e6:.0f} MB of KV, {t_total:.1f} s), fp64, {threads} threads"}
+
+
+# ---------------------------------------------------------------- arms
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    step = Step(device, args.partition, args.kernel)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def one_step():
+        step.run_write()
+        step.run_decode()
+
+    for _ in range(max(args.warmup, 3)):
+        one_step()
+    torch.cuda.synchronize()
+
+    # device-resident timing: per step events around write, decode
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        for k in range(K):
+            flush.zero_()  # L2 flush, outside the timed events
+            ev[k][0].record(stream)
+            step.run_write()
+            ev[k][1].record(stream)
+            step.run_decode()
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    step_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(K)]
+    dec_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    wr_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    mean_step = sum(step_ms) / K
+    mean_dec = sum(dec_ms) / K
+    t = torch.tensor([mean_step, mean_dec], dtype=torch.float64, device=device)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    mean_step, mean_dec = float(t[0]), float(t[1])
+
+    # end-to-end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(step, args, device, dist)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_oracle(step)
+
+    if rank != 0:
+        return
+    peak, peak_src = measured_peak()
+    dbytes = step.decode_bytes()
+    sbytes = dbytes + step.write_bytes()
+    achieved = dbytes / (mean_dec * 1e-3) / 1e9
+    value = world * sbytes / (mean_step * 1e-3) / 1e9
+    w = step.w
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(mean_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/q; lengths from the pages' seeded request mix)",
+        "config": {"workload": "llama8b-layer decode, batch 64, 32q/8kv heads, d=128, bf16 KV, "
+                               "block 16, sum ctx 121416", "num_seqs": w.num_seqs,
+                   "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads,
+                   "head_dim": w.head_dim, "block_size": w.block_size,
+                   "num_blocks": w.num_blocks, "sum_context": int(np.sum(w.context_lens)),
+                   "partition_tokens": args.partition or "auto", "kernel": args.kernel or "auto",
+                   "bytes_per_step": sbytes, "decode_bytes_per_step": dbytes,
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB memset, untimed)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "us_per_step": round(mean_step * 1e3, 2),
+        "us_per_step_p50": round(statistics.median(step_ms) * 1e3, 2),
+        "us_per_step_p90": round(float(np.percentile(step_ms, 90)) * 1e3, 2),
+        "us_decode": round(mean_dec * 1e3, 2),
+        "us_write": round(sum(wr_ms) / K * 1e3, 2),
+        "tokens_per_s": round(world * w.num_seqs / (mean_step * 1e-3), 1),
+        "pct_of_nominal_8tbps": round(100 * achieved / 8000.0, 1),
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (paged decode + split-K combine)",
+                     "achieved": round(achieved, 2), "peak": peak, "peak_source": peak_src,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(dbytes),
+                     "algorithmic_bytes": dbytes},
+        "gpu_launches": K * step.launches_per_step,
+        "clocks": clk.summary(),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(step, args, device, dist):
+    """Same metric through the public API with pinned host buffers: per step,
+    host slot mapping, host->device copies of the step's inputs, cache write,
+    decode, and a device->host read of the output."""
+    import torch
+    w = step.w
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    h_q, h_k, h_v = pin(step.q), pin(step.k_new), pin(step.v_new)
+    h_bt = torch.from_numpy(w.block_tables).pin_memory()
+    h_cl = torch.from_numpy(w.context_lens).pin_memory()
+    h_slots = torch.empty(w.num_seqs, dtype=torch.int32).pin_memory()
+    h_out = torch.empty(step.out.shape, dtype=torch.bfloat16).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(step.q), torch.empty_like(step.k_new), torch.empty_like(step.v_new)
+    d_bt, d_cl = torch.empty_like(step.block_tables), torch.empty_like(step.context_lens)
+    d_slots = torch.empty_like(step.slots)
+    bi = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_bt, h_cl, h_slots))
+    bo = h_out.numel() * h_out.element_size()
+
+    def one():
+        h_slots.numpy()[:] = step.pool.slot_mapping(w.block_tables, w.block_size, step.positions)
+        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_bt, h_bt), (d_cl, h_cl),
+                     (d_slots, h_slots)):
+            d.copy_(h, non_blocking=True)
+        step.run_write(d_slots, d_k, d_v)
+        step.run_decode(d_q, d_bt, d_cl)
+        h_out.copy_(step.out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()  # the host reads the result
+
+    for _ in range(max(args.warmup, 3)):
+        one()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / args.steps
+    t = torch.tensor([dt], dtype=torch.float64, device=device)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dt = float(t[0])
+    world = dist.get_world_size() if dist else 1
+    sbytes = step.decode_bytes() + step.write_bytes()
+    return {"value": round(world * sbytes / dt / 1e9, 2), "unit": "GB/s",
+            "us_per_step": round(dt * 1e6, 2), "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is a bounded sample of the
+    headline workload (a fixed set of (sequence, kv-head) units) decoded by
+    the fp64 CPU oracle on the host cores."""
+    if rank != 0:
+        return
+    from oracle import core as ocore
+    from paged_kv_cache_108_gb300 import synth
+    w = synth.llama8b(with_data=False)
+    rng = np.random.default_rng(w.seed)
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    kc = synth.normal_bf16(rng, shape)
+    vc = synth.normal_bf16(rng, shape)
+    q = synth.normal_bf16(rng, (w.num_seqs, w.num_heads, w.head_dim))
+    threads = os.cpu_count() or 1
+    # each step decodes sequences 0..7 (64 of the 512 (sequence, kv-head) units)
+    n_seq = 8
+    units = [(i, g) for i in range(n_seq) for g in range(w.num_kv_heads)]
+    ub = sum(int(w.context_lens[i]) * w.head_dim * 2 * 2 for i, _ in units)
+    qo = n_seq * w.num_heads * w.head_dim * 2 * 2
+    for _ in range(max(args.warmup, 3)):
+        ocore.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, units=units, nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ocore.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, units=units, nthreads=threads)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = (ub + qo) / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "llama8b-layer decode sample: sequences 0-7 x 8 kv heads "
+                                   "of the batch-64 step (32q/8kv, d=128, block 16)"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle",
+                             "sample": "64 (sequence, kv-head) units (sequences 0-7) of the "
+                                       "llama8b step per step"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

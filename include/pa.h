@@ -1,0 +1,246 @@
+/*
+ * pa.h -- C ABI of the GB300-native paged-KV decode library (libpa.so).
+ *
+ * The operations are those of vLLM-style PagedAttention as described on the
+ * pages "4.6 PagedAttention & KV-Cache Memory Management" (llm-stack-book,
+ * cited below as [LSB]), "Paged KV cache" (ai-infra-handbooks, [PKV]),
+ * "Allocate the Cache: Blocks, Waste, and PagedAttention" (int8ai.com, [ATC])
+ * and "PagedAttention - Explained" (mohdvasim.com, [PAE]).
+ *
+ * Conventions shared by every device entry point
+ *  - Device pointers are raw CUDA device addresses; the caller owns every
+ *    buffer (including the decode workspace) and keeps it alive until the
+ *    work queued on `stream` has finished.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  The library allocates no device memory and
+ *    performs no host<->device synchronisation or copy.
+ *  - Host-visible arguments are validated before anything is launched; on a
+ *    failed check nothing is launched and PA_ERR_INVALID or
+ *    PA_ERR_UNSUPPORTED is returned.  A failed launch returns PA_ERR_CUDA.
+ *    pa_last_error() gives a one-line description of the last failure on
+ *    the calling thread.
+ *  - Contents of device buffers (block ids, slots, context lengths) are not
+ *    visible to the host and are not validated there.  Kernels skip any
+ *    block id outside [0, num_blocks) or slot outside [0, num_blocks *
+ *    block_size) instead of touching memory out of bounds; the affected
+ *    outputs are then unspecified.
+ *
+ * Cache layout (per layer, one tensor for K and one for V):
+ *    [num_blocks, block_size, num_kv_heads, head_dim], row-major, elements
+ *    bf16 or fp8-e4m3.  [LSB] "Block Tables, the Allocator & Copy-on-Write"
+ *    (BlockManager docstring); [PKV] "Implementation" (PagedKVCache).
+ *    Token slot s = phys_block * block_size + offset addresses row
+ *    s of the flat view [num_blocks * block_size, num_kv_heads, head_dim].
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID = 1,     /* a host-visible argument is malformed */
+  PA_ERR_OOM = 2,         /* the block pool has too few free blocks */
+  PA_ERR_CUDA = 3,        /* a CUDA launch or driver call failed */
+  PA_ERR_UNSUPPORTED = 4  /* valid, but a shape this build has no kernel for */
+} pa_status;
+
+typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
+
+/* Shape of one K (or V) cache tensor.  Supported: head_dim in {64, 128};
+ * block_size >= 1; num_kv_heads >= 1; dtype a pa_kv_dtype. */
+typedef struct {
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t dtype; /* pa_kv_dtype */
+} pa_cache_desc;
+
+/* cudaStream_t without the CUDA headers. */
+typedef struct CUstream_st* pa_stream_t;
+
+/* ------------------------------------------------------------------------
+ * pa_reshape_and_cache -- slot-mapped cache write.
+ * [PKV] "Implementation", PagedKVCache.write: token i's K/V go to slot
+ * slot_mapping[i] of the flat pool; [LSB] "From Python bookkeeping to the
+ * tensors the kernel actually takes" (one index copy over the flat pool).
+ *
+ *  key, value    device, [num_tokens, num_kv_heads, head_dim] bf16,
+ *                contiguous, 16-byte aligned.
+ *  k_cache, v_cache  device, layout above; written in place.
+ *  slot_mapping  device, [num_tokens] int32.  A negative slot skips the
+ *                token (padding).
+ *  k_scale, v_scale  device float scalars for PA_KV_FP8_E4M3 (the cache
+ *                holds e4m3(x / scale), x / scale in IEEE fp32, rounded to
+ *                nearest-even and saturated to +-448); must be NULL for bf16.
+ *  num_tokens == 0 is valid and launches nothing.
+ * ---------------------------------------------------------------------- */
+pa_status pa_reshape_and_cache(const void* key, const void* value,
+                               void* k_cache, void* v_cache,
+                               pa_cache_desc cache,
+                               const int32_t* slot_mapping, int32_t num_tokens,
+                               const float* k_scale, const float* v_scale,
+                               pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_decode_workspace_size -- bytes of scratch pa_decode needs for a call
+ * with these sizes (split-K partial results; 0 if none can be needed).
+ * Any workspace at least this large is accepted.
+ * ---------------------------------------------------------------------- */
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads,
+                                int32_t head_dim, int32_t max_blocks_per_seq,
+                                int32_t block_size);
+
+/* Workspace bytes for pa_decode_ex with an explicit split-K partition
+ * length (a power of two in [64, 65536]); 0 means the automatic choice. */
+size_t pa_decode_workspace_size_ex(int32_t num_seqs, int32_t num_heads,
+                                   int32_t head_dim,
+                                   int32_t max_blocks_per_seq,
+                                   int32_t block_size,
+                                   int32_t partition_tokens);
+
+/* Tuning knobs of pa_decode_ex.  Zero means "choose automatically". */
+typedef struct {
+  int32_t partition_tokens; /* split-K partition length: power of two >= 64 */
+  int32_t kernel;           /* 0 auto, 1 SIMT, 2 tensor-core (tcgen05) */
+} pa_decode_opts;
+
+/* ------------------------------------------------------------------------
+ * pa_decode -- decode-time paged attention, one query token per sequence.
+ * [LSB] "The PagedAttention Kernel" (online softmax over the sequence's
+ * blocks, GQA head map h -> h / G; a CTA per (sequence, KV head));
+ * [LSB] "Performance considerations" (split-K over the sequence, as in
+ * PagedAttention v2); [PKV] "Paged attention" (block_tables, seq_lens).
+ *
+ *  out           device, [num_seqs, num_heads, head_dim] bf16 (written):
+ *                out[i,h] = softmax(scale * q[i,h] . K_i[:, h/G]^T) V_i[:, h/G]
+ *                over the first context_lens[i] tokens of sequence i, in
+ *                fp32, rounded to nearest-even bf16.  context_lens[i] == 0
+ *                gives a zero row.
+ *  q             device, [num_seqs, num_heads, head_dim] bf16, contiguous.
+ *  block_tables  device, [num_seqs, max_blocks_per_seq] int32; entry j of
+ *                row i is the physical block of logical block j.  Entries
+ *                at or past ceil(context_lens[i] / block_size) are not read.
+ *  context_lens  device, [num_seqs] int32: valid tokens of each sequence
+ *                after this step's write (so pa_reshape_and_cache must run
+ *                first on the same stream); at most
+ *                max_blocks_per_seq * block_size.
+ *  num_heads     query heads; a multiple of cache.num_kv_heads, with
+ *                G = num_heads / num_kv_heads in {1, 2, 4, 8}.
+ *  scale         logit scale (typically 1/sqrt(head_dim)).
+ *  k_scale, v_scale  device float scalars for fp8 caches, NULL for bf16.
+ *  workspace     device scratch of at least pa_decode_workspace_size(...)
+ *                bytes, 256-byte aligned; its contents need no
+ *                initialisation and are clobbered.
+ * ---------------------------------------------------------------------- */
+pa_status pa_decode(void* out, const void* q, const void* k_cache,
+                    const void* v_cache, pa_cache_desc cache,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                    const int32_t* context_lens, int32_t num_seqs,
+                    int32_t num_heads, float scale, const float* k_scale,
+                    const float* v_scale, void* workspace,
+                    size_t workspace_bytes, pa_stream_t stream);
+
+/* pa_decode with explicit tuning knobs (opts may be NULL). */
+pa_status pa_decode_ex(void* out, const void* q, const void* k_cache,
+                       const void* v_cache, pa_cache_desc cache,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* context_lens, int32_t num_seqs,
+                       int32_t num_heads, float scale, const float* k_scale,
+                       const float* v_scale, void* workspace,
+                       size_t workspace_bytes, const pa_decode_opts* opts,
+                       pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_copy_blocks -- device side of copy-on-write: for each (src, dst) pair,
+ * k_cache[dst] = k_cache[src] and v_cache[dst] = v_cache[src], bit-exact.
+ * [LSB] "Copy-on-write for shared prefixes" (cow_append returns (src, dst);
+ * "kernel copies src->dst, then writes").
+ *
+ *  block_pairs   device, [num_pairs, 2] int32 (src, dst).  Pairs must not
+ *                chain (no dst of one pair is the src of another) and no dst
+ *                may repeat; the copies of one call run concurrently.
+ *  num_pairs == 0 is valid and launches nothing.
+ * ---------------------------------------------------------------------- */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, pa_cache_desc cache,
+                         const int32_t* block_pairs, int32_t num_pairs,
+                         pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_slot_mapping -- host-side slot computation for a step's new tokens.
+ * slot = table[pos / block_size] * block_size + pos % block_size.
+ * [LSB] BlockManager.slot_index; [PKV] slot_mapping_for; [ATC] "How the
+ * Block Table Works"; [PAE] "The Custom CUDA Kernel Overview".
+ *
+ *  block_tables  host, [num_seqs, max_blocks_per_seq] int32.
+ *  token_seq     host, [num_tokens] sequence index of each token, or NULL
+ *                meaning token i belongs to sequence i (decode).
+ *  token_pos     host, [num_tokens] logical position of each token.
+ *  slot_mapping  host, [num_tokens] int32 (written).
+ *  Returns PA_ERR_INVALID if a position or sequence index is out of range.
+ * ---------------------------------------------------------------------- */
+pa_status pa_slot_mapping(const int32_t* block_tables, int32_t num_seqs,
+                          int32_t max_blocks_per_seq, int32_t block_size,
+                          const int32_t* token_seq, const int32_t* token_pos,
+                          int32_t num_tokens, int32_t* slot_mapping);
+
+/* ------------------------------------------------------------------------
+ * Host-side block pool (off the hot path; not thread-safe: one owner).
+ * Free queue is FIFO: allocation takes from the head, blocks whose ref count
+ * drops to 0 join the tail.  [PKV] "Implementation" (BlockPool: deque free
+ * queue, ref counts, allocate returns None when short); [LSB] BlockManager
+ * (fork, cow_append, free_seq).  Allocation is all-or-nothing.
+ * ---------------------------------------------------------------------- */
+typedef struct pa_pool pa_pool;
+
+/* Pool of num_blocks blocks, free queue 0..num_blocks-1.  NULL on bad size
+ * or host OOM. */
+pa_pool* pa_pool_create(int32_t num_blocks);
+/* Pool whose initial free queue is `order` (a permutation of
+ * 0..num_blocks-1, copied).  NULL if order is not a permutation. */
+pa_pool* pa_pool_create_ordered(int32_t num_blocks, const int32_t* order);
+void pa_pool_destroy(pa_pool* pool);
+int32_t pa_pool_num_blocks(const pa_pool* pool);
+int32_t pa_pool_num_free(const pa_pool* pool);
+/* Ref count of a block, or -1 for an id outside the pool. */
+int32_t pa_pool_refcount(const pa_pool* pool, int32_t block);
+/* Copies the free queue, head first, into out[0..cap); returns its length. */
+int32_t pa_pool_free_order(const pa_pool* pool, int32_t* out, int32_t cap);
+/* Take n blocks from the head of the free queue (ref count 1 each) into
+ * out_blocks[0..n).  PA_ERR_OOM (state unchanged) if fewer than n are free. */
+pa_status pa_pool_alloc(pa_pool* pool, int32_t n, int32_t* out_blocks);
+/* Fork: ref count += 1 for each listed block.  PA_ERR_INVALID (state
+ * unchanged) if any block is outside the pool or free. */
+pa_status pa_pool_incref(pa_pool* pool, const int32_t* blocks, int32_t n);
+/* Release: ref count -= 1 for each listed block; blocks reaching 0 join the
+ * tail of the free queue in list order.  PA_ERR_INVALID (state unchanged)
+ * if the list would drive any ref count below 0. */
+pa_status pa_pool_free(pa_pool* pool, const int32_t* blocks, int32_t n);
+/* Copy-on-write decision before writing into `block`: ref count 1 gives
+ * *out_dst = block (write in place); ref count > 1 takes a fresh block,
+ * decrements the shared one and gives the fresh id (the caller copies
+ * block -> *out_dst with pa_copy_blocks and remaps its table).  PA_ERR_OOM
+ * (state unchanged) when no block is free; PA_ERR_INVALID for a free or
+ * out-of-range block. */
+pa_status pa_pool_cow(pa_pool* pool, int32_t block, int32_t* out_dst);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics.
+ * ---------------------------------------------------------------------- */
+const char* pa_status_string(pa_status status);
+/* Description of the last failure on the calling thread ("" if none). */
+const char* pa_last_error(void);
+/* Library version string, e.g. "0.1.0 sm_103a". */
+const char* pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,314 @@
+// C entry points: argument validation, launch configuration, dispatch.
+// The contract of every function is stated in include/pa.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "pa.h"
+#include "pa_host.h"
+#include "pa_kernels.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+constexpr int kAutoPartition = 512;     // default split-K partition (tokens)
+constexpr int kAutoPartitionMin = 256;  // smallest automatic choice
+constexpr int kMaxPartition = 65536;
+
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int ilog2(int64_t x) {
+  int r = 0;
+  while ((int64_t(1) << r) < x) ++r;
+  return r;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Workspace layout for a given partition length: partial accumulators
+// [S, H, P, D] fp32 then (m, l) pairs [S, H, P] at a 256-byte boundary.
+struct WorkspaceLayout {
+  int64_t parts = 0;
+  size_t o_bytes = 0;
+  size_t ml_offset = 0;
+  size_t total = 0;
+};
+
+WorkspaceLayout workspace_layout(int64_t num_seqs, int64_t num_heads, int64_t head_dim,
+                                 int64_t max_ctx, int64_t partition) {
+  WorkspaceLayout w;
+  w.parts = ceil_div(max_ctx, partition);
+  if (w.parts <= 1 || num_seqs <= 0 || num_heads <= 0) {
+    w.parts = w.parts < 1 ? 1 : w.parts;
+    return w;  // a single partition writes the output directly
+  }
+  w.o_bytes = (size_t)(num_seqs * num_heads * w.parts * head_dim) * sizeof(float);
+  w.ml_offset = align_up(w.o_bytes, 256);
+  w.total = w.ml_offset + (size_t)(num_seqs * num_heads * w.parts) * 2 * sizeof(float);
+  return w;
+}
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 152;
+  return n;
+}
+
+int auto_partition(int64_t num_seqs, int64_t num_kv_heads, int64_t max_ctx) {
+  // Split long contexts so that enough CTAs exist to fill the machine a few
+  // times over (short sequences stay in one partition and skip the combine).
+  int ps = kAutoPartition;
+  const int64_t want = 4LL * num_sms();
+  while (ps > kAutoPartitionMin && num_seqs * num_kv_heads * ceil_div(max_ctx, ps) < want)
+    ps /= 2;
+  return ps;
+}
+
+pa_status check_cache(const pa_cache_desc& c, const char* fn) {
+  char buf[192];
+  if (c.num_blocks <= 0 || c.block_size <= 0 || c.num_kv_heads <= 0 || c.head_dim <= 0) {
+    snprintf(buf, sizeof buf, "%s: cache sizes must be positive", fn);
+    return pa_fail(PA_ERR_INVALID, buf);
+  }
+  if (c.dtype != PA_KV_BF16 && c.dtype != PA_KV_FP8_E4M3) {
+    snprintf(buf, sizeof buf, "%s: unknown cache dtype %d", fn, c.dtype);
+    return pa_fail(PA_ERR_INVALID, buf);
+  }
+  if (c.head_dim != 64 && c.head_dim != 128) {
+    snprintf(buf, sizeof buf, "%s: head_dim %d unsupported (64 or 128)", fn, c.head_dim);
+    return pa_fail(PA_ERR_UNSUPPORTED, buf);
+  }
+  if (!is_pow2(c.block_size) || c.block_size > 1024) {
+    snprintf(buf, sizeof buf, "%s: block_size %d unsupported (power of two <= 1024)", fn,
+             c.block_size);
+    return pa_fail(PA_ERR_UNSUPPORTED, buf);
+  }
+  if ((int64_t)c.num_blocks * c.block_size > INT32_MAX) {
+    snprintf(buf, sizeof buf, "%s: num_blocks * block_size exceeds 2^31-1 slots", fn);
+    return pa_fail(PA_ERR_UNSUPPORTED, buf);
+  }
+  return PA_OK;
+}
+
+pa_status check_scales(const pa_cache_desc& c, const float* ks, const float* vs, const char* fn) {
+  char buf[160];
+  if (c.dtype == PA_KV_FP8_E4M3 && (!ks || !vs)) {
+    snprintf(buf, sizeof buf, "%s: fp8 cache needs k_scale and v_scale", fn);
+    return pa_fail(PA_ERR_INVALID, buf);
+  }
+  if (c.dtype == PA_KV_BF16 && (ks || vs)) {
+    snprintf(buf, sizeof buf, "%s: k_scale/v_scale must be NULL for a bf16 cache", fn);
+    return pa_fail(PA_ERR_INVALID, buf);
+  }
+  return PA_OK;
+}
+
+pa_status cuda_status(cudaError_t e, const char* fn) {
+  if (e == cudaSuccess) return PA_OK;
+  char buf[256];
+  snprintf(buf, sizeof buf, "%s: %s", fn, cudaGetErrorString(e));
+  return pa_fail(PA_ERR_CUDA, buf);
+}
+
+}  // namespace
+
+void pa_set_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
+pa_status pa_fail(pa_status st, const char* msg) {
+  pa_set_error(msg);
+  return st;
+}
+
+extern "C" {
+
+const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID: return "PA_ERR_INVALID";
+    case PA_ERR_OOM: return "PA_ERR_OOM";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+  }
+  return "PA_ERR_UNKNOWN";
+}
+
+const char* pa_last_error(void) { return g_last_error.c_str(); }
+
+const char* pa_version(void) { return "0.1.0 sm_103a"; }
+
+pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache,
+                               void* v_cache, pa_cache_desc cache,
+                               const int32_t* slot_mapping, int32_t num_tokens,
+                               const float* k_scale, const float* v_scale,
+                               pa_stream_t stream) {
+  const char* fn = "pa_reshape_and_cache";
+  pa_status st = check_cache(cache, fn);
+  if (st != PA_OK) return st;
+  if ((st = check_scales(cache, k_scale, v_scale, fn)) != PA_OK) return st;
+  if (num_tokens < 0) return pa_fail(PA_ERR_INVALID, "pa_reshape_and_cache: num_tokens < 0");
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping)
+    return pa_fail(PA_ERR_INVALID, "pa_reshape_and_cache: NULL pointer");
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 4))
+    return pa_fail(PA_ERR_INVALID, "pa_reshape_and_cache: misaligned pointer");
+  const int64_t num_slots = (int64_t)cache.num_blocks * cache.block_size;
+  return cuda_status(pa::launch_reshape_and_cache(key, value, k_cache, v_cache, num_slots,
+                                                  cache.num_kv_heads, cache.head_dim,
+                                                  cache.dtype == PA_KV_FP8_E4M3, slot_mapping,
+                                                  num_tokens, k_scale, v_scale,
+                                                  reinterpret_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+size_t pa_decode_workspace_size_ex(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                   int32_t max_blocks_per_seq, int32_t block_size,
+                                   int32_t partition_tokens) {
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
+      block_size <= 0)
+    return 0;
+  int64_t ps = partition_tokens > 0 ? partition_tokens : kAutoPartitionMin;
+  if (partition_tokens > 0 && (!is_pow2(ps) || ps < pa::kMinPartition || ps > kMaxPartition))
+    return 0;
+  const int64_t max_ctx = (int64_t)max_blocks_per_seq * block_size;
+  return workspace_layout(num_seqs, num_heads, head_dim, max_ctx, ps).total;
+}
+
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                int32_t max_blocks_per_seq, int32_t block_size) {
+  return pa_decode_workspace_size_ex(num_seqs, num_heads, head_dim, max_blocks_per_seq,
+                                     block_size, 0);
+}
+
+pa_status pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache,
+                       pa_cache_desc cache, const int32_t* block_tables,
+                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                       int32_t num_seqs, int32_t num_heads, float scale, const float* k_scale,
+                       const float* v_scale, void* workspace, size_t workspace_bytes,
+                       const pa_decode_opts* opts, pa_stream_t stream) {
+  const char* fn = "pa_decode";
+  char buf[224];
+  pa_status st = check_cache(cache, fn);
+  if (st != PA_OK) return st;
+  if ((st = check_scales(cache, k_scale, v_scale, fn)) != PA_OK) return st;
+  if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_heads <= 0)
+    return pa_fail(PA_ERR_INVALID, "pa_decode: bad num_seqs / max_blocks_per_seq / num_heads");
+  if (num_seqs == 0) return PA_OK;
+  if (num_seqs > 65535) return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: more than 65535 sequences");
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return pa_fail(PA_ERR_INVALID, "pa_decode: NULL pointer");
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return pa_fail(PA_ERR_INVALID, "pa_decode: misaligned pointer");
+  if (num_heads % cache.num_kv_heads != 0)
+    return pa_fail(PA_ERR_INVALID, "pa_decode: num_heads is not a multiple of num_kv_heads");
+  const int group = num_heads / cache.num_kv_heads;
+  if (group != 1 && group != 2 && group != 4 && group != 8) {
+    snprintf(buf, sizeof buf, "pa_decode: GQA group %d unsupported (1, 2, 4 or 8)", group);
+    return pa_fail(PA_ERR_UNSUPPORTED, buf);
+  }
+  if (!std::isfinite(scale)) return pa_fail(PA_ERR_INVALID, "pa_decode: scale is not finite");
+  const int64_t max_ctx = (int64_t)max_blocks_per_seq * cache.block_size;
+  if (max_ctx > INT32_MAX / 2)
+    return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: max_blocks_per_seq * block_size too large");
+  const int kernel = opts ? opts->kernel : 0;
+  if (kernel != 0 && kernel != 1) {
+    snprintf(buf, sizeof buf, "pa_decode: kernel %d not available in this build", kernel);
+    return pa_fail(PA_ERR_UNSUPPORTED, buf);
+  }
+
+  int ps = opts ? opts->partition_tokens : 0;
+  if (ps != 0 && (!is_pow2(ps) || ps < pa::kMinPartition || ps > kMaxPartition)) {
+    snprintf(buf, sizeof buf, "pa_decode: partition_tokens %d is not a power of two in [64, %d]",
+             ps, kMaxPartition);
+    return pa_fail(PA_ERR_INVALID, buf);
+  }
+  if (ps == 0) ps = auto_partition(num_seqs, cache.num_kv_heads, max_ctx);
+  const WorkspaceLayout wl = workspace_layout(num_seqs, num_heads, cache.head_dim, max_ctx, ps);
+  if (wl.total > 0) {
+    if (!workspace || workspace_bytes < wl.total) {
+      snprintf(buf, sizeof buf, "pa_decode: workspace of %zu bytes needed, %zu given", wl.total,
+               workspace ? workspace_bytes : (size_t)0);
+      return pa_fail(PA_ERR_INVALID, buf);
+    }
+    if (!aligned(workspace, 16)) return pa_fail(PA_ERR_INVALID, "pa_decode: misaligned workspace");
+  }
+  if (wl.parts > 65535)
+    return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: too many partitions for one grid");
+
+  pa::DecodeParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.ws_o = wl.total ? static_cast<float*>(workspace) : nullptr;
+  p.ws_ml = wl.total ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + wl.ml_offset)
+                     : nullptr;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.num_blocks = cache.num_blocks;
+  p.block_size = cache.block_size;
+  p.log2_block_size = ilog2(cache.block_size);
+  p.num_kv_heads = cache.num_kv_heads;
+  p.num_heads = num_heads;
+  p.max_blocks = max_blocks_per_seq;
+  p.partition_tokens = ps;
+  p.max_parts = (int32_t)wl.parts;
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cache.dtype == PA_KV_FP8_E4M3
+                      ? pa::launch_decode_simt_fp8(p, cache.head_dim, group, num_seqs, s)
+                      : pa::launch_decode_simt_bf16(p, cache.head_dim, group, num_seqs, s);
+  if (e != cudaSuccess) return cuda_status(e, fn);
+  if (wl.parts > 1) {
+    e = pa::launch_decode_reduce(p, cache.head_dim, num_seqs, s);
+    if (e != cudaSuccess) return cuda_status(e, "pa_decode (combine)");
+  }
+  return PA_OK;
+}
+
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    pa_cache_desc cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                    const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, float scale,
+                    const float* k_scale, const float* v_scale, void* workspace,
+                    size_t workspace_bytes, pa_stream_t stream) {
+  return pa_decode_ex(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                      context_lens, num_seqs, num_heads, scale, k_scale, v_scale, workspace,
+                      workspace_bytes, nullptr, stream);
+}
+
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, pa_cache_desc cache,
+                         const int32_t* block_pairs, int32_t num_pairs, pa_stream_t stream) {
+  const char* fn = "pa_copy_blocks";
+  pa_status st = check_cache(cache, fn);
+  if (st != PA_OK) return st;
+  if (num_pairs < 0) return pa_fail(PA_ERR_INVALID, "pa_copy_blocks: num_pairs < 0");
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !block_pairs)
+    return pa_fail(PA_ERR_INVALID, "pa_copy_blocks: NULL pointer");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_pairs, 4))
+    return pa_fail(PA_ERR_INVALID, "pa_copy_blocks: misaligned pointer");
+  const int64_t elem = cache.dtype == PA_KV_FP8_E4M3 ? 1 : 2;
+  const int64_t block_bytes =
+      (int64_t)cache.block_size * cache.num_kv_heads * cache.head_dim * elem;
+  return cuda_status(pa::launch_copy_blocks(k_cache, v_cache, block_bytes, cache.num_blocks,
+                                            block_pairs, num_pairs,
+                                            reinterpret_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+}  // extern "C"

@@ -1,0 +1,148 @@
+// Cache write (reshape_and_cache) and block copy (copy-on-write) kernels.
+//
+// reshape_and_cache: "Paged KV cache" (ai-infra-handbooks), PagedKVCache.write
+// -- row i of key/value [N, H_kv, d] lands in row slot_mapping[i] of the pool
+// viewed flat as [num_blocks*block_size, H_kv, d].  One thread moves one
+// 16-byte piece of input (8 bf16 elements); consecutive threads cover
+// consecutive pieces of a token's H_kv*d contiguous elements, so both the
+// read and the scattered write are fully coalesced per token.  For an e4m3
+// cache each element becomes e4m3_rne_satfinite(x / scale) with x / scale an
+// IEEE fp32 division (fp8 KV cache: "4.6 PagedAttention & KV-Cache Memory
+// Management", section "The libraries that implement this").
+//
+// copy_blocks: "4.6 PagedAttention & KV-Cache Memory Management", section
+// "Copy-on-write for shared prefixes" -- the device copies block src -> dst
+// before the diverging token is written.  Whole blocks are contiguous
+// (block_size*H_kv*d*b bytes), so the copy is a plain 16-byte vector memcpy.
+#include <cuda_bf16.h>
+
+#include "pa_device.cuh"
+#include "pa_kernels.cuh"
+
+namespace pa {
+
+namespace {
+
+__device__ __forceinline__ uint16_t e4m3x2_rn_sat(float lo, float hi) {
+  uint16_t r;
+  // the first source lands in the upper byte, the second in the lower byte
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(256)
+    reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                             void* __restrict__ k_cache, void* __restrict__ v_cache,
+                             int64_t num_slots, int pieces_per_token,
+                             const int32_t* __restrict__ slot_mapping, int num_tokens,
+                             const float* __restrict__ k_scale,
+                             const float* __restrict__ v_scale) {
+  const int64_t total = (int64_t)num_tokens * pieces_per_token;
+  float ks = 1.f, vs = 1.f;
+  if (FP8) {
+    ks = *k_scale;
+    vs = *v_scale;
+  }
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t tok = idx / pieces_per_token;
+    const int64_t r = idx - tok * pieces_per_token;
+    const int64_t slot = slot_mapping[tok];
+    if (slot < 0 || slot >= num_slots) continue;  // padding token or bad slot
+    const int64_t dst = slot * pieces_per_token + r;
+    const uint4 kv = key[idx];
+    const uint4 vv = value[idx];
+    if (!FP8) {
+      reinterpret_cast<uint4*>(k_cache)[dst] = kv;
+      reinterpret_cast<uint4*>(v_cache)[dst] = vv;
+    } else {
+      float kf[8], vf[8];
+      Unpack16<false>::run(kv, kf);
+      Unpack16<false>::run(vv, vf);
+      uint32_t kw[2], vw[2];
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const uint16_t k01 = e4m3x2_rn_sat(__fdiv_rn(kf[4 * w + 0], ks), __fdiv_rn(kf[4 * w + 1], ks));
+        const uint16_t k23 = e4m3x2_rn_sat(__fdiv_rn(kf[4 * w + 2], ks), __fdiv_rn(kf[4 * w + 3], ks));
+        const uint16_t v01 = e4m3x2_rn_sat(__fdiv_rn(vf[4 * w + 0], vs), __fdiv_rn(vf[4 * w + 1], vs));
+        const uint16_t v23 = e4m3x2_rn_sat(__fdiv_rn(vf[4 * w + 2], vs), __fdiv_rn(vf[4 * w + 3], vs));
+        kw[w] = (uint32_t)k01 | ((uint32_t)k23 << 16);
+        vw[w] = (uint32_t)v01 | ((uint32_t)v23 << 16);
+      }
+      reinterpret_cast<uint2*>(k_cache)[dst] = make_uint2(kw[0], kw[1]);
+      reinterpret_cast<uint2*>(v_cache)[dst] = make_uint2(vw[0], vw[1]);
+    }
+  }
+}
+
+constexpr int kCopyThreads = 256;
+constexpr int64_t kCopyChunk = 32 * 1024;  // bytes per CTA
+
+__global__ void __launch_bounds__(kCopyThreads)
+    copy_blocks_kernel(char* __restrict__ k_cache, char* __restrict__ v_cache,
+                       int64_t block_bytes, int num_blocks,
+                       const int32_t* __restrict__ pairs) {
+  const int pi = blockIdx.x;
+  char* base = blockIdx.y ? v_cache : k_cache;
+  const int src = pairs[2 * pi];
+  const int dst = pairs[2 * pi + 1];
+  if ((unsigned)src >= (unsigned)num_blocks || (unsigned)dst >= (unsigned)num_blocks) return;
+  const int64_t off = (int64_t)blockIdx.z * kCopyChunk;
+  if (off >= block_bytes) return;
+  const int64_t len = min(kCopyChunk, block_bytes - off) / 16;
+  const uint4* s = reinterpret_cast<const uint4*>(base + (int64_t)src * block_bytes + off);
+  uint4* d = reinterpret_cast<uint4*>(base + (int64_t)dst * block_bytes + off);
+  constexpr int U = 8;
+  for (int64_t j0 = 0; j0 < len; j0 += (int64_t)U * kCopyThreads) {
+    uint4 tmp[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t j = j0 + u * kCopyThreads + threadIdx.x;
+      if (j < len) tmp[u] = s[j];
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t j = j0 + u * kCopyThreads + threadIdx.x;
+      if (j < len) d[j] = tmp[u];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_reshape_and_cache(const void* key, const void* value,
+                                     void* k_cache, void* v_cache,
+                                     int64_t num_slots, int num_kv_heads,
+                                     int head_dim, bool fp8,
+                                     const int32_t* slot_mapping,
+                                     int num_tokens, const float* k_scale,
+                                     const float* v_scale,
+                                     cudaStream_t stream) {
+  const int ppt = num_kv_heads * head_dim / 8;  // 16-byte input pieces per token
+  const int64_t total = (int64_t)num_tokens * ppt;
+  const int threads = 256;
+  const int64_t blocks = (total + threads - 1) / threads;
+  const int grid = (int)(blocks < 65535 * 8 ? blocks : 65535 * 8);
+  if (fp8)
+    reshape_and_cache_kernel<true><<<grid, threads, 0, stream>>>(
+        static_cast<const uint4*>(key), static_cast<const uint4*>(value), k_cache, v_cache,
+        num_slots, ppt, slot_mapping, num_tokens, k_scale, v_scale);
+  else
+    reshape_and_cache_kernel<false><<<grid, threads, 0, stream>>>(
+        static_cast<const uint4*>(key), static_cast<const uint4*>(value), k_cache, v_cache,
+        num_slots, ppt, slot_mapping, num_tokens, k_scale, v_scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int64_t block_bytes,
+                               int num_blocks, const int32_t* pairs, int num_pairs,
+                               cudaStream_t stream) {
+  const int64_t chunks = (block_bytes + kCopyChunk - 1) / kCopyChunk;
+  dim3 grid(num_pairs, 2, (unsigned)chunks);
+  copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(
+      static_cast<char*>(k_cache), static_cast<char*>(v_cache), block_bytes, num_blocks, pairs);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,85 @@
+// Device-side helpers: element unpacking, async copies, small reductions.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace pa {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global->shared async copy; src_bytes == 0 zero-fills the
+// destination without reading global memory.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src,
+                                            uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// bf16 pair packed in a 32-bit word -> two floats (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Two e4m3 codes (low byte first) -> two floats (exact: e4m3 is a subset of f16).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(h2) : "h"(codes));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
+}
+
+// Unpack 16 bytes of cache row into floats: 8 bf16 or 16 e4m3 values.
+template <bool FP8>
+struct Unpack16;
+
+template <>
+struct Unpack16<false> {
+  static constexpr int kElems = 8;
+  __device__ __forceinline__ static void run(const uint4& v, float* f) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+  }
+};
+
+template <>
+struct Unpack16<true> {
+  static constexpr int kElems = 16;
+  __device__ __forceinline__ static void run(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 a = e4m3x2_to_float2(static_cast<uint16_t>(w[i] & 0xffffu));
+      float2 b = e4m3x2_to_float2(static_cast<uint16_t>(w[i] >> 16));
+      f[4 * i + 0] = a.x; f[4 * i + 1] = a.y;
+      f[4 * i + 2] = b.x; f[4 * i + 3] = b.y;
+    }
+  }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace pa

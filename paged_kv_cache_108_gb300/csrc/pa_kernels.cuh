@@ -1,0 +1,61 @@
+// Internal declarations of the library's kernels and their launch helpers.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace pa {
+
+constexpr int kSimtThreads = 128;  // threads per decode CTA (SIMT kernel)
+constexpr int kChunkTokens = 64;   // tokens staged per pipeline stage
+constexpr int kMinPartition = 64;  // split-K partitions are multiples of this
+
+// Everything a decode kernel needs; device pointers except where noted.
+struct DecodeParams {
+  void* out;                   // [S, H, D] bf16
+  const void* q;               // [S, H, D] bf16
+  const void* k_cache;         // [NB, B, Hkv, D]
+  const void* v_cache;
+  const int32_t* block_tables;  // [S, max_blocks]
+  const int32_t* context_lens;  // [S]
+  float* ws_o;                 // [S, H, max_parts, D] unnormalised partials
+  float2* ws_ml;               // [S, H, max_parts] (running max in log2 units, sum)
+  const float* k_scale;        // fp8 only
+  const float* v_scale;
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t log2_block_size;
+  int32_t num_kv_heads;
+  int32_t num_heads;
+  int32_t max_blocks;
+  int32_t partition_tokens;  // multiple of kChunkTokens
+  int32_t max_parts;         // partitions per sequence the grid covers
+  float scale_log2;          // scale * log2(e)
+};
+
+// Launch the SIMT decode kernel for head_dim D in {64, 128}, group G in
+// {1, 2, 4, 8}; grid (max_parts, num_kv_heads, num_seqs).
+cudaError_t launch_decode_simt_bf16(const DecodeParams& p, int head_dim, int group,
+                                    int num_seqs, cudaStream_t stream);
+cudaError_t launch_decode_simt_fp8(const DecodeParams& p, int head_dim, int group,
+                                   int num_seqs, cudaStream_t stream);
+// Launch the split-K combine kernel.
+cudaError_t launch_decode_reduce(const DecodeParams& p, int head_dim,
+                                 int num_seqs, cudaStream_t stream);
+
+cudaError_t launch_reshape_and_cache(const void* key, const void* value,
+                                     void* k_cache, void* v_cache,
+                                     int64_t num_slots, int num_kv_heads,
+                                     int head_dim, bool fp8,
+                                     const int32_t* slot_mapping,
+                                     int num_tokens, const float* k_scale,
+                                     const float* v_scale,
+                                     cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache,
+                               int64_t block_bytes, int num_blocks,
+                               const int32_t* pairs, int num_pairs,
+                               cudaStream_t stream);
+
+}  // namespace pa

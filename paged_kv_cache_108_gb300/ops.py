@@ -1,0 +1,126 @@
+"""Python binding of the C ABI for torch tensors (argument marshalling only).
+
+Every function forwards ``tensor.data_ptr()`` values, sizes and the current
+CUDA stream to libpa.so; all computation happens in the library's kernels.
+Names and argument order follow include/pa.h.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import CacheDesc, DecodeOpts, PA_KV_BF16, PA_KV_FP8_E4M3
+
+_FP8_DTYPES = (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8))
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, contiguous=True) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
+    """Descriptor of a [num_blocks, block_size, num_kv_heads, head_dim] cache."""
+    if k_cache.dim() != 4:
+        raise ValueError("cache must be [num_blocks, block_size, num_kv_heads, head_dim]")
+    if k_cache.dtype == torch.bfloat16:
+        dt = PA_KV_BF16
+    elif k_cache.dtype in _FP8_DTYPES:
+        dt = PA_KV_FP8_E4M3
+    else:
+        raise ValueError(f"cache dtype must be bfloat16 or float8_e4m3fn/uint8, got {k_cache.dtype}")
+    nb, bs, hkv, d = k_cache.shape
+    return CacheDesc(nb, bs, hkv, d, dt)
+
+
+def _scales(desc: CacheDesc, k_scale, v_scale):
+    if desc.dtype == PA_KV_BF16:
+        if k_scale is not None or v_scale is not None:
+            raise ValueError("k_scale/v_scale are only for fp8 caches")
+        return None, None
+    if k_scale is None or v_scale is None:
+        raise ValueError("fp8 caches need k_scale and v_scale (device float32 scalars)")
+    return (_dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32))
+
+
+def _same_cache(k_cache, v_cache):
+    if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise ValueError("k_cache and v_cache must have the same shape and dtype")
+
+
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, k_scale=None,
+                      v_scale=None, stream=None) -> None:
+    """Write key/value [N, H_kv, d] (bf16) into the caches at ``slot_mapping``."""
+    _same_cache(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    ks, vs = _scales(desc, k_scale, v_scale)
+    n = int(slot_mapping.numel())
+    _lib.check(_lib.lib().pa_reshape_and_cache(
+        _dev(key, "key", torch.bfloat16), _dev(value, "value", torch.bfloat16),
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), desc,
+        _dev(slot_mapping, "slot_mapping", torch.int32), n, ks, vs, _stream(stream)))
+
+
+def decode_workspace_size(num_seqs: int, num_heads: int, head_dim: int,
+                          max_blocks_per_seq: int, block_size: int,
+                          partition_tokens: int = 0) -> int:
+    return int(_lib.lib().pa_decode_workspace_size_ex(
+        num_seqs, num_heads, head_dim, max_blocks_per_seq, block_size, partition_tokens))
+
+
+def alloc_workspace(num_seqs, num_heads, head_dim, max_blocks_per_seq, block_size,
+                    partition_tokens=0, device=None) -> torch.Tensor:
+    """A caller-owned device workspace for ``decode`` (torch allocates it)."""
+    n = decode_workspace_size(num_seqs, num_heads, head_dim, max_blocks_per_seq, block_size,
+                              partition_tokens)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device or "cuda")
+
+
+def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, k_scale=None,
+           v_scale=None, workspace=None, partition_tokens=0, kernel=0, stream=None):
+    """Paged decode attention; writes ``out`` [B_s, H_q, d] bf16 and returns it."""
+    _same_cache(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    ks, vs = _scales(desc, k_scale, v_scale)
+    if q.dim() != 3 or out.shape != q.shape:
+        raise ValueError("q and out must both be [num_seqs, num_heads, head_dim]")
+    num_seqs, num_heads, _ = q.shape
+    if block_tables.dim() != 2 or block_tables.shape[0] != num_seqs:
+        raise ValueError("block_tables must be [num_seqs, max_blocks_per_seq]")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr = _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    opts = DecodeOpts(int(partition_tokens), int(kernel))
+    _lib.check(_lib.lib().pa_decode_ex(
+        _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), desc, _dev(block_tables, "block_tables", torch.int32),
+        int(block_tables.shape[1]), _dev(context_lens, "context_lens", torch.int32), num_seqs,
+        num_heads, ctypes.c_float(scale), ks, vs, ws_ptr, ws_bytes, ctypes.byref(opts),
+        _stream(stream)))
+    return out
+
+
+def copy_blocks(k_cache, v_cache, block_pairs, stream=None) -> None:
+    """cache[dst] = cache[src] for each (src, dst) row of ``block_pairs`` [n, 2] int32."""
+    _same_cache(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    n = int(block_pairs.shape[0]) if block_pairs.dim() == 2 else int(block_pairs.numel()) // 2
+    ptr = _dev(block_pairs, "block_pairs", torch.int32) if n > 0 else None
+    _lib.check(_lib.lib().pa_copy_blocks(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                                         desc, ptr, n, _stream(stream)))

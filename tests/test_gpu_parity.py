@@ -1,0 +1,154 @@
+"""GPU parity: the CUDA path against the fp64 oracle on the same seeded inputs.
+
+Cache writes and block copies must match bit for bit (the whole pool is
+compared, including slots that were never written); attention outputs must
+satisfy |gpu - oracle| <= 1e-2 + 2e-2 |oracle| for a bf16 cache and
+<= 6e-2 + 6e-2 |oracle| for an e4m3 cache (oracle run on the dequantised
+cache).  Slot mappings computed by the library must equal the oracle's.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import core as ocore
+from paged_kv_cache_108_gb300 import ops, synth
+
+from tests import harness
+
+pytestmark = pytest.mark.gpu
+
+requires_gpu = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")
+
+
+def _check_step(w, partition_tokens=0, kernel=0, units=None):
+    got = harness.product_step(w, partition_tokens=partition_tokens, kernel=kernel)
+    ref = harness.oracle_step(w, units=units)
+    assert np.array_equal(got["slots_ctx"], ref["slots_ctx"])
+    assert np.array_equal(got["slots_new"], ref["slots_new"])
+    assert np.array_equal(got["k_cache"], ref["k_cache"]), "K cache differs from the oracle's"
+    assert np.array_equal(got["v_cache"], ref["v_cache"]), "V cache differs from the oracle's"
+    mask = None
+    if units is not None:
+        G = w.num_heads // w.num_kv_heads
+        mask = np.zeros(got["out"].shape, dtype=bool)
+        for s, g in units:
+            mask[s, g * G:(g + 1) * G] = True
+    err = harness.assert_close(got["out"], ref["out"], w.kv_dtype == "fp8", mask)
+    return got, ref, err
+
+
+@requires_gpu
+def test_tiny_workload():
+    _check_step(synth.tiny())
+
+
+@requires_gpu
+@pytest.mark.parametrize("partition", [0, 64, 256, 1024])
+def test_llama8b_batch64(partition):
+    _check_step(synth.llama8b(), partition_tokens=partition)
+
+
+@requires_gpu
+def test_long_context_split_k():
+    _check_step(synth.longctx())
+
+
+@requires_gpu
+@pytest.mark.parametrize("block_size", [1, 16, 64, 256])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_block_size_and_precision_sweep(block_size, kv_dtype):
+    _check_step(synth.sweep(block_size, kv_dtype))
+
+
+@requires_gpu
+@pytest.mark.parametrize("hq,hkv,d", [(8, 8, 64), (16, 8, 128), (32, 4, 128), (16, 2, 64)])
+def test_head_configurations(hq, hkv, d):
+    lens = [1, 2, 15, 16, 17, 63, 64, 65, 200, 1000]
+    w = synth.make(f"heads-{hq}-{hkv}-{d}", lens, hq, hkv, d, 16, seed=77)
+    _check_step(w, partition_tokens=128)
+
+
+@requires_gpu
+def test_single_token_returns_v_exactly():
+    w = synth.make("n1", [1, 1, 1], 8, 2, 128, 16, seed=5)
+    got = harness.product_step(w)
+    # softmax over one token is 1, so the output is v itself (exact in bf16)
+    vnew = ocore.bf16_to_f64(w.v_new)
+    G = w.num_heads // w.num_kv_heads
+    assert np.array_equal(got["out"], np.repeat(vnew, G, axis=1))
+
+
+@requires_gpu
+def test_permutation_invariance_bit_identical():
+    lens = synth.llama8b_lengths(16)
+    a = synth.make("perm-a", lens, 32, 8, 128, 16, seed=11, num_blocks=2000)
+    b = synth.make("perm-b", lens, 32, 8, 128, 16, seed=11, num_blocks=2000)
+    # same data, different physical placement
+    rng = np.random.default_rng(99)
+    perm = rng.permutation(2000).astype(np.int32)
+    used = a.block_tables.copy()
+    mask = np.zeros_like(used, dtype=bool)
+    for i, n in enumerate(lens):
+        mask[i, :-(-n // 16)] = True
+    b.block_tables = np.where(mask, perm[used], 0).astype(np.int32)
+    oa = harness.product_step(a)["out"]
+    ob = harness.product_step(b)["out"]
+    assert np.array_equal(oa, ob)
+
+
+@requires_gpu
+def test_empty_context_and_padding_slots():
+    w = synth.make("edge", [0, 5, 0, 33], 8, 4, 64, 16, seed=21)
+    skip = np.array([False, False, False, True])
+    got = harness.product_step(w, skip_new=skip)
+    ref = harness.oracle_step(w, skip_new=skip)
+    assert np.array_equal(got["k_cache"], ref["k_cache"])
+    assert np.array_equal(got["v_cache"], ref["v_cache"])
+    assert np.all(got["out"][0] == 0) and np.all(got["out"][2] == 0)
+    harness.assert_close(got["out"], ref["out"], False)
+
+
+@requires_gpu
+def test_copy_blocks_bit_exact():
+    rng = np.random.default_rng(3)
+    for kv_dtype, shape in [("bf16", (40, 16, 8, 128)), ("fp8", (40, 16, 8, 128)),
+                            ("bf16", (9, 256, 2, 64))]:
+        dt = np.uint16 if kv_dtype == "bf16" else np.uint8
+        kc = rng.integers(0, np.iinfo(dt).max + 1, size=shape, dtype=dt)
+        vc = rng.integers(0, np.iinfo(dt).max + 1, size=shape, dtype=dt)
+        pairs = np.array([[3, 7], [0, 1], [5, shape[0] - 1]], dtype=np.int32)
+        dk = harness.to_dev_bits(kc, kv_dtype, "cuda")
+        dv = harness.to_dev_bits(vc, kv_dtype, "cuda")
+        ops.copy_blocks(dk, dv, torch.from_numpy(pairs).cuda())
+        ops.copy_blocks(dk, dv, torch.zeros((0, 2), dtype=torch.int32, device="cuda"))
+        ocore.copy_blocks(kc, vc, pairs)
+        torch.cuda.synchronize()
+        assert np.array_equal(harness.bits_from_dev(dk), kc)
+        assert np.array_equal(harness.bits_from_dev(dv), vc)
+
+
+@requires_gpu
+def test_invalid_arguments_launch_nothing():
+    from paged_kv_cache_108_gb300._lib import PaError
+    w = synth.tiny()
+    kc = harness.to_dev_bits(w.junk_k, "bf16", "cuda")
+    q = harness.to_dev_bits(w.q, "bf16", "cuda")
+    bt = torch.from_numpy(w.block_tables).cuda()
+    cl = torch.from_numpy(w.context_lens).cuda()
+    out = torch.full_like(q, 7.0)
+    with pytest.raises((PaError, ValueError)):  # fp8 scales given for a bf16 cache
+        ops.decode(out, q, kc, kc, bt, cl, 0.125, k_scale=torch.ones(1, device="cuda"),
+                   v_scale=torch.ones(1, device="cuda"))
+    with pytest.raises(PaError):  # partition length not a power of two
+        ops.decode(out, q, kc, kc, bt, cl, 0.125, partition_tokens=96)
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
+    w2 = synth.make("ws", [300, 20], 8, 2, 64, 16, seed=4)
+    kc2 = harness.to_dev_bits(w2.junk_k, "bf16", "cuda")
+    q2 = harness.to_dev_bits(w2.q, "bf16", "cuda")
+    out2 = torch.full_like(q2, 7.0)
+    with pytest.raises(PaError):  # a split needs a workspace
+        ops.decode(out2, q2, kc2, kc2, torch.from_numpy(w2.block_tables).cuda(),
+                   torch.from_numpy(w2.context_lens).cuda(), 0.125, partition_tokens=64)
+    torch.cuda.synchronize()
+    assert torch.all(out2 == 7.0)

@@ -24,12 +24,17 @@ def _native():
 
 
 def _impls():
-    impls = [("model", pool_model.BlockPoolModel, pool_model.SequenceTablesModel)]
+    impls = [("model", pool_model.BlockPoolModel, pool_model.SequenceTablesModel,
+              pool_model.slot_of)]
     try:
         npool = _native()
-        impls.append(("native", npool.BlockPool, npool.SequenceTables))
+
+        def native_slot(table, pos, block_size):
+            return int(npool.slot_mapping(np.asarray([table], dtype=np.int32), block_size, [pos])[0])
+
+        impls.append(("native", npool.BlockPool, npool.SequenceTables, native_slot))
     except Exception as e:  # noqa: BLE001 -- reported as a skip below
-        impls.append(pytest.param(("native", None, None),
+        impls.append(pytest.param(("native", None, None, None),
                                   marks=pytest.mark.skip(reason=f"native pool unavailable: {e}")))
     return impls
 
@@ -40,7 +45,7 @@ IDS = ["model", "native"]
 
 @pytest.mark.parametrize("impl", IMPLS, ids=IDS)
 def test_fifo_free_queue_and_slots(impl):
-    _, Pool, _ = impl
+    _, Pool, _, slot_fn = impl
     g = G["fifo_example"]
     pool = Pool(g["num_blocks"])
     table = pool.allocate(3)
@@ -49,13 +54,13 @@ def test_fifo_free_queue_and_slots(impl):
     pool.free(table)
     got = pool.allocate(g["third_alloc_n"])
     assert list(got) == g["third_alloc"]
-    slots = [pool_model.slot_of(got, p, g["slot_block_size"]) for p in range(g["slot_positions"])]
+    slots = [slot_fn(got, p, g["slot_block_size"]) for p in range(g["slot_positions"])]
     assert slots == g["slots"]
 
 
 @pytest.mark.parametrize("impl", IMPLS, ids=IDS)
 def test_round_robin_tables(impl):
-    _, Pool, _ = impl
+    _, Pool, _, _ = impl
     g = G["round_robin_tables"]
     pool = Pool(g["num_blocks"])
     B = g["block_size"]
@@ -69,7 +74,7 @@ def test_round_robin_tables(impl):
 
 @pytest.mark.parametrize("impl", IMPLS, ids=IDS)
 def test_block_boundary_grow_before_write(impl):
-    _, Pool, Seqs = impl
+    _, Pool, Seqs, _ = impl
     g = G["block_boundary"]
     B = g["block_size"]
     mgr = Seqs(Pool(g["num_blocks"]), B)
@@ -85,7 +90,7 @@ def test_block_boundary_grow_before_write(impl):
 
 @pytest.mark.parametrize("impl", IMPLS, ids=IDS)
 def test_growth_trace_with_injected_free_order(impl):
-    _, Pool, Seqs = impl
+    _, Pool, Seqs, _ = impl
     g = G["growth_trace"]
     B = g["block_size"]
     order = list(g["initial_table"]) + [g["next_free"]] + [b for b in range(16)
@@ -101,7 +106,7 @@ def test_growth_trace_with_injected_free_order(impl):
 
 @pytest.mark.parametrize("impl", IMPLS, ids=IDS)
 def test_can_allocate_all_or_nothing(impl):
-    _, Pool, _ = impl
+    _, Pool, _, _ = impl
     g = G["can_allocate"]
     for tokens, fits in g["cases"]:
         pool = Pool(g["num_blocks"])
@@ -114,7 +119,7 @@ def test_can_allocate_all_or_nothing(impl):
 
 @pytest.mark.parametrize("impl", IMPLS, ids=IDS)
 def test_fork_and_copy_on_write(impl):
-    _, Pool, Seqs = impl
+    _, Pool, Seqs, _ = impl
     B = 4
     pool = Pool(10)
     mgr = Seqs(pool, B)
@@ -136,7 +141,7 @@ def test_fork_and_copy_on_write(impl):
 
 @pytest.mark.parametrize("impl", IMPLS, ids=IDS)
 def test_exhaustion(impl):
-    _, Pool, Seqs = impl
+    _, Pool, Seqs, _ = impl
     pool = Pool(2)
     mgr = Seqs(pool, 4)
     mgr.allocate("a", 8)
