@@ -204,7 +204,7 @@ def cpu_baseline_oracle(step, budget_s=10.0):
     per_unit_bytes = {(i, g): int(w.context_lens[i]) * w.head_dim * 2 * 2 for i, g in units}
     chunk = max(threads, 32)
     at = 0
-    while t_total < budget_s and reps < 64:
+    while t_total < budget_s and reps < 100000:
         sel = units[at:at + chunk]
         if not sel:
             at = 0

@@ -105,7 +105,11 @@ def test_empty_context_and_padding_slots():
     assert np.array_equal(got["k_cache"], ref["k_cache"])
     assert np.array_equal(got["v_cache"], ref["v_cache"])
     assert np.all(got["out"][0] == 0) and np.all(got["out"][2] == 0)
-    harness.assert_close(got["out"], ref["out"], False)
+    # sequence 3's newest slot was skipped, so it still holds arbitrary bits:
+    # compare the sequences whose context is fully written
+    keep = np.zeros(got["out"].shape, dtype=bool)
+    keep[:3] = True
+    harness.assert_close(got["out"], ref["out"], False, keep)
 
 
 @requires_gpu
