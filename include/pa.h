@@ -158,6 +158,44 @@ pa_status pa_decode_ex(void* out, const void* q, const void* k_cache,
                        pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * pa_decode_noalloc -- pa_decode for callers that cannot provide scratch.
+ * The source pages have no counterpart to this entry point; it is a
+ * library convenience.
+ *
+ * pa_decode needs a caller-owned workspace for its split-K partial results.
+ * Some callers cannot hand out device memory at the call site: a plugin
+ * whose host application owns every device allocation, or a
+ * latency-critical serving loop that must not call cudaMalloc because
+ * cudaMalloc can synchronise the device.  This variant takes the same
+ * arguments minus the workspace and keeps the partials in a fixed array of
+ * PA_DECODE_NOALLOC_SCRATCH_BYTES bytes compiled into the library (every GPU
+ * that loads the library holds it until the process exits).  It allocates
+ * nothing and calls no allocating routine.
+ *
+ *  - Output and numerics are those of pa_decode; the split-K partition
+ *    length is the shortest power of two from 256 tokens whose partials fit.
+ *  - PA_ERR_UNSUPPORTED, with nothing launched, when the sizes need more
+ *    scratch than the array holds even with 65536-token partitions; use
+ *    pa_decode with a workspace then.
+ *  - The first call on each device looks up the array's device address
+ *    (with that device current) and caches it; make that first call before
+ *    any stream capture begins.
+ *  - All calls on a device share the one array, which keeps the last call's
+ *    contents (nothing in it has to start at zero).  Calls whose GPU work
+ *    overlaps -- e.g. issued on two streams without ordering -- race on the
+ *    array and give wrong results: order them on one stream.
+ * ---------------------------------------------------------------------- */
+#define PA_DECODE_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache,
+                            const void* v_cache, pa_cache_desc cache,
+                            const int32_t* block_tables,
+                            int32_t max_blocks_per_seq,
+                            const int32_t* context_lens, int32_t num_seqs,
+                            int32_t num_heads, float scale,
+                            const float* k_scale, const float* v_scale,
+                            pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * pa_copy_blocks -- device side of copy-on-write: for each (src, dst) pair,
  * k_cache[dst] = k_cache[src] and v_cache[dst] = v_cache[src], bit-exact.
  * [LSB] "Copy-on-write for shared prefixes" (cow_append returns (src, dst);
