@@ -182,7 +182,12 @@ size_t pa_decode_workspace_size_ex(int32_t num_seqs, int32_t num_heads, int32_t 
   if (partition_tokens > 0 && (!is_pow2(ps) || ps < pa::kMinPartition || ps > kMaxPartition))
     return 0;
   const int64_t max_ctx = (int64_t)max_blocks_per_seq * block_size;
-  return workspace_layout(num_seqs, num_heads, head_dim, max_ctx, ps).total;
+  size_t need = workspace_layout(num_seqs, num_heads, head_dim, max_ctx, ps).total;
+  if (head_dim == 128) {  // the tensor-core kernel may serve this shape
+    const size_t tc = pa::tc_workspace_bytes(num_seqs, num_heads, max_ctx, num_sms());
+    if (tc > need) need = tc;
+  }
+  return need;
 }
 
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
@@ -223,9 +228,43 @@ pa_status pa_decode_ex(void* out, const void* q, const void* k_cache, const void
   if (max_ctx > INT32_MAX / 2)
     return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: max_blocks_per_seq * block_size too large");
   const int kernel = opts ? opts->kernel : 0;
-  if (kernel != 0 && kernel != 1) {
+  if (kernel != 0 && kernel != 1 && kernel != 2) {
     snprintf(buf, sizeof buf, "pa_decode: kernel %d not available in this build", kernel);
     return pa_fail(PA_ERR_UNSUPPORTED, buf);
+  }
+
+  const bool fp8 = cache.dtype == PA_KV_FP8_E4M3;
+  const bool tc_ok = kernel != 1 && pa::tc_supported(cache.head_dim, group, fp8, num_seqs,
+                                                      cache.block_size);
+  if (kernel == 2 || (kernel == 0 && tc_ok)) {
+    if (!tc_ok)
+      return pa_fail(PA_ERR_UNSUPPORTED,
+                     "pa_decode: tensor-core kernel needs a bf16 cache, head_dim 128, "
+                     "block_size >= 8 and at most 1024 sequences");
+    const int nsm = num_sms();
+    const size_t need = pa::tc_workspace_bytes(num_seqs, num_heads, max_ctx, nsm);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) {
+      snprintf(buf, sizeof buf, "pa_decode: workspace of %zu bytes (256-byte aligned) needed",
+               need);
+      return pa_fail(PA_ERR_INVALID, buf);
+    }
+    pa::TcLaunch a{};
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.workspace = workspace;
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = cache.num_kv_heads;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = cache.num_blocks;
+    a.block_size = cache.block_size;
+    a.num_ctas = nsm;
+    a.scale = scale;
+    return cuda_status(pa::launch_decode_tc(a, reinterpret_cast<cudaStream_t>(stream)), fn);
   }
 
   int ps = opts ? opts->partition_tokens : 0;

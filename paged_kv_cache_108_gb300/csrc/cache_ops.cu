@@ -38,6 +38,8 @@ __global__ void __launch_bounds__(256)
                              const int32_t* __restrict__ slot_mapping, int num_tokens,
                              const float* __restrict__ k_scale,
                              const float* __restrict__ v_scale) {
+  // let a dependent decode kernel start its prologue while this one runs
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int64_t total = (int64_t)num_tokens * pieces_per_token;
   float ks = 1.f, vs = 1.f;
   if (FP8) {

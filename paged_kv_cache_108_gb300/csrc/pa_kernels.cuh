@@ -44,6 +44,23 @@ cudaError_t launch_decode_simt_fp8(const DecodeParams& p, int head_dim, int grou
 cudaError_t launch_decode_reduce(const DecodeParams& p, int head_dim,
                                  int num_seqs, cudaStream_t stream);
 
+// Tensor-core (tcgen05 + TMA) decode for a bf16 cache with head_dim 128.
+struct TcLaunch {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  void* workspace;  // >= tc_workspace_bytes(...)
+  int num_seqs, num_heads, num_kv_heads, max_blocks, num_blocks, block_size;
+  int num_ctas;     // persistent CTAs (one per SM)
+  float scale;
+};
+bool tc_supported(int head_dim, int group, bool fp8, int num_seqs, int block_size);
+size_t tc_workspace_bytes(int64_t num_seqs, int64_t num_heads, int64_t max_ctx, int num_ctas);
+cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream);
+
 cudaError_t launch_reshape_and_cache(const void* key, const void* value,
                                      void* k_cache, void* v_cache,
                                      int64_t num_slots, int num_kv_heads,

@@ -152,6 +152,26 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool a_mn_ma
          | ((uint32_t)(m >> 4) << 24);   // M / 16
 }
 
+// Warp-wide max of a float via the integer max reduction: the bit pattern
+// with the magnitude bits of negatives flipped orders like the float.
+__device__ __forceinline__ float warp_max_f32(float x) {
+  int k = __float_as_int(x);
+  k ^= (k >> 31) & 0x7fffffff;
+  int r;
+  asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;\n" : "=r"(r) : "r"(k));
+  r ^= (r >> 31) & 0x7fffffff;
+  return __int_as_float(r);
+}
+
+// Programmatic dependent launch: wait for the preceding grid's completion
+// and memory flush / let the dependent grid start launching.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 __device__ __forceinline__ void bar_sync_named(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -79,12 +79,19 @@ def product_step(w: synth.Workload, device="cuda", partition_tokens=0, kernel=0,
     cl = torch.from_numpy(w.context_lens).to(device)
     ws = ops.alloc_workspace(w.num_seqs, w.num_heads, w.head_dim, w.max_blocks, B,
                              partition_tokens, device=device)
+    # arbitrary bytes: the workspace needs no initialisation; word 0 is zeroed
+    # because the tensor-core kernel reports expired waits / bad ids there
+    ws.random_(0, 256)
+    ws[:4] = 0
     out = torch.empty_like(q)
     ops.decode(out, q, kc, vc, bt, cl, w.scale, ks, vs, ws, partition_tokens, kernel)
     torch.cuda.synchronize()
+    err = int(ws[:4].view(torch.int32).item()) if ws.numel() >= 4 else 0
     return {"out": out.float().cpu().numpy().astype(np.float64), "k_cache": bits_from_dev(kc),
             "v_cache": bits_from_dev(vc), "slots_ctx": slots_ctx, "slots_new": slots_new,
-            "dev": {"k_cache": kc, "v_cache": vc, "q": q, "bt": bt, "cl": cl, "ks": ks, "vs": vs}}
+            "err": err,
+            "dev": {"k_cache": kc, "v_cache": vc, "q": q, "bt": bt, "cl": cl, "ks": ks, "vs": vs,
+                    "ws": ws}}
 
 
 def oracle_step(w: synth.Workload, skip_new=None, decode=True, units=None):

@@ -85,11 +85,14 @@ def test_write_and_copy_reject_bad_arguments():
 
 def test_workspace_size():
     lib = _lib.lib()
-    # contexts that fit one partition need no workspace
-    assert lib.pa_decode_workspace_size(64, 32, 128, 16, 16) == 0
-    # 64 seqs x 32 heads x 14 partitions of 256 (3584 tokens max)
-    n = lib.pa_decode_workspace_size(64, 32, 128, 224, 16)
+    # head_dim 64 (SIMT kernel only): contexts within one partition need none
+    assert lib.pa_decode_workspace_size(64, 32, 64, 16, 16) == 0
+    # 64 seqs x 32 heads x 14 partitions of 256 tokens (3584 tokens max)
+    n = lib.pa_decode_workspace_size(64, 32, 64, 224, 16)
     parts = -(-224 * 16 // 256)
-    o = 64 * 32 * parts * 128 * 4
+    o = 64 * 32 * parts * 64 * 4
     assert n == -(-o // 256) * 256 + 64 * 32 * parts * 8
     assert lib.pa_decode_workspace_size_ex(64, 32, 128, 224, 16, 96) == 0  # bad partition
+    # head_dim 128 also covers the tensor-core kernel's per-CTA partials
+    n128 = lib.pa_decode_workspace_size(64, 32, 128, 224, 16)
+    assert n128 >= 2 * o and n128 >= 64 * 32 * 28 * 128 * 4 // 28

@@ -1,0 +1,114 @@
+"""GPU parity of the tensor-core (tcgen05 + TMA) decode kernel against the
+fp64 oracle, and agreement with the SIMT kernel.
+
+Same bars as tests/test_gpu_parity.py; additionally the kernel's error word
+(workspace word 0: an expired bounded wait or an out-of-range block id) must
+stay zero."""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_108_gb300 import synth
+from tests import harness
+
+pytestmark = pytest.mark.gpu
+
+requires_gpu = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")
+
+TC = 2
+
+
+def _check(w, **kw):
+    got = harness.product_step(w, kernel=TC, **kw)
+    assert got["err"] == 0, f"tensor-core kernel error word {got['err']}"
+    ref = harness.oracle_step(w)
+    assert np.array_equal(got["k_cache"], ref["k_cache"])
+    assert np.array_equal(got["v_cache"], ref["v_cache"])
+    return harness.assert_close(got["out"], ref["out"], False), got, ref
+
+
+@requires_gpu
+def test_tc_small_group_mix():
+    lens = [1, 2, 15, 16, 17, 127, 128, 129, 255, 256, 257, 1000]
+    w = synth.make("tc-small", lens, 32, 8, 128, 16, seed=31)
+    _check(w)
+
+
+@requires_gpu
+def test_tc_llama8b_batch64():
+    _check(synth.llama8b())
+
+
+@requires_gpu
+def test_tc_long_context():
+    _check(synth.longctx())
+
+
+@requires_gpu
+@pytest.mark.parametrize("block_size", [8, 16, 64, 256])
+def test_tc_block_sizes(block_size):
+    _check(synth.sweep(block_size, "bf16"))
+
+
+@requires_gpu
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (64, 8), (4, 2)])
+def test_tc_head_groups(hq, hkv):
+    lens = [3, 130, 700, 2000, 64, 1]
+    w = synth.make(f"tc-heads-{hq}-{hkv}", lens, hq, hkv, 128, 16, seed=41)
+    _check(w)
+
+
+@requires_gpu
+def test_tc_empty_sequences():
+    w = synth.make("tc-empty", [0, 300, 0, 5], 32, 8, 128, 16, seed=43)
+    err, got, ref = _check(w)
+    assert np.all(got["out"][0] == 0) and np.all(got["out"][2] == 0)
+
+
+@requires_gpu
+def test_tc_agrees_with_simt_and_is_permutation_invariant():
+    lens = synth.llama8b_lengths(16)
+    a = synth.make("perm-a", lens, 32, 8, 128, 16, seed=11, num_blocks=2000)
+    b = synth.make("perm-b", lens, 32, 8, 128, 16, seed=11, num_blocks=2000)
+    rng = np.random.default_rng(99)
+    perm = rng.permutation(2000).astype(np.int32)
+    mask = np.zeros_like(a.block_tables, dtype=bool)
+    for i, n in enumerate(lens):
+        mask[i, :-(-n // 16)] = True
+    b.block_tables = np.where(mask, perm[a.block_tables], 0).astype(np.int32)
+    oa = harness.product_step(a, kernel=TC)
+    ob = harness.product_step(b, kernel=TC)
+    assert oa["err"] == 0 and ob["err"] == 0
+    assert np.array_equal(oa["out"], ob["out"])
+    simt = harness.product_step(a, kernel=1)["out"]
+    harness.assert_close(oa["out"], simt, False)
+
+
+@requires_gpu
+def test_tc_workspace_shared_across_shapes_and_repeated_calls():
+    """One workspace serves calls of different shapes back to back (merge
+    counters of one shape land where another shape keeps partials), and a
+    repeated call gives bit-identical output."""
+    from paged_kv_cache_108_gb300 import ops
+    big = synth.longctx()
+    small = synth.make("tc-reuse", [5000, 300, 9000, 17], 32, 8, 128, 16, seed=47)
+    outs = {}
+    ws = None
+    for w in (big, small, big, small):
+        got = harness.product_step(w, kernel=TC)
+        assert got["err"] == 0
+        dev = got["dev"]
+        if ws is None:
+            ws = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+            ws.random_(0, 256)
+        ws[:4] = 0
+        out = torch.empty_like(dev["q"])
+        ops.decode(out, dev["q"], dev["k_cache"], dev["v_cache"], dev["bt"], dev["cl"], w.scale,
+                   workspace=ws, kernel=TC)
+        torch.cuda.synchronize()
+        assert int(ws[:4].view(torch.int32).item()) == 0
+        res = out.float().cpu().numpy().astype(np.float64)
+        assert np.array_equal(res, got["out"]), w.name
+        if w.name in outs:
+            assert np.array_equal(outs[w.name], res)
+        outs[w.name] = res
