@@ -105,7 +105,19 @@ size_t pa_decode_workspace_size_ex(int32_t num_seqs, int32_t num_heads,
                                    int32_t block_size,
                                    int32_t partition_tokens);
 
-/* Tuning knobs of pa_decode_ex.  Zero means "choose automatically". */
+/* Tuning knobs of pa_decode_ex.  Zero means "choose automatically".
+ *  kernel 1: SIMT kernel (CUDA cores, cp.async ring, fixed split-K
+ *            partitions of partition_tokens, separate combine kernel); serves
+ *            every supported shape.
+ *  kernel 2: tensor-core kernel (tcgen05 MMA, TMA loads, persistent CTAs that
+ *            each stream an equal share of 128-token chunks, in-kernel merge
+ *            of split units); needs a bf16 cache, head_dim 128, block_size
+ *            >= 8 and at most 1024 sequences, else PA_ERR_UNSUPPORTED.
+ *            partition_tokens is ignored.  It sets workspace word 0 (int32)
+ *            to a nonzero code if one of its bounded internal waits expired
+ *            or a block id was out of range; the library never clears that
+ *            word, so a caller that wants to check it zeroes it first.
+ *  kernel 0: kernel 2 where it applies, else kernel 1. */
 typedef struct {
   int32_t partition_tokens; /* split-K partition length: power of two >= 64 */
   int32_t kernel;           /* 0 auto, 1 SIMT, 2 tensor-core (tcgen05) */
@@ -137,7 +149,9 @@ typedef struct {
  *  k_scale, v_scale  device float scalars for fp8 caches, NULL for bf16.
  *  workspace     device scratch of at least pa_decode_workspace_size(...)
  *                bytes, 256-byte aligned; its contents need no
- *                initialisation and are clobbered.
+ *                initialisation and are clobbered.  One workspace may serve
+ *                successive calls of different shapes on one stream; calls
+ *                that share it must not overlap on the GPU.
  * ---------------------------------------------------------------------- */
 pa_status pa_decode(void* out, const void* q, const void* k_cache,
                     const void* v_cache, pa_cache_desc cache,

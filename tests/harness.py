@@ -128,3 +128,137 @@ def assert_close(got: np.ndarray, ref: np.ndarray, fp8: bool, mask=None):
             f"{int(bad.sum())} of {bad.size} outputs outside |g-r| <= {atol} + {rtol}|r|; "
             f"worst flat index {i}: got {g.ravel()[i]}, oracle {r.ravel()[i]}")
     return float(err.max()) if err.size else 0.0
+
+
+# ---------------------------------------------------------------- serving mix
+
+def serving_pool_size(mix: synth.ServingMix) -> int:
+    """Blocks for the serving mix with 20 % headroom (prefix blocks shared per
+    group, private suffix blocks, one copy-on-write block per sequence)."""
+    B = mix.block_size
+    shared = mix.num_groups * -(-mix.prefix_len // B)
+    private = sum(-(-(mix.prefix_len + int(s)) // B) - mix.prefix_len // B + 1
+                  for s in mix.suffix_lens)
+    return int(1.2 * (shared + private)) + 8
+
+
+def _serving_tables(mix: synth.ServingMix, tables, num_blocks):
+    """Build the serving state with `tables` (native or model bookkeeping):
+    per group a parent allocates the prefix and forks the rest of the group;
+    every sequence then takes its first divergent write at position
+    prefix_len (copy-on-write if that block is shared) and grows to its
+    context length.  Returns the (src, dst) copy pairs in order and each
+    group's prefix table as it was when the prefix was written (before any
+    copy-on-write remapped the parent's last shared block)."""
+    G, P, B = mix.group_size, mix.prefix_len, mix.block_size
+    pairs, prefix_tables = [], []
+    for grp in range(mix.num_groups):
+        parent = grp * G
+        tables.allocate(parent, P)
+        prefix_tables.append(list(tables.tables[parent]))
+        for c in range(1, G):
+            tables.fork(parent, parent + c)
+    for i in range(mix.num_seqs):
+        n = P + int(mix.suffix_lens[i])
+        tables.append_token(i, P)
+        src, dst = tables.cow_for_write(i, P)
+        if src != dst:
+            pairs.append((src, dst))
+        for pos in range(P + 1, n):
+            tables.append_token(i, pos)
+    return pairs, prefix_tables
+
+
+def serving_lengths(mix):
+    return (mix.prefix_len + mix.suffix_lens).astype(np.int32)
+
+
+def _serving_writes(mix, table_arr, prefix_tables, slot_fn):
+    """(slots of prefix tokens, slots of suffix context tokens, slots of the
+    step's new tokens) in the order the context rows are consumed: each
+    group's prefix through its table at prefix time, then each sequence's
+    suffix positions prefix..n-2, then position n-1 of every sequence."""
+    P = mix.prefix_len
+    n = serving_lengths(mix)
+    pre = [slot_fn(prefix_tables[g], p) for g in range(mix.num_groups) for p in range(P)]
+    suf = [slot_fn(table_arr[i], p) for i in range(mix.num_seqs) for p in range(P, int(n[i]) - 1)]
+    new = [slot_fn(table_arr[i], int(n[i]) - 1) for i in range(mix.num_seqs)]
+    return (np.array(pre, np.int32), np.array(suf, np.int32), np.array(new, np.int32))
+
+
+def serving_unique_tokens(mix):
+    n = serving_lengths(mix)
+    return mix.num_groups * mix.prefix_len + int(np.sum(n - 1 - mix.prefix_len))
+
+
+def serving_product(mix, data, num_blocks, device="cuda", kernel=0):
+    """Product path: native pool and tables, cache writes, copy-on-write copies
+    and decode on the GPU.  The prefix is written before the copies (it was
+    computed before the fork); the suffix and the new token after them."""
+    npool = pool.BlockPool(num_blocks, free_order=mix.free_order(num_blocks))
+    tabs = pool.SequenceTables(npool, mix.block_size)
+    pairs, prefix_tables = _serving_tables(mix, tabs, num_blocks)
+    bt = tabs.block_table_array(list(range(mix.num_seqs)))
+    B = mix.block_size
+    # one native slot-mapping call per kind of write
+    n = serving_lengths(mix)
+    P = mix.prefix_len
+    pt = np.array(prefix_tables, dtype=np.int32)
+    pre_seq = np.repeat(np.arange(mix.num_groups), P).astype(np.int32)
+    pre_pos = np.tile(np.arange(P), mix.num_groups).astype(np.int32)
+    suf_seq = np.concatenate([np.full(int(n[i]) - 1 - P, i, np.int32) for i in range(mix.num_seqs)])
+    suf_pos = np.concatenate([np.arange(P, int(n[i]) - 1, dtype=np.int32) for i in range(mix.num_seqs)])
+    s_pre = pool.slot_mapping(pt, B, pre_pos, pre_seq)
+    s_suf = pool.slot_mapping(bt, B, suf_pos, suf_seq)
+    s_new = pool.slot_mapping(bt, B, n - 1, np.arange(mix.num_seqs, dtype=np.int32))
+    kc = to_dev_bits(data["junk_k"], "bf16", device)
+    vc = to_dev_bits(data["junk_v"], "bf16", device)
+    npre = s_pre.size
+    ck, cv = data["ctx_k"], data["ctx_v"]
+    ops.reshape_and_cache(to_dev_bits(ck[:npre], "bf16", device), to_dev_bits(cv[:npre], "bf16", device),
+                          kc, vc, torch.from_numpy(s_pre).to(device))
+    pr = np.array(pairs, dtype=np.int32).reshape(-1, 2)
+    ops.copy_blocks(kc, vc, torch.from_numpy(pr).to(device))
+    ops.reshape_and_cache(to_dev_bits(ck[npre:], "bf16", device), to_dev_bits(cv[npre:], "bf16", device),
+                          kc, vc, torch.from_numpy(s_suf).to(device))
+    ops.reshape_and_cache(to_dev_bits(data["k_new"], "bf16", device),
+                          to_dev_bits(data["v_new"], "bf16", device), kc, vc,
+                          torch.from_numpy(s_new).to(device))
+    q = to_dev_bits(data["q"], "bf16", device)
+    bt_d = torch.from_numpy(bt).to(device)
+    cl = torch.from_numpy(n).to(device)
+    ws = ops.alloc_workspace(mix.num_seqs, mix.num_heads, mix.head_dim, bt.shape[1], B, device=device)
+    ws.random_(0, 256)
+    ws[:4] = 0
+    out = torch.empty_like(q)
+    ops.decode(out, q, kc, vc, bt_d, cl, mix.head_dim ** -0.5, workspace=ws, kernel=kernel)
+    torch.cuda.synchronize()
+    return {"tables": bt, "pairs": pr, "slots": (s_pre, s_suf, s_new),
+            "k_cache": bits_from_dev(kc), "v_cache": bits_from_dev(vc),
+            "out": out.float().cpu().numpy().astype(np.float64),
+            "err": int(ws[:4].view(torch.int32).item())}
+
+
+def serving_oracle(mix, data, num_blocks, decode=True):
+    mpool = pool_model.BlockPoolModel(num_blocks, free_order=list(mix.free_order(num_blocks)))
+    tabs = pool_model.SequenceTablesModel(mpool, mix.block_size)
+    pairs, prefix_tables = _serving_tables(mix, tabs, num_blocks)
+    width = max(len(t) for t in tabs.tables.values())
+    bt = np.zeros((mix.num_seqs, width), dtype=np.int32)
+    for i in range(mix.num_seqs):
+        bt[i, :len(tabs.tables[i])] = tabs.tables[i]
+    s_pre, s_suf, s_new = _serving_writes(
+        mix, bt, prefix_tables, lambda row, p: pool_model.slot_of(row, p, mix.block_size))
+    kc, vc = data["junk_k"].copy(), data["junk_v"].copy()
+    npre = s_pre.size
+    ocore.reshape_and_cache(data["ctx_k"][:npre], data["ctx_v"][:npre], kc, vc, s_pre)
+    pr = np.array(pairs, dtype=np.int32).reshape(-1, 2)
+    ocore.copy_blocks(kc, vc, pr)
+    ocore.reshape_and_cache(data["ctx_k"][npre:], data["ctx_v"][npre:], kc, vc, s_suf)
+    ocore.reshape_and_cache(data["k_new"], data["v_new"], kc, vc, s_new)
+    res = {"tables": bt, "pairs": pr, "slots": (s_pre, s_suf, s_new), "k_cache": kc,
+           "v_cache": vc}
+    if decode:
+        res["out"] = ocore.decode(data["q"], kc, vc, bt, serving_lengths(mix),
+                                  mix.head_dim ** -0.5, nthreads=os.cpu_count() or 1)
+    return res
