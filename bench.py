@@ -4,9 +4,9 @@ Workload (the headline configuration): 64 sequences, 32 query / 8 KV heads,
 head_dim 128, bf16 cache, block size 16; context lengths are prompt + output
 of the first 64 requests of the seeded request mix (sum 121,416 tokens,
 732..3360); blocks are a seeded permutation of a pool 1.2x the blocks used.
-One step = the host slot mapping of the 64 new tokens, the cache write of
-their K/V (pa_reshape_and_cache) and paged decode over all 64 sequences
-(pa_decode: paged-decode kernel + split-K combine).
+One step = the host slot mapping of the 64 new tokens, then one library call
+(pa_write_and_decode): the cache write of their K/V and paged decode over
+all 64 sequences.  The decode call alone and the write alone are also timed.
 
 Metric: achieved HBM GB/s on the algorithmic bytes a step must move
 (K and V of every context token once, q, out, block-table entries, lengths,
@@ -82,8 +82,11 @@ class Step:
         self.context_lens = torch.from_numpy(w.context_lens).to(device)
         self.out = torch.empty_like(self.q)
         self.ws = ops.alloc_workspace(S, H, d, w.max_blocks, B, partition, device=device)
-        self.splits = ops.decode_workspace_size(S, H, d, w.max_blocks, B, partition) > 0
-        self.launches_per_step = 2 + (1 if self.splits else 0)
+        # the tensor-core decode (one launch, merge inside) serves this shape
+        # unless the SIMT kernel is forced; SIMT adds a combine launch
+        simt = kernel == 1
+        splits = 3360 > (partition or 256)
+        self.launches_per_step = 2 + (1 if simt and splits else 0)
 
     # algorithmic bytes of one step (what the method must move)
     def decode_bytes(self) -> int:
@@ -100,6 +103,16 @@ class Step:
     def run_write(self, slots=None, k=None, v=None):
         self.ops.reshape_and_cache(self.k_new if k is None else k, self.v_new if v is None else v,
                                    self.k_cache, self.v_cache, self.slots if slots is None else slots)
+
+    def run_step(self, slots=None, k=None, v=None, q=None, bt=None, cl=None):
+        """The step as one call: cache write of the new tokens, then decode."""
+        w = self.w
+        self.ops.write_and_decode(self.k_new if k is None else k, self.v_new if v is None else v,
+                                  self.slots if slots is None else slots, self.out,
+                                  self.q if q is None else q, self.k_cache, self.v_cache,
+                                  self.block_tables if bt is None else bt,
+                                  self.context_lens if cl is None else cl, w.scale,
+                                  workspace=self.ws)
 
     def run_decode(self, q=None, bt=None, cl=None):
         w = self.w
@@ -244,33 +257,47 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as dist
 
     def one_step():
-        step.run_write()
-        step.run_decode()
+        if step.kernel == 0:
+            step.run_step()
+        else:  # a forced kernel choice goes through the separate calls
+            step.run_write()
+            step.run_decode()
 
     for _ in range(max(args.warmup, 3)):
         one_step()
+        step.run_decode()
     torch.cuda.synchronize()
 
-    # device-resident timing: per step events around write, decode
+    # device-resident timing.  Loop 1 times the step (value); loop 2 times
+    # the decode call alone (roofline of the dominant kernel); loop 3 the
+    # cache write alone.  Each timed call follows an untimed L2 flush.
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
         for k in range(K):
-            flush_l2()  # outside the timed events
+            flush_l2()
             ev[k][0].record(stream)
-            step.run_write()
+            one_step()
             ev[k][1].record(stream)
-            step.run_decode()
+        for k in range(K):
+            flush_l2()
             ev[k][2].record(stream)
+            step.run_decode()
+            ev[k][3].record(stream)
+        for k in range(K):
+            flush_l2()
+            ev[k][4].record(stream)
+            step.run_write()
+            ev[k][5].record(stream)
         torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    step_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(K)]
-    dec_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
-    wr_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    step_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    dec_ms = [ev[k][2].elapsed_time(ev[k][3]) for k in range(K)]
+    wr_ms = [ev[k][4].elapsed_time(ev[k][5]) for k in range(K)]
     mean_step = sum(step_ms) / K
     mean_dec = sum(dec_ms) / K
     t = torch.tensor([mean_step, mean_dec], dtype=torch.float64, device=device)
@@ -317,12 +344,12 @@ def run_ours(args, rank, world, local_rank):
         "us_write": round(sum(wr_ms) / K * 1e3, 2),
         "tokens_per_s": round(world * w.num_seqs / (mean_step * 1e-3), 1),
         "pct_of_nominal_8tbps": round(100 * achieved / 8000.0, 1),
-        "roofline": {"bound": "hbm", "kernel": "pa_decode (paged decode + split-K combine)",
+        "roofline": {"bound": "hbm", "kernel": "pa_decode alone (tcgen05 paged decode; split units merged in-kernel)",
                      "achieved": round(achieved, 2), "peak": peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic(dbytes),
                      "algorithmic_bytes": dbytes},
-        "gpu_launches": K * step.launches_per_step,
+        "gpu_launches": K * 2 * step.launches_per_step,
         "clocks": clk.summary(),
     }
     if e2e is not None:
@@ -355,8 +382,11 @@ def run_e2e(step, args, device, dist):
         for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_bt, h_bt), (d_cl, h_cl),
                      (d_slots, h_slots)):
             d.copy_(h, non_blocking=True)
-        step.run_write(d_slots, d_k, d_v)
-        step.run_decode(d_q, d_bt, d_cl)
+        if step.kernel == 0:
+            step.run_step(d_slots, d_k, d_v, d_q, d_bt, d_cl)
+        else:
+            step.run_write(d_slots, d_k, d_v)
+            step.run_decode(d_q, d_bt, d_cl)
         h_out.copy_(step.out, non_blocking=True)
         torch.cuda.current_stream().synchronize()  # the host reads the result
 

@@ -172,6 +172,31 @@ pa_status pa_decode_ex(void* out, const void* q, const void* k_cache,
                        pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * pa_write_and_decode -- one decode step: pa_reshape_and_cache of the new
+ * tokens followed by pa_decode, in one call.  [LSB] "Putting It Together: A
+ * Minimal Paged Serving Loop" (serve_step: write the token's K/V at its
+ * slot, then attend over the sequence's blocks).
+ *
+ * Arguments are those of the two calls (num_tokens new tokens; decode with
+ * the automatic kernel choice).  Because the library itself launches the
+ * write just before the decode, the tensor-core decode kernel starts while
+ * the write still runs and reads lengths, block tables and q at once; it
+ * waits for the write only before its first cache read.  Results are those
+ * of the two separate calls.
+ * ---------------------------------------------------------------------- */
+pa_status pa_write_and_decode(const void* key, const void* value,
+                              const int32_t* slot_mapping, int32_t num_tokens,
+                              void* out, const void* q, void* k_cache,
+                              void* v_cache, pa_cache_desc cache,
+                              const int32_t* block_tables,
+                              int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, int32_t num_seqs,
+                              int32_t num_heads, float scale,
+                              const float* k_scale, const float* v_scale,
+                              void* workspace, size_t workspace_bytes,
+                              pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * pa_decode_noalloc -- pa_decode for callers that cannot provide scratch.
  * The source pages have no counterpart to this entry point; it is a
  * library convenience.

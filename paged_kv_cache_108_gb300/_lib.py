@@ -58,6 +58,8 @@ SIGNATURES = {
                            P, SIZE, ctypes.POINTER(DecodeOpts), P]),
     "pa_decode_noalloc": (I32, [P, P, P, P, CacheDesc, P, I32, P, I32, I32, ctypes.c_float, P,
                                 P, P]),
+    "pa_write_and_decode": (I32, [P, P, P, I32, P, P, P, P, CacheDesc, P, I32, P, I32, I32,
+                                  ctypes.c_float, P, P, P, SIZE, P]),
     "pa_copy_blocks": (I32, [P, P, CacheDesc, P, I32, P]),
     "pa_slot_mapping": (I32, [PI32, I32, I32, I32, PI32, PI32, I32, PI32]),
     "pa_pool_create": (P, [I32]),

@@ -196,12 +196,19 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t hea
                                      block_size, 0);
 }
 
-pa_status pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache,
-                       pa_cache_desc cache, const int32_t* block_tables,
-                       int32_t max_blocks_per_seq, const int32_t* context_lens,
-                       int32_t num_seqs, int32_t num_heads, float scale, const float* k_scale,
-                       const float* v_scale, void* workspace, size_t workspace_bytes,
-                       const pa_decode_opts* opts, pa_stream_t stream) {
+}  // extern "C"
+
+// pa_decode_ex's body.  prev_writes_cache_only: the kernel launched just
+// before on `stream` is this library's cache write, so the tensor-core
+// kernel may read its metadata (lengths, tables, q) while that write is still
+// running and wait for it only before its first cache read.
+static pa_status decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                             pa_cache_desc cache, const int32_t* block_tables,
+                             int32_t max_blocks_per_seq, const int32_t* context_lens,
+                             int32_t num_seqs, int32_t num_heads, float scale,
+                             const float* k_scale, const float* v_scale, void* workspace,
+                             size_t workspace_bytes, const pa_decode_opts* opts,
+                             pa_stream_t stream, bool prev_writes_cache_only) {
   const char* fn = "pa_decode";
   char buf[224];
   pa_status st = check_cache(cache, fn);
@@ -264,6 +271,7 @@ pa_status pa_decode_ex(void* out, const void* q, const void* k_cache, const void
     a.block_size = cache.block_size;
     a.num_ctas = nsm;
     a.scale = scale;
+    a.early_meta = prev_writes_cache_only;
     return cuda_status(pa::launch_decode_tc(a, reinterpret_cast<cudaStream_t>(stream)), fn);
   }
 
@@ -318,6 +326,34 @@ pa_status pa_decode_ex(void* out, const void* q, const void* k_cache, const void
     if (e != cudaSuccess) return cuda_status(e, "pa_decode (combine)");
   }
   return PA_OK;
+}
+
+extern "C" {
+
+pa_status pa_decode_ex(void* out, const void* q, const void* k_cache, const void* v_cache,
+                       pa_cache_desc cache, const int32_t* block_tables,
+                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                       int32_t num_seqs, int32_t num_heads, float scale, const float* k_scale,
+                       const float* v_scale, void* workspace, size_t workspace_bytes,
+                       const pa_decode_opts* opts, pa_stream_t stream) {
+  return decode_impl(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_heads, scale, k_scale, v_scale, workspace,
+                     workspace_bytes, opts, stream, false);
+}
+
+pa_status pa_write_and_decode(const void* key, const void* value, const int32_t* slot_mapping,
+                              int32_t num_tokens, void* out, const void* q, void* k_cache,
+                              void* v_cache, pa_cache_desc cache, const int32_t* block_tables,
+                              int32_t max_blocks_per_seq, const int32_t* context_lens,
+                              int32_t num_seqs, int32_t num_heads, float scale,
+                              const float* k_scale, const float* v_scale, void* workspace,
+                              size_t workspace_bytes, pa_stream_t stream) {
+  pa_status st = pa_reshape_and_cache(key, value, k_cache, v_cache, cache, slot_mapping,
+                                      num_tokens, k_scale, v_scale, stream);
+  if (st != PA_OK) return st;
+  return decode_impl(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                     context_lens, num_seqs, num_heads, scale, k_scale, v_scale, workspace,
+                     workspace_bytes, nullptr, stream, num_tokens > 0);
 }
 
 pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,

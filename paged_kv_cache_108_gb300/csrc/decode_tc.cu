@@ -19,14 +19,16 @@
 // word at (epoch, 0), so replaying the same launch also starts from zero.
 // Load balance is one chunk, whatever the mix of context lengths.
 //
-// Warp roles (192 threads):
+// Warp roles (224 threads):
 //   warps 0-3  softmax + epilogue: thread t owns TMEM lane t (a token of the
 //              logits tile, a d-element of the output tile);
 //   warp 4     producer: per chunk, TMA tensor loads of each physical block's
 //              K and V rows (4-D tensor map [blocks, block_size, H_kv, d],
 //              128-byte swizzle, two 64-column halves) into a 3-stage ring,
 //              and per segment a TMA load of the group's query rows;
-//   warp 5     TMEM allocation and the single MMA-issuing thread.
+//   warp 5     TMEM allocation and the single MMA-issuing thread;
+//   warp 6     merge warp: counts finished pieces of split units and merges
+//              a unit's pieces when its last piece is done.
 //
 // Per chunk c (double-buffered TMEM tiles S[c&1], O[c&1] and smem P[c&1]):
 //   S = K_c q^T         tcgen05.mma M=128 tokens, N=16 (query heads padded),
@@ -68,7 +70,7 @@ constexpr int TILE_B = CH * D * 2;     // 32 KiB: one K or V chunk
 constexpr int HALF_B = CH * 128;       // 16 KiB: one 64-column half of a tile
 constexpr int QTILE_B = NQ * D * 2;    // 4 KiB
 constexpr int PTILE_B = NQ * CH * 2;   // 4 KiB
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 224;
 constexpr int TMEM_COLS = 64;          // S[2] x 16 + O[2] x 16 columns
 
 constexpr int OFF_K = 0;
@@ -79,15 +81,15 @@ constexpr int OFF_BAR = OFF_P + 2 * PTILE_B;
 // barrier indices
 constexpr int B_FULL_K = 0, B_FULL_V = 3, B_EMPTY = 6, B_S_FULL = 9, B_S_EMPTY = 11,
               B_P_FULL = 13, B_P_EMPTY = 15, B_O_FULL = 17, B_O_EMPTY = 19, B_Q_FULL = 21,
-              B_Q_EMPTY = 23, NBARS = 25;
+              B_Q_EMPTY = 23, B_EPI = 25, NBARS = 27;
 constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 4;
-constexpr int OFF_MERGE = OFF_ABORT + 4;   // "this CTA merges the unit" flag
 constexpr int OFF_RED = OFF_ABORT + 12;      // [2][4][8] floats, chunk max
 constexpr int OFF_LRED = OFF_RED + 2 * 4 * 8 * 4;  // [4][8] floats, epilogue sums
 constexpr int OFF_CP = OFF_LRED + 4 * 8 * 4;       // chunk prefix per sequence, [S+1] int
 constexpr int kMaxSeqs = 1024;
-constexpr int SMEM_BYTES = OFF_CP + (kMaxSeqs + 1) * 4 + 1024;  // + alignment slack
+constexpr int OFF_NLEN = OFF_CP + (kMaxSeqs + 1) * 4;  // clamped context length per sequence
+constexpr int SMEM_BYTES = OFF_NLEN + kMaxSeqs * 4 + 1024;  // + alignment slack
 
 constexpr long long kWaitClocks = 1LL << 31;
 
@@ -103,6 +105,7 @@ struct Params {
   int num_ctas, max_seg, box_tok, log2_box;
   float scale_log2;
   unsigned long long epoch;  // 48-bit tag of this call
+  int early_meta;            // previous kernel wrote only the cache
 };
 
 struct Smem {
@@ -161,40 +164,78 @@ __device__ __forceinline__ int cta_of(long long k, long long K, int C) {
   return c;
 }
 
-// Walks this CTA's chunk range in order; identical in every role.
+// Walks this CTA's chunk range; identical in every role.  The range is
+// visited as up to three contiguous pieces: the unit it ends in (shared with
+// the next CTA), then the unit it starts in (shared with the previous CTA),
+// then the whole units in between.  Both pieces of every split unit are thus
+// finished early in their CTAs, so the merge of a split unit happens while
+// the pipeline still has work to hide it, and every CTA ends on whole units.
 struct ChunkWalk {
   const int* cp;   // smem chunk prefix: cp[i] = chunks of sequences < i (all heads)
+  const int* nl;   // smem clamped context lengths
   int S, Hkv;
-  long long k, hi, lo;
+  long long k;                 // current global chunk index
+  long long lo0, hi0, lo1, hi1, lo2, hi2;  // the pieces, in visiting order
+  long long cur_lo, cur_hi;    // the piece being visited
+  int nsub, si;
   int seq, g, j, nch, n;
-  const int32_t* ctx;
-  int cap;
 
   __device__ void load_unit() {
     nch = (cp[seq + 1] - cp[seq]) / Hkv;
-    n = min(ctx[seq], cap);
+    n = nl[seq];
   }
-  __device__ void init(long long lo_, long long hi_) {
-    lo = lo_;
-    hi = hi_;
-    k = lo_;
-    if (k >= hi) return;
-    // largest seq with cp[seq] <= k (and a non-empty unit)
-    int a = 0, b = S - 1;
+  // position (seq, g, j) of chunk kk
+  __device__ void seek(long long kk) {
+    k = kk;
+    int a = 0, b = S - 1;  // largest seq with cp[seq] <= kk
     while (a < b) {
       const int m = (a + b + 1) >> 1;
-      if (cp[m] <= k) a = m; else b = m - 1;
+      if (cp[m] <= kk) a = m; else b = m - 1;
     }
     seq = a;
-    while (cp[seq + 1] <= k) ++seq;  // skip empty sequences sharing the prefix value
+    while (cp[seq + 1] <= kk) ++seq;  // skip empty sequences sharing the prefix value
     load_unit();
-    const int r = (int)(k - cp[seq]);
+    const int r = (int)(kk - cp[seq]);
     g = r / nch;
     j = r - g * nch;
   }
+  __device__ void init(long long lo, long long hi) {
+    nsub = 0;
+    si = 0;
+    if (lo >= hi) {
+      k = 0;
+      return;
+    }
+    seek(hi - 1);
+    const long long tail_lo = max(lo, k - j);  // first chunk of the last unit
+    seek(lo);
+    const long long head_hi = min(hi, k - j + nch);  // end of the first unit
+    lo1 = hi1 = lo2 = hi2 = 0;
+    if (head_hi >= hi) {
+      lo0 = lo; hi0 = hi; nsub = 1;
+    } else {
+      lo0 = tail_lo; hi0 = hi;
+      lo1 = lo; hi1 = head_hi;
+      nsub = 2;
+      if (head_hi < tail_lo) {
+        lo2 = head_hi; hi2 = tail_lo;
+        nsub = 3;
+      }
+    }
+    cur_lo = lo0;
+    cur_hi = hi0;
+    seek(lo0);
+  }
+  __device__ bool done() const { return si >= nsub; }
   __device__ void next() {
-    ++k;
-    if (k >= hi) return;
+    if (++k >= cur_hi) {
+      if (++si < nsub) {
+        cur_lo = si == 1 ? lo1 : lo2;
+        cur_hi = si == 1 ? hi1 : hi2;
+        seek(cur_lo);
+      }
+      return;
+    }
     if (++j == nch) {
       j = 0;
       if (++g == Hkv) {
@@ -204,8 +245,8 @@ struct ChunkWalk {
       }
     }
   }
-  __device__ bool first_of_segment() const { return j == 0 || k == lo; }
-  __device__ bool last_of_segment() const { return j == nch - 1 || k == hi - 1; }
+  __device__ bool first_of_segment() const { return j == 0 || k == cur_lo; }
+  __device__ bool last_of_segment() const { return j == nch - 1 || k == cur_hi - 1; }
   __device__ int valid() const { return min(CH, n - j * CH); }
 };
 
@@ -228,6 +269,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int S = p.num_seqs, Hkv = p.num_kv_heads, H = p.num_heads;
   const int cap = p.max_blocks << p.log2_bs;
   int* cp = reinterpret_cast<int*>(sm.base + OFF_CP);
+  int* nl = reinterpret_cast<int*>(sm.base + OFF_NLEN);
 
   // ---------------- prologue ----------------
   if (warp == 5) {
@@ -238,15 +280,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int i = 0; i < NBARS; ++i) {
       uint32_t cnt = 1;
       if ((i >= B_S_EMPTY && i < B_S_EMPTY + 2) || (i >= B_P_FULL && i < B_P_FULL + 2) ||
-          (i >= B_O_EMPTY && i < B_O_EMPTY + 2))
+          (i >= B_O_EMPTY && i < B_O_EMPTY + 2) || (i >= B_EPI && i < B_EPI + 2))
         cnt = 128;
       ptx::mbar_init(sm.bar(i), cnt);
     }
     *sm.abort_flag() = 0;
     ptx::fence_mbar_init();
   }
-  // inputs may come from the previous kernel in the stream
-  ptx::grid_dependency_wait();
+  // Inputs may come from the previous kernel in the stream.  When that kernel
+  // is known to write only the KV cache, only the producer waits, right
+  // before its first cache load; lengths, tables and q are read at once.
+  if (!p.early_meta) ptx::grid_dependency_wait();
   if (warp == 4 && lane == 0) {
     ptx::prefetch_tmap(&tm_k);
     ptx::prefetch_tmap(&tm_v);
@@ -265,16 +309,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
   }
+  // chunk counts per sequence, loaded by all threads at once
+  for (int i = tid; i < S; i += NTHREADS) {
+    const int n = min(p.context_lens[i], cap);
+    nl[i] = n;
+    cp[i] = n > 0 ? Hkv * ((n + CH - 1) / CH) : 0;
+  }
+  __syncthreads();
   if (warp == 0) {
-    // chunk prefix over sequences: cp[i] = sum_{i' < i} H_kv * ceil(n_i' / CH)
+    // exclusive prefix in place: cp[i] = sum_{i' < i} H_kv * ceil(n_i' / CH)
     int carry = 0;
     for (int base = 0; base < S; base += 32) {
       const int i = base + lane;
-      int v = 0;
-      if (i < S) {
-        const int n = min(p.context_lens[i], cap);
-        v = n > 0 ? Hkv * ((n + CH - 1) / CH) : 0;
-      }
+      const int v = i < S ? cp[i] : 0;
       int incl = v;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -301,14 +348,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   walk.cp = cp;
   walk.S = S;
   walk.Hkv = Hkv;
-  walk.ctx = p.context_lens;
-  walk.cap = cap;
+  walk.nl = nl;
 
   if (warp == 4) {
     // ================= producer =================
     walk.init(lo, hi);
     int local = 0, seg = 0;
-    for (; walk.k < hi; walk.next(), ++local) {
+    for (; !walk.done(); walk.next(), ++local) {
       const int s = local % NST;
       const uint32_t ph = (local / NST) & 1;
       const int cs = walk.j * CH;
@@ -338,6 +384,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ++seg;
       }
       const uint32_t bytes = (uint32_t)nbox * p.box_tok * 256u;
+      if (p.early_meta && local == 0) ptx::grid_dependency_wait();
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_K + s), bytes);
         ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_V + s), bytes);
@@ -403,7 +450,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ptx::tc_commit(sm.bar(B_EMPTY + s));
         return true;
       };
-      for (; walk.k < hi; walk.next(), ++local) {
+      for (; !walk.done(); walk.next(), ++local) {
         const int s = local % NST;
         const uint32_t ph = (local / NST) & 1;
         const int b = local & 1;
@@ -440,6 +487,69 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         drain_bar(sm.bar(B_P_EMPTY + (L & 1)), (L >> 1) & 1);
       }
     }
+  } else if (warp == 6) {
+    // ================= merge warp =================
+    // Follows the same walk; for each piece of a split unit (at most the
+    // first and the last unit of this CTA's range) it waits for the softmax
+    // warps' partial, counts the arrival, and if this was the unit's last
+    // piece merges all pieces into the output: the merge latency stays off
+    // the softmax warps' critical path.
+    walk.init(lo, hi);
+    int e = 0;
+    for (; !walk.done(); walk.next()) {
+      if (!walk.last_of_segment()) continue;
+      const long long first = walk.k - walk.j;
+      const int c0 = cta_of(first, Ktot, C);
+      const int c1 = cta_of(first + walk.nch - 1, Ktot, C);
+      if (c0 == c1) continue;  // whole unit: the softmax warps wrote the output
+      const bool good = wait_bar(sm, sm.bar(B_EPI + (e++ & 1)), 0, p.err, 14);
+      if (!good) continue;
+      __threadfence();  // the partial written by this CTA is visible before the count
+      const int u = walk.seq * Hkv + walk.g;
+      const int nseg = c1 - c0 + 1;
+      int last = 0;
+      if (lane == 0) last = (arrive(&p.counters[u], p.epoch) == nseg);
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (!last) continue;
+      __threadfence();  // see every other piece's partial
+      const int64_t slot0 = (int64_t)u * p.max_seg;
+      float M[G], Ls[G], a[G][4];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        M[h] = -INFINITY;
+        Ls[h] = 0.f;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) a[h][r] = 0.f;
+      }
+      for (int jj = 0; jj < nseg; ++jj) {
+        float2 ml[G];
+        float ov[G][4];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          ml[h] = __ldcg(&p.ws_ml[(slot0 + jj) * G + h]);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) ov[h][r] = __ldcg(&p.ws_o[((slot0 + jj) * G + h) * D + lane + 32 * r]);
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float mn = fmaxf(M[h], ml[h].x);
+          const float rs = fast_exp2(M[h] - mn);  // 0 for the first piece
+          const float w = fast_exp2(ml[h].x - mn);
+          Ls[h] = Ls[h] * rs + w * ml[h].y;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) a[h][r] = a[h][r] * rs + w * ov[h][r];
+          M[h] = mn;
+        }
+      }
+      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                         ((int64_t)walk.seq * H + (int64_t)walk.g * G) * D + lane;
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          o[(int64_t)h * D + 32 * r] = __float2bfloat16_rn(a[h][r] / Ls[h]);
+      if (lane == 0) p.counters[u] = p.epoch << 16;  // count 0: a replay starts afresh
+    }
   } else {
     // ================= softmax + epilogue (warps 0-3) =================
     const int t = tid;  // TMEM lane: token in S, d in O
@@ -463,6 +573,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       bool last;
     } prev{0, 0, 0, 0, 0, false};
 
+    int split_epi = 0;  // split-unit partials handed to the merge warp (<= 2)
     auto epilogue = [&](const Info& in, const float* ms, const float* ls) {
       float lt[G];
 #pragma unroll
@@ -487,63 +598,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int h = 0; h < G; ++h) o[(int64_t)h * D] = __float2bfloat16_rn(acc[h] / lt[h]);
       } else {
-        const int nseg = c1 - c0 + 1;
-        const int64_t slot0 = (int64_t)u * p.max_seg;
-        const int64_t slot = slot0 + ((int)blockIdx.x - c0);
+        // a piece of a split unit: leave the partial for the merge warp
+        const int64_t slot = (int64_t)u * p.max_seg + ((int)blockIdx.x - c0);
 #pragma unroll
         for (int h = 0; h < G; ++h) p.ws_o[(slot * G + h) * D + t] = acc[h];
 #pragma unroll
         for (int h = 0; h < G; ++h)
           if (t == h) p.ws_ml[slot * G + h] = make_float2(ms[h], lt[h]);
-        __threadfence();
-        ptx::bar_sync_named(2, 128);
-        volatile int* merge = reinterpret_cast<volatile int*>(sm.base + OFF_MERGE);
-        if (t == 0) *merge = (arrive(&p.counters[u], p.epoch) == nseg);
-        ptx::bar_sync_named(2, 128);
-        if (*merge) {
-          // last segment of the unit to finish: merge every CTA's partial,
-          // folding up to 4 segments per round so their loads overlap
-          __threadfence();
-          float M[G], Ls[G], a[G];
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            M[h] = -INFINITY;
-            Ls[h] = 0.f;
-            a[h] = 0.f;
-          }
-          for (int j0 = 0; j0 < nseg; j0 += 4) {
-            float2 mlj[4][G];
-            float oj[4][G];
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-              for (int h = 0; h < G; ++h) {
-                const bool in = j0 + jj < nseg;
-                const int64_t sl = slot0 + (in ? j0 + jj : 0);
-                mlj[jj][h] = in ? __ldcg(&p.ws_ml[sl * G + h]) : make_float2(-INFINITY, 0.f);
-                oj[jj][h] = in ? __ldcg(&p.ws_o[(sl * G + h) * D + t]) : 0.f;
-              }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              float mb = M[h];
-#pragma unroll
-              for (int jj = 0; jj < 4; ++jj) mb = fmaxf(mb, mlj[jj][h].x);
-              const float r = fast_exp2(M[h] - mb);  // 0 on the first round
-              Ls[h] *= r;
-              a[h] *= r;
-#pragma unroll
-              for (int jj = 0; jj < 4; ++jj) {
-                const float wgt = fast_exp2(mlj[jj][h].x - mb);
-                Ls[h] += wgt * mlj[jj][h].y;
-                a[h] += wgt * oj[jj][h];
-              }
-              M[h] = mb;
-            }
-          }
-#pragma unroll
-          for (int h = 0; h < G; ++h) o[(int64_t)h * D] = __float2bfloat16_rn(a[h] / Ls[h]);
-          if (t == 0) p.counters[u] = p.epoch << 16;  // count 0: a replay starts afresh
-        }
+        ptx::mbar_arrive(sm.bar(B_EPI + (split_epi++ & 1)));
       }
     };
 
@@ -573,7 +635,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     walk.init(lo, hi);
     int local = 0;
-    for (; walk.k < hi; walk.next(), ++local) {
+    for (; !walk.done(); walk.next(), ++local) {
       const int s = local % NST;
       const uint32_t ph = (local / NST) & 1;
       const int b = local & 1;
@@ -793,6 +855,7 @@ cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream) {
   while ((1 << lx) < box_tok) ++lx;
   prm.log2_box = lx;
   prm.scale_log2 = a.scale * 1.4426950408889634f;
+  prm.early_meta = a.early_meta ? 1 : 0;
   {
     // a distinct 48-bit tag per call (the merge counters' epoch)
     static std::atomic<unsigned long long> next_epoch{0x5eed00000000ull};

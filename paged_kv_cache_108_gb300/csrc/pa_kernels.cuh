@@ -56,6 +56,7 @@ struct TcLaunch {
   int num_seqs, num_heads, num_kv_heads, max_blocks, num_blocks, block_size;
   int num_ctas;     // persistent CTAs (one per SM)
   float scale;
+  bool early_meta;  // the previous kernel only wrote the cache (see decode_tc.cu)
 };
 bool tc_supported(int head_dim, int group, bool fp8, int num_seqs, int block_size);
 size_t tc_workspace_bytes(int64_t num_seqs, int64_t num_heads, int64_t max_ctx, int num_ctas);

@@ -124,3 +124,27 @@ def copy_blocks(k_cache, v_cache, block_pairs, stream=None) -> None:
     ptr = _dev(block_pairs, "block_pairs", torch.int32) if n > 0 else None
     _lib.check(_lib.lib().pa_copy_blocks(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
                                          desc, ptr, n, _stream(stream)))
+
+
+def write_and_decode(key, value, slot_mapping, out, q, k_cache, v_cache, block_tables,
+                     context_lens, scale, k_scale=None, v_scale=None, workspace=None,
+                     stream=None):
+    """One decode step: cache write of the new tokens, then paged decode."""
+    _same_cache(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    ks, vs = _scales(desc, k_scale, v_scale)
+    if q.dim() != 3 or out.shape != q.shape:
+        raise ValueError("q and out must both be [num_seqs, num_heads, head_dim]")
+    num_seqs, num_heads, _ = q.shape
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr = _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _lib.check(_lib.lib().pa_write_and_decode(
+        _dev(key, "key", torch.bfloat16), _dev(value, "value", torch.bfloat16),
+        _dev(slot_mapping, "slot_mapping", torch.int32), int(slot_mapping.numel()),
+        _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), desc, _dev(block_tables, "block_tables", torch.int32),
+        int(block_tables.shape[1]), _dev(context_lens, "context_lens", torch.int32), num_seqs,
+        num_heads, ctypes.c_float(scale), ks, vs, ws_ptr, ws_bytes, _stream(stream)))
+    return out

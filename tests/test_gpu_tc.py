@@ -112,3 +112,31 @@ def test_tc_workspace_shared_across_shapes_and_repeated_calls():
         if w.name in outs:
             assert np.array_equal(outs[w.name], res)
         outs[w.name] = res
+
+
+@requires_gpu
+def test_write_and_decode_matches_separate_calls():
+    """The one-call step gives the same caches and bit-identical output as the
+    separate write and decode calls (the overlap changes only timing)."""
+    from paged_kv_cache_108_gb300 import ops, pool
+    w = synth.llama8b()
+    got = harness.product_step(w)  # separate calls
+    dev = got["dev"]
+    kc = harness.to_dev_bits(w.junk_k, "bf16", "cuda")
+    vc = harness.to_dev_bits(w.junk_v, "bf16", "cuda")
+    seq_idx, pos = harness.ctx_positions(w)
+    ops.reshape_and_cache(harness.to_dev_bits(w.ctx_k, "bf16", "cuda"),
+                          harness.to_dev_bits(w.ctx_v, "bf16", "cuda"), kc, vc,
+                          torch.from_numpy(pool.slot_mapping(w.block_tables, w.block_size, pos, seq_idx)).cuda())
+    out = torch.empty_like(dev["q"])
+    ws = ops.alloc_workspace(w.num_seqs, w.num_heads, w.head_dim, w.max_blocks, w.block_size)
+    ws.random_(0, 256)
+    for _ in range(2):
+        ops.write_and_decode(harness.to_dev_bits(w.k_new, "bf16", "cuda"),
+                             harness.to_dev_bits(w.v_new, "bf16", "cuda"),
+                             torch.from_numpy(got["slots_new"]).cuda(), out, dev["q"], kc, vc,
+                             dev["bt"], dev["cl"], w.scale, workspace=ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(harness.bits_from_dev(kc), got["k_cache"])
+        assert np.array_equal(harness.bits_from_dev(vc), got["v_cache"])
+        assert np.array_equal(out.float().cpu().numpy().astype(np.float64), got["out"])
