@@ -365,28 +365,39 @@ def run_e2e(step, args, device, dist):
     decode, and a device->host read of the output."""
     import torch
     w = step.w
-    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-    h_q, h_k, h_v = pin(step.q), pin(step.k_new), pin(step.v_new)
-    h_bt = torch.from_numpy(w.block_tables).pin_memory()
-    h_cl = torch.from_numpy(w.context_lens).pin_memory()
-    h_slots = torch.empty(w.num_seqs, dtype=torch.int32).pin_memory()
+    # The step's inputs travel as one packed pinned buffer (one host->device
+    # copy per step); the device-side views point into one staging buffer.
+    parts = [("q", step.q), ("k", step.k_new), ("v", step.v_new),
+             ("bt", step.block_tables), ("cl", step.context_lens), ("slots", step.slots)]
+    offs, total = {}, 0
+    for name, t in parts:
+        offs[name] = total
+        total += -(-(t.numel() * t.element_size()) // 256) * 256
+    h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(total, dtype=torch.uint8, device=device)
+
+    def view(buf, name, like):
+        nbytes = like.numel() * like.element_size()
+        return buf[offs[name]:offs[name] + nbytes].view(like.dtype).view(like.shape)
+
+    h_v = {name: view(h_in, name, t) for name, t in parts}
+    d_v = {name: view(d_in, name, t) for name, t in parts}
+    for name, t in parts:
+        if name != "slots":
+            h_v[name].copy_(t.cpu())
     h_out = torch.empty(step.out.shape, dtype=torch.bfloat16).pin_memory()
-    d_q, d_k, d_v = torch.empty_like(step.q), torch.empty_like(step.k_new), torch.empty_like(step.v_new)
-    d_bt, d_cl = torch.empty_like(step.block_tables), torch.empty_like(step.context_lens)
-    d_slots = torch.empty_like(step.slots)
-    bi = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_bt, h_cl, h_slots))
+    bi = total
     bo = h_out.numel() * h_out.element_size()
 
     def one():
-        h_slots.numpy()[:] = step.pool.slot_mapping(w.block_tables, w.block_size, step.positions)
-        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_bt, h_bt), (d_cl, h_cl),
-                     (d_slots, h_slots)):
-            d.copy_(h, non_blocking=True)
+        h_v["slots"].numpy()[:] = step.pool.slot_mapping(w.block_tables, w.block_size,
+                                                         step.positions)
+        d_in.copy_(h_in, non_blocking=True)
         if step.kernel == 0:
-            step.run_step(d_slots, d_k, d_v, d_q, d_bt, d_cl)
+            step.run_step(d_v["slots"], d_v["k"], d_v["v"], d_v["q"], d_v["bt"], d_v["cl"])
         else:
-            step.run_write(d_slots, d_k, d_v)
-            step.run_decode(d_q, d_bt, d_cl)
+            step.run_write(d_v["slots"], d_v["k"], d_v["v"])
+            step.run_decode(d_v["q"], d_v["bt"], d_v["cl"])
         h_out.copy_(step.out, non_blocking=True)
         torch.cuda.current_stream().synchronize()  # the host reads the result
 

@@ -89,7 +89,9 @@ constexpr int OFF_LRED = OFF_RED + 2 * 4 * 8 * 4;  // [4][8] floats, epilogue su
 constexpr int OFF_CP = OFF_LRED + 4 * 8 * 4;       // chunk prefix per sequence, [S+1] int
 constexpr int kMaxSeqs = 1024;
 constexpr int OFF_NLEN = OFF_CP + (kMaxSeqs + 1) * 4;  // clamped context length per sequence
-constexpr int SMEM_BYTES = OFF_NLEN + kMaxSeqs * 4 + 1024;  // + alignment slack
+constexpr int OFF_TAB = OFF_NLEN + kMaxSeqs * 4;  // block-id ring: 4 chunks x 16 boxes
+constexpr int TAB_SLOTS = 4, TAB_AHEAD = 3;
+constexpr int SMEM_BYTES = OFF_TAB + TAB_SLOTS * 16 * 4 + 1024;  // + alignment slack
 
 constexpr long long kWaitClocks = 1LL << 31;
 
@@ -352,7 +354,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (warp == 4) {
     // ================= producer =================
+    // Block ids travel through a shared-memory ring filled by 4-byte cp.async
+    // copies TAB_AHEAD chunks ahead (lane b copies and later uses box b's id;
+    // block_size >= 8 keeps a chunk within 16 boxes), so table reads overlap
+    // instead of following one another.
+    const uint32_t tab = sm.base_u32 + OFF_TAB;
+    const int* tab_s = reinterpret_cast<const int*>(sm.base + OFF_TAB);
+    auto fetch_ids = [&](const ChunkWalk& w, int slot) {
+      const int nb = (w.valid() + p.box_tok - 1) >> p.log2_box;
+      if (lane < nb)
+        cp_async_4(tab + (slot * 16 + lane) * 4,
+                   p.block_tables + (int64_t)w.seq * p.max_blocks +
+                       ((w.j * CH + lane * p.box_tok) >> p.log2_bs));
+    };
     walk.init(lo, hi);
+    ChunkWalk ahead = walk;
+#pragma unroll
+    for (int d = 0; d < TAB_AHEAD; ++d) {
+      if (!ahead.done()) {
+        fetch_ids(ahead, d);
+        ahead.next();
+      }
+      cp_async_commit();
+    }
     int local = 0, seg = 0;
     for (; !walk.done(); walk.next(), ++local) {
       const int s = local % NST;
@@ -360,15 +384,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int cs = walk.j * CH;
       const int valid = walk.valid();
       const int nbox = (valid + p.box_tok - 1) >> p.log2_box;
-      // block ids of this chunk (<= 4 per lane) are fetched before waiting for
-      // the ring slot, so their latency hides behind the wait
-      const int32_t* table = p.block_tables + (int64_t)walk.seq * p.max_blocks;
-      int phys_r[CH / 32];
-#pragma unroll
-      for (int r = 0; r < CH / 32; ++r) {
-        const int bx = lane + 32 * r;
-        phys_r[r] = bx < nbox ? table[(cs + bx * p.box_tok) >> p.log2_bs] : 0;
-      }
+      cp_async_wait<TAB_AHEAD - 1>();  // this chunk's ids have landed
+      const int phys_in = lane < nbox ? tab_s[(local % TAB_SLOTS) * 16 + lane] : 0;
       if (!wait_bar(sm, sm.bar(B_EMPTY + s), ph ^ 1, p.err, 1)) break;
       if (walk.first_of_segment()) {
         const int qs = seg & 1;
@@ -385,31 +402,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       const uint32_t bytes = (uint32_t)nbox * p.box_tok * 256u;
       if (p.early_meta && local == 0) ptx::grid_dependency_wait();
+      const uint32_t kdst = sm.base_u32 + OFF_K + s * TILE_B;
+      const uint32_t vdst = sm.base_u32 + OFF_V + s * TILE_B;
+      const uint32_t row = (uint32_t)(lane * p.box_tok) * 128u;
+      const int off = (cs + lane * p.box_tok) & (p.block_size - 1);
+      int phys = phys_in;
+      if (lane < nbox && (unsigned)phys >= (unsigned)p.num_blocks) {
+        atomicExch(p.err, 3);  // bad block id: load block 0 instead of faulting
+        phys = 0;
+      }
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_K + s), bytes);
         ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_V + s), bytes);
       }
       __syncwarp();
-      const uint32_t kdst = sm.base_u32 + OFF_K + s * TILE_B;
-      const uint32_t vdst = sm.base_u32 + OFF_V + s * TILE_B;
-#pragma unroll
-      for (int r = 0; r < CH / 32; ++r) {
-        const int bx = lane + 32 * r;
-        if (bx >= nbox) break;
-        const int tok0 = cs + bx * p.box_tok;
-        const int off = tok0 & (p.block_size - 1);
-        int phys = phys_r[r];
-        if ((unsigned)phys >= (unsigned)p.num_blocks) {
-          atomicExch(p.err, 3);  // bad block id: load block 0 instead of faulting
-          phys = 0;
-        }
-        const uint32_t row = (uint32_t)(bx * p.box_tok) * 128u;
+      if (lane < nbox) {
         ptx::tma_load_4d(kdst + row, &tm_k, sm.bar(B_FULL_K + s), 0, walk.g, off, phys);
         ptx::tma_load_4d(kdst + HALF_B + row, &tm_k, sm.bar(B_FULL_K + s), 64, walk.g, off, phys);
         ptx::tma_load_4d(vdst + row, &tm_v, sm.bar(B_FULL_V + s), 0, walk.g, off, phys);
         ptx::tma_load_4d(vdst + HALF_B + row, &tm_v, sm.bar(B_FULL_V + s), 64, walk.g, off, phys);
       }
+      if (!ahead.done()) {
+        fetch_ids(ahead, (local + TAB_AHEAD) % TAB_SLOTS);
+        ahead.next();
+      }
+      cp_async_commit();
     }
+    cp_async_wait<0>();
     // drain: the last loads issued must land before the CTA can exit
     __syncwarp();
     if (lane == 0) {
