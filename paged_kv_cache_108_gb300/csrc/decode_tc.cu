@@ -440,68 +440,84 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp == 5) {
     // ================= MMA issuer =================
+    // Two cursors: the logits MMA of chunk nq (needs its K tile, a free S
+    // buffer and, at a segment start, the q tile) and the PV MMA of chunk
+    // npv < nq (needs P, a free O buffer and the V tile).  The thread polls
+    // both and issues whichever is ready, so a stage is released as soon as
+    // its own PV completes, never held back by a later chunk's K load.
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(128, NQ, false);
       constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, NQ, true);
       walk.init(lo, hi);
-      int local = 0, seg = 0, cur_q = 0;
-      bool ok = true;
-      auto pv = [&](int L) {
-        const int s = L % NST;
-        const uint32_t ph = (L / NST) & 1;
-        const int b = L & 1;
-        const uint32_t bph = (L >> 1) & 1;
-        bool good = wait_bar(sm, sm.bar(B_P_FULL + b), bph, p.err, 4);
-        good = good && wait_bar(sm, sm.bar(B_O_EMPTY + b), bph ^ 1, p.err, 5);
-        good = good && wait_bar(sm, sm.bar(B_FULL_V + s), ph, p.err, 6);
-        if (!good) return false;
-        ptx::tc_fence_after();
-        const uint32_t vbase = sm.base_u32 + OFF_V + s * TILE_B;
-        const uint32_t pbase = sm.base_u32 + OFF_P + b * PTILE_B;
+      int nq = 0, npv = 0, seg = 0, cur_q = 0;
+      long long t_idle = clock64();
+      while (true) {
+        bool progress = false;
+        if (!walk.done()) {
+          const int s = nq % NST;
+          const int b = nq & 1;
+          const bool first = walk.first_of_segment();
+          bool ready = ptx::mbar_test_wait(sm.bar(B_FULL_K + s), (nq / NST) & 1) &&
+                       ptx::mbar_test_wait(sm.bar(B_S_EMPTY + b), ((nq >> 1) & 1) ^ 1);
+          if (ready && first) ready = ptx::mbar_test_wait(sm.bar(B_Q_FULL + (seg & 1)), (seg >> 1) & 1);
+          if (ready) {
+            if (first) cur_q = seg++ & 1;
+            ptx::tc_fence_after();
+            const uint32_t kbase = sm.base_u32 + OFF_K + s * TILE_B;
+            const uint32_t qbase = sm.base_u32 + OFF_Q + cur_q * QTILE_B;
 #pragma unroll
-        for (int kk = 0; kk < CH / 16; ++kk) {
-          const uint64_t da = ptx::smem_desc_sw128(vbase + kk * 2048, HALF_B, 1024);
-          const uint64_t db = ptx::smem_desc_sw128(pbase + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024);
-          ptx::tc_mma_f16(tmem + 32 + 16 * b, da, db, IDESC_PV, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t da = ptx::smem_desc_sw128(kbase + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
+              const uint64_t db = ptx::smem_desc_sw128(qbase + (kk >> 2) * (QTILE_B / 2) + (kk & 3) * 32, 16, 1024);
+              ptx::tc_mma_f16(tmem + 16 * b, da, db, IDESC_QK, kk > 0);
+            }
+            ptx::tc_commit(sm.bar(B_S_FULL + b));
+            if (walk.last_of_segment()) ptx::tc_commit(sm.bar(B_Q_EMPTY + cur_q));
+            walk.next();
+            ++nq;
+            progress = true;
+          }
         }
-        ptx::tc_commit(sm.bar(B_O_FULL + b));
-        ptx::tc_commit(sm.bar(B_P_EMPTY + b));
-        ptx::tc_commit(sm.bar(B_EMPTY + s));
-        return true;
-      };
-      for (; !walk.done(); walk.next(), ++local) {
-        const int s = local % NST;
-        const uint32_t ph = (local / NST) & 1;
-        const int b = local & 1;
-        const uint32_t bph = (local >> 1) & 1;
-        if (walk.first_of_segment()) {
-          cur_q = seg & 1;
-          ok = wait_bar(sm, sm.bar(B_Q_FULL + cur_q), (seg >> 1) & 1, p.err, 7);
-          ++seg;
-        }
-        ok = ok && wait_bar(sm, sm.bar(B_FULL_K + s), ph, p.err, 8);
-        ok = ok && wait_bar(sm, sm.bar(B_S_EMPTY + b), bph ^ 1, p.err, 9);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        const uint32_t kbase = sm.base_u32 + OFF_K + s * TILE_B;
-        const uint32_t qbase = sm.base_u32 + OFF_Q + cur_q * QTILE_B;
+        if (npv < nq) {
+          const int s = npv % NST;
+          const int b = npv & 1;
+          const uint32_t bph = (npv >> 1) & 1;
+          if (ptx::mbar_test_wait(sm.bar(B_P_FULL + b), bph) &&
+              ptx::mbar_test_wait(sm.bar(B_O_EMPTY + b), bph ^ 1) &&
+              ptx::mbar_test_wait(sm.bar(B_FULL_V + s), (npv / NST) & 1)) {
+            ptx::tc_fence_after();
+            const uint32_t vbase = sm.base_u32 + OFF_V + s * TILE_B;
+            const uint32_t pbase = sm.base_u32 + OFF_P + b * PTILE_B;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t da = ptx::smem_desc_sw128(kbase + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
-          const uint64_t db = ptx::smem_desc_sw128(qbase + (kk >> 2) * (QTILE_B / 2) + (kk & 3) * 32, 16, 1024);
-          ptx::tc_mma_f16(tmem + 16 * b, da, db, IDESC_QK, kk > 0);
-        }
-        ptx::tc_commit(sm.bar(B_S_FULL + b));
-        if (walk.last_of_segment()) ptx::tc_commit(sm.bar(B_Q_EMPTY + cur_q));
-        if (local > 0 && !pv(local - 1)) {
-          ok = false;
+            for (int kk = 0; kk < CH / 16; ++kk) {
+              const uint64_t da = ptx::smem_desc_sw128(vbase + kk * 2048, HALF_B, 1024);
+              const uint64_t db = ptx::smem_desc_sw128(pbase + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024);
+              ptx::tc_mma_f16(tmem + 32 + 16 * b, da, db, IDESC_PV, kk > 0);
+            }
+            ptx::tc_commit(sm.bar(B_O_FULL + b));
+            ptx::tc_commit(sm.bar(B_P_EMPTY + b));
+            ptx::tc_commit(sm.bar(B_EMPTY + s));
+            ++npv;
+            progress = true;
+          }
+        } else if (walk.done()) {
           break;
         }
+        if (progress) {
+          t_idle = clock64();
+        } else {
+          if (*sm.abort_flag()) break;
+          if (clock64() - t_idle > kWaitClocks) {
+            *sm.abort_flag() = 1;
+            atomicExch(p.err, 8);
+            break;
+          }
+        }
       }
-      if (ok && local > 0) ok = pv(local - 1);
       // drain: every commit this thread issued must land before exit
-      if (local > 0) {
-        const int L = local - 1;
+      if (nq > 0) drain_bar(sm.bar(B_S_FULL + ((nq - 1) & 1)), ((nq - 1) >> 1) & 1);
+      if (npv > 0) {
+        const int L = npv - 1;
         drain_bar(sm.bar(B_EMPTY + L % NST), (L / NST) & 1);
         drain_bar(sm.bar(B_P_EMPTY + (L & 1)), (L >> 1) & 1);
       }
