@@ -84,6 +84,7 @@ constexpr int B_FULL_K = 0, B_FULL_V = 3, B_EMPTY = 6, B_S_FULL = 9, B_S_EMPTY =
               B_Q_EMPTY = 23, B_EPI = 25, NBARS = 27;
 constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 4;
+constexpr int OFF_SQ = OFF_ABORT + 4;        // [2] ints: sequences of the range's ends
 constexpr int OFF_RED = OFF_ABORT + 12;      // [2][4][8] floats, chunk max
 constexpr int OFF_LRED = OFF_RED + 2 * 4 * 8 * 4;  // [4][8] floats, epilogue sums
 constexpr int OFF_CP = OFF_LRED + 4 * 8 * 4;       // chunk prefix per sequence, [S+1] int
@@ -182,59 +183,73 @@ struct ChunkWalk {
   int nsub, si;
   int seq, g, j, nch, n;
 
+  int sq1, g1, j1, sq2, g2;    // where pieces 1 and 2 start (piece 2 starts a unit)
+
   __device__ void load_unit() {
     nch = (cp[seq + 1] - cp[seq]) / Hkv;
     n = nl[seq];
   }
-  // position (seq, g, j) of chunk kk
-  __device__ void seek(long long kk) {
+  // position (seq, g, j) of chunk kk, given the sequence s holding it
+  __device__ void seek_in(int s, long long kk) {
     k = kk;
-    int a = 0, b = S - 1;  // largest seq with cp[seq] <= kk
-    while (a < b) {
-      const int m = (a + b + 1) >> 1;
-      if (cp[m] <= kk) a = m; else b = m - 1;
-    }
-    seq = a;
-    while (cp[seq + 1] <= kk) ++seq;  // skip empty sequences sharing the prefix value
+    seq = s;
     load_unit();
-    const int r = (int)(kk - cp[seq]);
+    const int r = (int)(kk - cp[s]);
     g = r / nch;
     j = r - g * nch;
   }
-  __device__ void init(long long lo, long long hi) {
+  // seq_lo / seq_hi: the sequences holding chunks lo and hi - 1
+  __device__ void init(long long lo, long long hi, int seq_lo, int seq_hi) {
     nsub = 0;
     si = 0;
     if (lo >= hi) {
       k = 0;
       return;
     }
-    seek(hi - 1);
-    const long long tail_lo = max(lo, k - j);  // first chunk of the last unit
-    seek(lo);
+    seek_in(seq_lo, lo);
     const long long head_hi = min(hi, k - j + nch);  // end of the first unit
-    lo1 = hi1 = lo2 = hi2 = 0;
     if (head_hi >= hi) {
       lo0 = lo; hi0 = hi; nsub = 1;
-    } else {
-      lo0 = tail_lo; hi0 = hi;
-      lo1 = lo; hi1 = head_hi;
-      nsub = 2;
-      if (head_hi < tail_lo) {
-        lo2 = head_hi; hi2 = tail_lo;
-        nsub = 3;
-      }
+      cur_lo = lo0;
+      cur_hi = hi0;
+      return;
+    }
+    sq1 = seq; g1 = g; j1 = j;
+    // the unit after the first one (a chunk exists there: head_hi < hi)
+    sq2 = seq;
+    g2 = g + 1;
+    if (g2 == Hkv) {
+      g2 = 0;
+      do { ++sq2; } while (cp[sq2 + 1] == cp[sq2]);
+    }
+    seek_in(seq_hi, hi - 1);
+    const long long tail_lo = k - j;  // first chunk of the last unit (>= head_hi)
+    lo0 = tail_lo; hi0 = hi;
+    lo1 = lo; hi1 = head_hi;
+    lo2 = hi2 = 0;
+    nsub = 2;
+    if (head_hi < tail_lo) {
+      lo2 = head_hi; hi2 = tail_lo;
+      nsub = 3;
     }
     cur_lo = lo0;
     cur_hi = hi0;
-    seek(lo0);
+    k = tail_lo;
+    j = 0;
   }
   __device__ bool done() const { return si >= nsub; }
   __device__ void next() {
     if (++k >= cur_hi) {
       if (++si < nsub) {
-        cur_lo = si == 1 ? lo1 : lo2;
-        cur_hi = si == 1 ? hi1 : hi2;
-        seek(cur_lo);
+        if (si == 1) {
+          cur_lo = lo1; cur_hi = hi1;
+          seq = sq1; g = g1; j = j1;
+        } else {
+          cur_lo = lo2; cur_hi = hi2;
+          seq = sq2; g = g2; j = 0;
+        }
+        k = cur_lo;
+        load_unit();
       }
       return;
     }
@@ -345,6 +360,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int C = (int)(Ktot < p.num_ctas ? Ktot : p.num_ctas);
   const long long lo = (int)blockIdx.x < C ? range_lo(blockIdx.x, Ktot, C) : 0;
   const long long hi = (int)blockIdx.x < C ? range_lo(blockIdx.x + 1, Ktot, C) : 0;
+  // the sequences holding chunks lo and hi - 1, found by all threads at once
+  int* sq = reinterpret_cast<int*>(sm.base + OFF_SQ);
+  if (lo < hi) {
+    for (int i = tid; i < S; i += NTHREADS) {
+      const int a = cp[i], b = cp[i + 1];
+      if (a <= lo && lo < b) sq[0] = i;
+      if (a < hi && hi <= b) sq[1] = i;
+    }
+  }
+  __syncthreads();
+  const int seq_lo = lo < hi ? sq[0] : 0, seq_hi = lo < hi ? sq[1] : 0;
 
   ChunkWalk walk;
   walk.cp = cp;
@@ -367,7 +393,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                    p.block_tables + (int64_t)w.seq * p.max_blocks +
                        ((w.j * CH + lane * p.box_tok) >> p.log2_bs));
     };
-    walk.init(lo, hi);
+    walk.init(lo, hi, seq_lo, seq_hi);
     ChunkWalk ahead = walk;
 #pragma unroll
     for (int d = 0; d < TAB_AHEAD; ++d) {
@@ -448,7 +474,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(128, NQ, false);
       constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, NQ, true);
-      walk.init(lo, hi);
+      walk.init(lo, hi, seq_lo, seq_hi);
       int nq = 0, npv = 0, seg = 0, cur_q = 0;
       long long t_idle = clock64();
       while (true) {
@@ -529,7 +555,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // warps' partial, counts the arrival, and if this was the unit's last
     // piece merges all pieces into the output: the merge latency stays off
     // the softmax warps' critical path.
-    walk.init(lo, hi);
+    walk.init(lo, hi, seq_lo, seq_hi);
     int e = 0;
     for (; !walk.done(); walk.next()) {
       if (!walk.last_of_segment()) continue;
@@ -668,7 +694,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     };
 
-    walk.init(lo, hi);
+    walk.init(lo, hi, seq_lo, seq_hi);
     int local = 0;
     for (; !walk.done(); walk.next(), ++local) {
       const int s = local % NST;
