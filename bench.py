@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--partition", type=int, default=0, help="split-K partition (0 = auto)")
     ap.add_argument("--kernel", type=int, default=0, help="decode kernel (0 auto, 1 SIMT, 2 tcgen05)")
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
+                    help="KV cache type: bf16, or fp8-e4m3 with per-tensor scales")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -56,21 +58,36 @@ def parse():
 class Step:
     """Device-resident state of the headline decode step."""
 
-    def __init__(self, device, partition=0, kernel=0):
+    def __init__(self, device, partition=0, kernel=0, kv_dtype="bf16"):
         import torch
 
         from paged_kv_cache_108_gb300 import ops, pool, synth
         self.torch, self.ops, self.pool = torch, ops, pool
-        w = synth.llama8b(with_data=False)
+        w = synth.llama8b(with_data=False, kv_dtype=kv_dtype)
         self.w = w
         self.device = device
         self.partition, self.kernel = partition, kernel
+        self.fp8 = kv_dtype == "fp8"
+        self.kv_bytes = 1 if self.fp8 else 2
         B, hkv, d, H = w.block_size, w.num_kv_heads, w.head_dim, w.num_heads
         gen = torch.Generator(device=device)
         gen.manual_seed(w.seed)
         shape = (w.num_blocks, B, hkv, d)
-        self.k_cache = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
-        self.v_cache = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+        self.k_scale = self.v_scale = None
+        if self.fp8:
+            # N(0,1) quantised to e4m3 with scale amax / 448 (per tensor)
+            caches, scales = [], []
+            for _ in range(2):
+                x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+                sc = (x.abs().max() / 448.0).reshape(1)
+                caches.append((x / sc).to(torch.float8_e4m3fn).view(torch.uint8))
+                scales.append(sc)
+                del x
+            self.k_cache, self.v_cache = caches
+            self.k_scale, self.v_scale = scales
+        else:
+            self.k_cache = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+            self.v_cache = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
         S = w.num_seqs
         self.q = torch.randn((S, H, d), generator=gen, device=device).to(torch.bfloat16)
         self.k_new = torch.randn((S, hkv, d), generator=gen, device=device).to(torch.bfloat16)
@@ -91,18 +108,20 @@ class Step:
     # algorithmic bytes of one step (what the method must move)
     def decode_bytes(self) -> int:
         w = self.w
-        kv = int(np.sum(w.context_lens)) * w.num_kv_heads * w.head_dim * 2 * 2
+        kv = int(np.sum(w.context_lens)) * w.num_kv_heads * w.head_dim * self.kv_bytes * 2
         qo = 2 * w.num_seqs * w.num_heads * w.head_dim * 2
         table = int(sum(math.ceil(n / w.block_size) for n in w.context_lens)) * 4
         return kv + qo + table + w.num_seqs * 4
 
     def write_bytes(self) -> int:
         w = self.w
-        return 2 * (2 * w.num_seqs * w.num_kv_heads * w.head_dim * 2) + w.num_seqs * 4
+        # K and V: bf16 tokens read, cache rows written
+        return 2 * w.num_seqs * w.num_kv_heads * w.head_dim * (2 + self.kv_bytes) + w.num_seqs * 4
 
     def run_write(self, slots=None, k=None, v=None):
         self.ops.reshape_and_cache(self.k_new if k is None else k, self.v_new if v is None else v,
-                                   self.k_cache, self.v_cache, self.slots if slots is None else slots)
+                                   self.k_cache, self.v_cache, self.slots if slots is None else slots,
+                                   self.k_scale, self.v_scale)
 
     def run_step(self, slots=None, k=None, v=None, q=None, bt=None, cl=None):
         """The step as one call: cache write of the new tokens, then decode."""
@@ -112,14 +131,15 @@ class Step:
                                   self.q if q is None else q, self.k_cache, self.v_cache,
                                   self.block_tables if bt is None else bt,
                                   self.context_lens if cl is None else cl, w.scale,
-                                  workspace=self.ws)
+                                  self.k_scale, self.v_scale, workspace=self.ws)
 
     def run_decode(self, q=None, bt=None, cl=None):
         w = self.w
         self.ops.decode(self.out, self.q if q is None else q, self.k_cache, self.v_cache,
                         self.block_tables if bt is None else bt,
-                        self.context_lens if cl is None else cl, w.scale, workspace=self.ws,
-                        partition_tokens=self.partition, kernel=self.kernel)
+                        self.context_lens if cl is None else cl, w.scale, self.k_scale,
+                        self.v_scale, workspace=self.ws, partition_tokens=self.partition,
+                        kernel=self.kernel)
 
 
 # ---------------------------------------------------------------- helpers
@@ -133,9 +153,10 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic(step_bytes):
+def recorded_traffic(step_bytes, kv_dtype="bf16"):
     """ncu DRAM bytes per decode call, if recorded for the current kernel source."""
-    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    name = "decode_traffic.json" if kv_dtype == "bf16" else f"decode_traffic_{kv_dtype}.json"
+    path = os.path.join(ROOT, "profiles", name)
     try:
         with open(path) as f:
             rec = json.load(f)
@@ -207,14 +228,21 @@ def cpu_baseline_oracle(step, budget_s=10.0):
     from oracle import core as ocore
     torch = step.torch
     w = step.w
-    kc = step.k_cache.view(torch.int16).cpu().numpy().view(np.uint16)
-    vc = step.v_cache.view(torch.int16).cpu().numpy().view(np.uint16)
+    if step.fp8:
+        kc = step.k_cache.cpu().numpy()
+        vc = step.v_cache.cpu().numpy()
+        ks, vs = float(step.k_scale.item()), float(step.v_scale.item())
+    else:
+        kc = step.k_cache.view(torch.int16).cpu().numpy().view(np.uint16)
+        vc = step.v_cache.view(torch.int16).cpu().numpy().view(np.uint16)
+        ks = vs = 1.0
     q = step.q.view(torch.int16).cpu().numpy().view(np.uint16)
     threads = os.cpu_count() or 1
     units = [(i, g) for i in range(w.num_seqs) for g in range(w.num_kv_heads)]
     # bounded sample: the first sequences' units until the budget is spent
     bytes_done, t_total, reps = 0, 0.0, 0
-    per_unit_bytes = {(i, g): int(w.context_lens[i]) * w.head_dim * 2 * 2 for i, g in units}
+    per_unit_bytes = {(i, g): int(w.context_lens[i]) * w.head_dim * step.kv_bytes * 2
+                      for i, g in units}
     chunk = max(threads, 32)
     at = 0
     while t_total < budget_s and reps < 100000:
@@ -223,7 +251,7 @@ def cpu_baseline_oracle(step, budget_s=10.0):
             at = 0
             continue
         t0 = time.perf_counter()
-        ocore.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, units=sel,
+        ocore.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, ks, vs, units=sel,
                      nthreads=threads)
         t_total += time.perf_counter() - t0
         bytes_done += sum(per_unit_bytes[u] for u in sel)
@@ -241,7 +269,7 @@ def run_ours(args, rank, world, local_rank):
     import torch
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
-    step = Step(device, args.partition, args.kernel)
+    step = Step(device, args.partition, args.kernel, args.kv_dtype)
     stream = torch.cuda.current_stream()
     # L2 flush: read a buffer 4x the L2 size.  Reading (not writing) leaves
     # only clean lines behind, so the timed kernels do not pay for writing
@@ -325,9 +353,13 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(mean_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16 K/V/q; lengths from the pages' seeded request mix)",
-        "config": {"workload": "llama8b-layer decode, batch 64, 32q/8kv heads, d=128, bf16 KV, "
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if step.fp8 else "bf16",
+        "data": ("synthetic (seeded N(0,1) K/V quantised to e4m3 with scale amax/448, bf16 q; "
+                 "lengths from the pages' seeded request mix)" if step.fp8 else
+                 "synthetic (seeded N(0,1) bf16 K/V/q; lengths from the pages' seeded request mix)"),
+        "config": {"workload": "llama8b-layer decode, batch 64, 32q/8kv heads, d=128, "
+                               f"{'e4m3 (per-tensor scale)' if step.fp8 else 'bf16'} KV, "
                                "block 16, sum ctx 121416", "num_seqs": w.num_seqs,
                    "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "block_size": w.block_size,
@@ -347,7 +379,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "kernel": "pa_decode alone (tcgen05 paged decode; split units merged in-kernel)",
                      "achieved": round(achieved, 2), "peak": peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(dbytes),
+                     "traffic": recorded_traffic(dbytes, args.kv_dtype),
                      "algorithmic_bytes": dbytes},
         "gpu_launches": K * 2 * step.launches_per_step,
         "clocks": clk.summary(),

@@ -110,9 +110,13 @@ size_t pa_decode_workspace_size_ex(int32_t num_seqs, int32_t num_heads,
  *            partitions of partition_tokens, separate combine kernel); serves
  *            every supported shape.
  *  kernel 2: tensor-core kernel (tcgen05 MMA, TMA loads, persistent CTAs that
- *            each stream an equal share of 128-token chunks, in-kernel merge
- *            of split units); needs a bf16 cache, head_dim 128, block_size
- *            >= 8 and at most 1024 sequences, else PA_ERR_UNSUPPORTED.
+ *            each stream an equal share of 128-token (bf16) or 256-token
+ *            (e4m3) chunks, in-kernel merge of split units); needs head_dim
+ *            128, block_size >= 8 and at most 1024 sequences, else
+ *            PA_ERR_UNSUPPORTED.  For an e4m3 cache the MMAs take the cache
+ *            bytes as they are (kind::f8f6f4); q and the softmax weights are
+ *            split into e4m3 parts (three for q, two for the weights) whose
+ *            sum keeps them to about 2^-12 and 2^-8 relative.
  *            partition_tokens is ignored.  It sets workspace word 0 (int32)
  *            to a nonzero code if one of its bounded internal waits expired
  *            or a block id was out of range; the library never clears that

@@ -246,7 +246,7 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
   if (kernel == 2 || (kernel == 0 && tc_ok)) {
     if (!tc_ok)
       return pa_fail(PA_ERR_UNSUPPORTED,
-                     "pa_decode: tensor-core kernel needs a bf16 cache, head_dim 128, "
+                     "pa_decode: tensor-core kernel needs head_dim 128, "
                      "block_size >= 8 and at most 1024 sequences");
     const int nsm = num_sms();
     const size_t need = pa::tc_workspace_bytes(num_seqs, num_heads, max_ctx, nsm);
@@ -260,6 +260,9 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
     a.q = q;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
+    a.fp8 = fp8;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.workspace = workspace;

@@ -44,6 +44,15 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t codes) {
   return __half22float2(h);
 }
 
+// Two floats -> two e4m3 codes, round to nearest even, saturating to +-448
+// (low byte = lo, high byte = hi; the instruction puts its first source in
+// the upper byte).
+__device__ __forceinline__ uint16_t pack_e4m3x2_rn(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // Unpack 16 bytes of cache row into floats: 8 bf16 or 16 e4m3 values.
 template <bool FP8>
 struct Unpack16;

@@ -44,12 +44,15 @@ cudaError_t launch_decode_simt_fp8(const DecodeParams& p, int head_dim, int grou
 cudaError_t launch_decode_reduce(const DecodeParams& p, int head_dim,
                                  int num_seqs, cudaStream_t stream);
 
-// Tensor-core (tcgen05 + TMA) decode for a bf16 cache with head_dim 128.
+// Tensor-core (tcgen05 + TMA) decode for a bf16 or fp8-e4m3 cache with head_dim 128.
 struct TcLaunch {
   void* out;
   const void* q;
   const void* k_cache;
   const void* v_cache;
+  bool fp8;              // e4m3 cache with per-tensor k_scale / v_scale
+  const float* k_scale;  // device scalars (fp8 only)
+  const float* v_scale;
   const int32_t* block_tables;
   const int32_t* context_lens;
   void* workspace;  // >= tc_workspace_bytes(...)

@@ -115,6 +115,18 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f8f6f4 (8-bit inputs named in the
+// instruction descriptor, fp32 accumulate).
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread completes.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
@@ -133,6 +145,20 @@ __device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, float (&v)[8]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+// Warp-collective: 16 consecutive fp32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
@@ -159,6 +185,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool a_mn_ma
   return (1u << 4)                       // D format: f32
          | (1u << 7)                     // A format: bf16
          | (1u << 10)                    // B format: bf16
+         | ((a_mn_major ? 1u : 0u) << 15)  // A major-ness
+         | (0u << 16)                    // B K-major
+         | ((uint32_t)(n >> 3) << 17)    // N / 8
+         | ((uint32_t)(m >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor, kind::f8f6f4: fp32 accumulator, e4m3 A and B
+// (format code 0), A K-major or MN-major, B K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n, bool a_mn_major) {
+  return (1u << 4)                       // D format: f32
+         | (0u << 7)                     // A format: e4m3
+         | (0u << 10)                    // B format: e4m3
          | ((a_mn_major ? 1u : 0u) << 15)  // A major-ness
          | (0u << 16)                    // B K-major
          | ((uint32_t)(n >> 3) << 17)    // N / 8

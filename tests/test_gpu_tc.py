@@ -24,7 +24,7 @@ def _check(w, **kw):
     ref = harness.oracle_step(w)
     assert np.array_equal(got["k_cache"], ref["k_cache"])
     assert np.array_equal(got["v_cache"], ref["v_cache"])
-    return harness.assert_close(got["out"], ref["out"], False), got, ref
+    return harness.assert_close(got["out"], ref["out"], w.kv_dtype == "fp8"), got, ref
 
 
 @requires_gpu
@@ -140,3 +140,46 @@ def test_write_and_decode_matches_separate_calls():
         assert np.array_equal(harness.bits_from_dev(kc), got["k_cache"])
         assert np.array_equal(harness.bits_from_dev(vc), got["v_cache"])
         assert np.array_equal(out.float().cpu().numpy().astype(np.float64), got["out"])
+
+
+# ---- e4m3 cache: kind::f8f6f4 MMAs with q and P split into e4m3 parts ----
+
+@requires_gpu
+@pytest.mark.parametrize("block_size", [8, 16, 64, 256])
+def test_tc_fp8_block_sizes(block_size):
+    _check(synth.sweep(block_size, "fp8"))
+
+
+@requires_gpu
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (32, 8), (64, 8), (4, 2)])
+def test_tc_fp8_head_groups(hq, hkv):
+    lens = [3, 130, 700, 2000, 64, 1, 257]
+    w = synth.make(f"tc-fp8-heads-{hq}-{hkv}", lens, hq, hkv, 128, 16, kv_dtype="fp8", seed=47)
+    _check(w)
+
+
+@requires_gpu
+def test_tc_fp8_long_context_split_units():
+    _check(synth.longctx(kv_dtype="fp8"))
+
+
+@requires_gpu
+@pytest.mark.parametrize("qmult", [1e-3, 13.7, 77.3])
+def test_tc_fp8_query_magnitudes(qmult):
+    # the q warp scales each group's q by a power of two before splitting it
+    # into e4m3 parts; tiny and large q must come out as accurate as unit q
+    lens = [5, 129, 600, 1500, 40]
+    w = synth.make(f"tc-fp8-q{qmult}", lens, 32, 8, 128, 16, kv_dtype="fp8", seed=53)
+    qf = (w.q.astype(np.uint32) << np.uint32(16)).view(np.float32) * np.float32(qmult)
+    w.q = synth.bf16_bits(qf)
+    _check(w)
+
+
+@requires_gpu
+def test_tc_fp8_agrees_with_simt():
+    w = synth.make("tc-fp8-vs-simt", synth.llama8b_lengths(16), 32, 8, 128, 16,
+                   kv_dtype="fp8", seed=59)
+    _, got, ref = _check(w)
+    simt = harness.product_step(w, kernel=1)["out"]
+    harness.assert_close(simt, ref["out"], True)
+    assert np.max(np.abs(got["out"] - simt)) < 6e-2
