@@ -53,6 +53,24 @@ def parse():
     return ap.parse_args()
 
 
+# ---------------------------------------------------------------- ranks
+
+def slowest_over_ranks(values, dist, device):
+    """Each per-rank time replaced by its maximum over all ranks (the job
+    finishes with its slowest replica); identity without a process group."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_throughput(world, bytes_per_replica_step, seconds_per_step):
+    """Whole-job rate: every replica moves its own bytes in the slowest
+    replica's step time (weak scaling)."""
+    return world * bytes_per_replica_step / seconds_per_step
+
+
 # ---------------------------------------------------------------- workload
 
 class Step:
@@ -328,10 +346,7 @@ def run_ours(args, rank, world, local_rank):
     wr_ms = [ev[k][4].elapsed_time(ev[k][5]) for k in range(K)]
     mean_step = sum(step_ms) / K
     mean_dec = sum(dec_ms) / K
-    t = torch.tensor([mean_step, mean_dec], dtype=torch.float64, device=device)
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    mean_step, mean_dec = float(t[0]), float(t[1])
+    mean_step, mean_dec = slowest_over_ranks([mean_step, mean_dec], dist, device)
 
     # end-to-end through the public API with host buffers
     e2e = None
@@ -348,7 +363,7 @@ def run_ours(args, rank, world, local_rank):
     dbytes = step.decode_bytes()
     sbytes = dbytes + step.write_bytes()
     achieved = dbytes / (mean_dec * 1e-3) / 1e9
-    value = world * sbytes / (mean_step * 1e-3) / 1e9
+    value = job_throughput(world, sbytes, mean_step * 1e-3) / 1e9
     w = step.w
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -443,13 +458,10 @@ def run_e2e(step, args, device, dist):
         one()
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / args.steps
-    t = torch.tensor([dt], dtype=torch.float64, device=device)
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    dt = float(t[0])
+    dt = slowest_over_ranks([dt], dist, device)[0]
     world = dist.get_world_size() if dist else 1
     sbytes = step.decode_bytes() + step.write_bytes()
-    return {"value": round(world * sbytes / dt / 1e9, 2), "unit": "GB/s",
+    return {"value": round(job_throughput(world, sbytes, dt) / 1e9, 2), "unit": "GB/s",
             "us_per_step": round(dt * 1e6, 2), "h2d_bytes_per_step": bi,
             "d2h_bytes_per_step": bo}
 
