@@ -48,6 +48,12 @@ def parse():
     ap.add_argument("--kernel", type=int, default=0, help="decode kernel (0 auto, 1 SIMT, 2 tcgen05)")
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
                     help="KV cache type: bf16, or fp8-e4m3 with per-tensor scales")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default="llama8b",
+                    help="llama8b: the headline layer (batch 64); longctx: 8 sequences of "
+                         "4K..128K tokens; serving: 256 MHA sequences in groups of 8 sharing "
+                         "a 1024-token prefix")
+    ap.add_argument("--block-size", type=int, default=16,
+                    help="tokens per physical block (llama8b workload: 1, 16, 64, 256)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -73,15 +79,60 @@ def job_throughput(world, bytes_per_replica_step, seconds_per_step):
 
 # ---------------------------------------------------------------- workload
 
-class Step:
-    """Device-resident state of the headline decode step."""
+WORKLOADS = {
+    "llama8b": "llama8b-layer decode, batch 64, 32q/8kv heads, d=128",
+    "longctx": "long-context decode, 8 sequences of 4K-128K tokens, 32q/8kv heads, d=128",
+    "serving": "serving step, 256 MHA sequences (32q/32kv, d=128) in 32 groups of 8 sharing "
+               "a 1024-token prefix, suffixes U[16, 2048]",
+}
 
-    def __init__(self, device, partition=0, kernel=0, kv_dtype="bf16"):
+
+def build_workload(name, block_size, kv_dtype):
+    """Shapes, lengths and block tables of a workload (no K/V values).
+    Returns (workload, unique_tokens): the tokens whose K/V are stored once
+    (fewer than sum(context_lens) when sequences share prefix blocks)."""
+    from paged_kv_cache_108_gb300 import synth
+    if name == "llama8b":
+        w = synth.llama8b(block_size=block_size, kv_dtype=kv_dtype, with_data=False)
+        return w, int(np.sum(w.context_lens))
+    if name == "longctx":
+        w = synth.longctx(kv_dtype=kv_dtype, with_data=False)
+        return w, int(np.sum(w.context_lens))
+    # serving mix: each group's prefix blocks appear in all its members' tables
+    mix = synth.serving()
+    B, P = mix.block_size, mix.prefix_len
+    lens = (P + mix.suffix_lens).astype(np.int32)
+    pre_blocks = -(-P // B)
+    priv = [-(-int(n) // B) - P // B for n in lens]
+    used = mix.num_groups * pre_blocks + sum(priv)
+    num_blocks = int(math.ceil(1.2 * used))
+    perm = np.random.default_rng(mix.seed).permutation(num_blocks).astype(np.int32)
+    tables = np.zeros((mix.num_seqs, max(P // B + c for c in priv)), dtype=np.int32)
+    at = 0
+    for grp in range(mix.num_groups):
+        prefix = perm[at:at + pre_blocks]
+        at += pre_blocks
+        for i in range(grp * mix.group_size, (grp + 1) * mix.group_size):
+            tables[i, :P // B] = prefix[:P // B]
+            tables[i, P // B:P // B + priv[i]] = perm[at:at + priv[i]]
+            at += priv[i]
+    w = synth.Workload("serving", mix.num_heads, mix.num_kv_heads, mix.head_dim, B, kv_dtype,
+                       num_blocks, lens, tables, 1.0 / math.sqrt(mix.head_dim), mix.seed)
+    unique = mix.num_groups * P + int(np.sum(lens - P))
+    return w, unique
+
+
+class Step:
+    """Device-resident state of one decode step of a workload."""
+
+    def __init__(self, device, partition=0, kernel=0, kv_dtype="bf16", workload="llama8b",
+                 block_size=16):
         import torch
 
         from paged_kv_cache_108_gb300 import ops, pool, synth
         self.torch, self.ops, self.pool = torch, ops, pool
-        w = synth.llama8b(with_data=False, kv_dtype=kv_dtype)
+        w, self.unique_tokens = build_workload(workload, block_size, kv_dtype)
+        self.workload = workload
         self.w = w
         self.device = device
         self.partition, self.kernel = partition, kernel
@@ -104,8 +155,8 @@ class Step:
             self.k_cache, self.v_cache = caches
             self.k_scale, self.v_scale = scales
         else:
-            self.k_cache = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
-            self.v_cache = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+            self.k_cache = torch.randn(shape, generator=gen, device=device, dtype=torch.bfloat16)
+            self.v_cache = torch.randn(shape, generator=gen, device=device, dtype=torch.bfloat16)
         S = w.num_seqs
         self.q = torch.randn((S, H, d), generator=gen, device=device).to(torch.bfloat16)
         self.k_new = torch.randn((S, hkv, d), generator=gen, device=device).to(torch.bfloat16)
@@ -120,13 +171,17 @@ class Step:
         # the tensor-core decode (one launch, merge inside) serves this shape
         # unless the SIMT kernel is forced; SIMT adds a combine launch
         simt = kernel == 1
-        splits = 3360 > (partition or 256)
-        self.launches_per_step = 2 + (1 if simt and splits else 0)
+        G = H // hkv
+        tc = kernel == 2 or (kernel == 0 and d == 128 and B >= 8 and S <= 1024 and G in (1, 2, 4, 8))
+        splits = int(np.max(w.context_lens)) > (partition or 256)
+        self.launches_per_step = 2 + (1 if not tc and splits else 0)
 
-    # algorithmic bytes of one step (what the method must move)
-    def decode_bytes(self) -> int:
+    # algorithmic bytes of one step (what the method must move): K/V rows
+    # stored once are read once (shared prefix blocks count once)
+    def decode_bytes(self, logical=False) -> int:
         w = self.w
-        kv = int(np.sum(w.context_lens)) * w.num_kv_heads * w.head_dim * self.kv_bytes * 2
+        tokens = int(np.sum(w.context_lens)) if logical else self.unique_tokens
+        kv = tokens * w.num_kv_heads * w.head_dim * self.kv_bytes * 2
         qo = 2 * w.num_seqs * w.num_heads * w.head_dim * 2
         table = int(sum(math.ceil(n / w.block_size) for n in w.context_lens)) * 4
         return kv + qo + table + w.num_seqs * 4
@@ -277,7 +332,7 @@ def cpu_baseline_oracle(step, budget_s=10.0):
         reps += 1
     gbs = bytes_done / t_total / 1e9
     return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{reps} batches of {chunk} (sequence, kv-head) units of the llama8b step "
+            "sample": f"{reps} batches of {chunk} (sequence, kv-head) units of the {step.workload} step "
                       f"({bytes_done / 1e6:.0f} MB of KV, {t_total:.1f} s), fp64, {threads} threads"}
 
 
@@ -287,7 +342,8 @@ def run_ours(args, rank, world, local_rank):
     import torch
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
-    step = Step(device, args.partition, args.kernel, args.kv_dtype)
+    step = Step(device, args.partition, args.kernel, args.kv_dtype, args.workload,
+                args.block_size)
     stream = torch.cuda.current_stream()
     # L2 flush: read a buffer 4x the L2 size.  Reading (not writing) leaves
     # only clean lines behind, so the timed kernels do not pay for writing
@@ -373,14 +429,18 @@ def run_ours(args, rank, world, local_rank):
         "data": ("synthetic (seeded N(0,1) K/V quantised to e4m3 with scale amax/448, bf16 q; "
                  "lengths from the pages' seeded request mix)" if step.fp8 else
                  "synthetic (seeded N(0,1) bf16 K/V/q; lengths from the pages' seeded request mix)"),
-        "config": {"workload": "llama8b-layer decode, batch 64, 32q/8kv heads, d=128, "
+        "config": {"workload": f"{WORKLOADS[args.workload]}, "
                                f"{'e4m3 (per-tensor scale)' if step.fp8 else 'bf16'} KV, "
-                               "block 16, sum ctx 121416", "num_seqs": w.num_seqs,
+                               f"block {w.block_size}, sum ctx {int(np.sum(w.context_lens))}",
+                   "num_seqs": w.num_seqs,
                    "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "block_size": w.block_size,
                    "num_blocks": w.num_blocks, "sum_context": int(np.sum(w.context_lens)),
                    "partition_tokens": args.partition or "auto", "kernel": args.kernel or "auto",
                    "bytes_per_step": sbytes, "decode_bytes_per_step": dbytes,
+                   **({"decode_bytes_logical": step.decode_bytes(logical=True),
+                       "unique_context_tokens": step.unique_tokens}
+                      if step.unique_tokens != int(np.sum(w.context_lens)) else {}),
                    "l2": f"flushed between steps by reading a {L2_FLUSH_BYTES >> 20} MB buffer "
                          "(untimed)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -394,7 +454,10 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "kernel": "pa_decode alone (tcgen05 paged decode; split units merged in-kernel)",
                      "achieved": round(achieved, 2), "peak": peak, "peak_source": peak_src,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(dbytes, args.kv_dtype),
+                     # the ncu record covers the headline layer at block 16 only
+                     "traffic": (recorded_traffic(dbytes, args.kv_dtype)
+                                 if args.workload == "llama8b" and args.block_size == 16
+                                 else None),
                      "algorithmic_bytes": dbytes},
         "gpu_launches": K * 2 * step.launches_per_step,
         "clocks": clk.summary(),
