@@ -6,10 +6,13 @@
 // head map h -> h / G, online softmax; section "Performance considerations":
 // split the sequence across CTAs and merge), organised for Blackwell:
 //
-// Work split.  The KV of every (sequence, KV head) unit is cut into 128-token
-// chunks; all chunks of all units are numbered in (sequence, head, chunk)
-// order and each persistent CTA (one per SM) takes an equal contiguous range
-// of that numbering.  A unit whose chunks all fall in one CTA is finished
+// Work split.  The KV of every (sequence, KV head) unit is cut into chunks
+// (128 tokens for bf16, 256 for e4m3); all chunks of all units are numbered
+// in (head, sequence, chunk) order and each persistent CTA (one per SM) takes
+// an equal contiguous range of that numbering.  Head-major order puts the
+// units of one KV head side by side, so sequences forked from a common
+// prefix (adjacent in the batch) read their shared blocks within a few
+// microseconds of each other, mostly from L2.  A unit whose chunks all fall in one CTA is finished
 // there; otherwise each CTA writes an unnormalised partial (m, l, o) for its
 // piece ("segment"), and the last of the unit's CTAs to finish merges the
 // partials.  The arrival count of a unit is a 64-bit word tagged with a
@@ -105,8 +108,8 @@ struct Cfg {
                        B_Q_EMPTY = B_Q_FULL + 2, B_EPI = B_Q_EMPTY + 2, NBARS = B_EPI + 2;
   static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
-  static constexpr int OFF_SQ = OFF_ABORT + 4;     // [2] ints: sequences of the range's ends
-  static constexpr int OFF_QEXP = OFF_SQ + 8;      // [2] floats: 2^-e of each q tile (fp8)
+  static constexpr int OFF_SQ = OFF_ABORT + 4;     // [3] ints: sequences of the range's ends, first
+  static constexpr int OFF_QEXP = OFF_SQ + 12;     // [2] floats: 2^-e of each q tile (fp8)
   static constexpr int OFF_RED = OFF_QEXP + 8;     // [2][4][8] floats, chunk max
   static constexpr int OFF_LRED = OFF_RED + 2 * 4 * 8 * 4;   // [4][8] floats, epilogue sums
   static constexpr int OFF_CP = OFF_LRED + 4 * 8 * 4;        // chunk prefix per sequence, [S+1]
@@ -200,9 +203,11 @@ __device__ __forceinline__ int cta_of(long long k, long long K, int C) {
 // the pipeline still has work to hide it, and every CTA ends on whole units.
 template <int CH>
 struct ChunkWalk {
-  const int* cp;   // smem chunk prefix: cp[i] = chunks of sequences < i (all heads)
+  const int* cp;   // smem chunk prefix: cp[i] = chunks of sequences < i (one head)
   const int* nl;   // smem clamped context lengths
   int S, Hkv;
+  long long Ctot;  // chunks of one head over all sequences (cp[S])
+  int first_ne;    // first sequence with a chunk
   long long k;                 // current global chunk index
   long long lo0, hi0, lo1, hi1, lo2, hi2;  // the pieces, in visiting order
   long long cur_lo, cur_hi;    // the piece being visited
@@ -212,7 +217,7 @@ struct ChunkWalk {
   int sq1, g1, j1, sq2, g2;    // where pieces 1 and 2 start (piece 2 starts a unit)
 
   __device__ void load_unit() {
-    nch = (cp[seq + 1] - cp[seq]) / Hkv;
+    nch = cp[seq + 1] - cp[seq];
     n = nl[seq];
   }
   // position (seq, g, j) of chunk kk, given the sequence s holding it
@@ -220,9 +225,16 @@ struct ChunkWalk {
     k = kk;
     seq = s;
     load_unit();
-    const int r = (int)(kk - cp[s]);
-    g = r / nch;
-    j = r - g * nch;
+    g = (int)(kk / Ctot);
+    j = (int)(kk - g * Ctot - cp[s]);
+  }
+  // the unit after (q, h): the next sequence with chunks, or the next head
+  __device__ void next_unit(int& q, int& h) const {
+    do { ++q; } while (q < S && cp[q + 1] == cp[q]);
+    if (q == S) {
+      q = first_ne;
+      ++h;
+    }
   }
   // seq_lo / seq_hi: the sequences holding chunks lo and hi - 1
   __device__ void init(long long lo, long long hi, int seq_lo, int seq_hi) {
@@ -243,11 +255,8 @@ struct ChunkWalk {
     sq1 = seq; g1 = g; j1 = j;
     // the unit after the first one (a chunk exists there: head_hi < hi)
     sq2 = seq;
-    g2 = g + 1;
-    if (g2 == Hkv) {
-      g2 = 0;
-      do { ++sq2; } while (cp[sq2 + 1] == cp[sq2]);
-    }
+    g2 = g;
+    next_unit(sq2, g2);
     seek_in(seq_hi, hi - 1);
     const long long tail_lo = k - j;  // first chunk of the last unit (>= head_hi)
     lo0 = tail_lo; hi0 = hi;
@@ -281,11 +290,8 @@ struct ChunkWalk {
     }
     if (++j == nch) {
       j = 0;
-      if (++g == Hkv) {
-        g = 0;
-        do { ++seq; } while (cp[seq + 1] == cp[seq]);
-        load_unit();
-      }
+      next_unit(seq, g);
+      load_unit();
     }
   }
   __device__ bool first_of_segment() const { return j == 0 || k == cur_lo; }
@@ -373,11 +379,11 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
   for (int i = tid; i < S; i += NTHREADS) {
     const int n = i == tid ? n_own : min(__ldg(&p.context_lens[i]), cap);
     nl[i] = n;
-    cp[i] = n > 0 ? Hkv * ((n + CH - 1) / CH) : 0;
+    cp[i] = n > 0 ? (n + CH - 1) / CH : 0;
   }
   __syncthreads();
   if (warp == 0) {
-    // exclusive prefix in place: cp[i] = sum_{i' < i} H_kv * ceil(n_i' / CH)
+    // exclusive prefix in place: cp[i] = sum_{i' < i} ceil(n_i' / CH)
     int carry = 0;
     for (int base = 0; base < S; base += 32) {
       const int i = base + lane;
@@ -397,23 +403,29 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm.base + OFF_TMEM);
-  const long long Ktot = cp[S];
+  const long long Ctot = cp[S];         // chunks of one KV head
+  const long long Ktot = Ctot * Hkv;
   // only min(CTAs, chunks) CTAs take work, so every working CTA owns at least
   // one chunk and a unit never spans more CTAs than it has chunks
   const int C = (int)(Ktot < p.num_ctas ? Ktot : p.num_ctas);
   const long long lo = (int)blockIdx.x < C ? range_lo(blockIdx.x, Ktot, C) : 0;
   const long long hi = (int)blockIdx.x < C ? range_lo(blockIdx.x + 1, Ktot, C) : 0;
-  // the sequences holding chunks lo and hi - 1, found by all threads at once
+  // the sequences holding chunks lo and hi - 1 and the first sequence with
+  // chunks, found by all threads at once (chunk k of the (head, sequence,
+  // chunk) numbering is chunk k mod Ctot of its head)
   int* sq = reinterpret_cast<int*>(sm.base + OFF_SQ);
   if (lo < hi) {
+    const long long r_lo = lo % Ctot, r_hi = (hi - 1) % Ctot;
     for (int i = tid; i < S; i += NTHREADS) {
       const int a = cp[i], b = cp[i + 1];
-      if (a <= lo && lo < b) sq[0] = i;
-      if (a < hi && hi <= b) sq[1] = i;
+      if (a <= r_lo && r_lo < b) sq[0] = i;
+      if (a <= r_hi && r_hi < b) sq[1] = i;
+      if (a == 0 && b > 0) sq[2] = i;
     }
   }
   __syncthreads();
   const int seq_lo = lo < hi ? sq[0] : 0, seq_hi = lo < hi ? sq[1] : 0;
+  const int first_ne = lo < hi ? sq[2] : 0;
   if (warp < 4) {
     // empty sequences get zero rows (spread over the CTAs)
     for (int i = blockIdx.x; i < S; i += gridDim.x) {
@@ -429,6 +441,8 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
   walk.S = S;
   walk.Hkv = Hkv;
   walk.nl = nl;
+  walk.Ctot = Ctot;
+  walk.first_ne = first_ne;
 
   if (warp == 4) {
     // ================= producer =================
