@@ -148,3 +148,58 @@ def write_and_decode(key, value, slot_mapping, out, q, k_cache, v_cache, block_t
         int(block_tables.shape[1]), _dev(context_lens, "context_lens", torch.int32), num_seqs,
         num_heads, ctypes.c_float(scale), ks, vs, ws_ptr, ws_bytes, _stream(stream)))
     return out
+
+
+class StepGraph:
+    """One decode step captured once as a CUDA graph over fixed buffers.
+
+    The graph holds, in stream order: the host-to-device copies in ``h2d``
+    (pairs ``(device_tensor, pinned_host_tensor)``), ``write_and_decode`` on
+    the given tensors (cache write of the new tokens, then paged decode), and
+    the device-to-host copies in ``d2h`` (pairs ``(pinned_host_tensor,
+    device_tensor)``).  ``replay()`` re-runs all of it on whatever the buffers
+    hold, for about one host call's cost; shapes and pointers are fixed at
+    capture.  The pages call the per-step host-to-device staging of step
+    metadata critical-path work ("4.6 PagedAttention & KV-Cache Memory
+    Management", section "From Python bookkeeping to GPU tensors"); a
+    captured step issues it with the kernels in one submission.
+
+    The decode kernel's merge counters carry a per-launch tag and are left
+    at count zero by every completed launch, so replaying the same captured
+    launch is safe; after a launch that reported an error in workspace word 0
+    the workspace must be re-zeroed before the next replay."""
+
+    def __init__(self, key, value, slot_mapping, out, q, k_cache, v_cache, block_tables,
+                 context_lens, scale, k_scale=None, v_scale=None, workspace=None, h2d=(),
+                 d2h=()):
+        self._h2d = list(h2d)
+        self._d2h = list(d2h)
+        for dev_t, host_t in self._h2d:
+            _dev(dev_t, "h2d destination")
+            if host_t.is_cuda or not host_t.is_pinned():
+                raise ValueError("h2d sources must be pinned host tensors")
+        for host_t, dev_t in self._d2h:
+            _dev(dev_t, "d2h source")
+            if host_t.is_cuda or not host_t.is_pinned():
+                raise ValueError("d2h destinations must be pinned host tensors")
+        self._args = (key, value, slot_mapping, out, q, k_cache, v_cache, block_tables,
+                      context_lens, scale, k_scale, v_scale, workspace)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self._body()  # eager run: per-kernel attributes are set before capture
+        torch.cuda.current_stream().wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._body()
+
+    def _body(self):
+        for dev_t, host_t in self._h2d:
+            dev_t.copy_(host_t, non_blocking=True)
+        write_and_decode(*self._args)
+        for host_t, dev_t in self._d2h:
+            host_t.copy_(dev_t, non_blocking=True)
+
+    def replay(self):
+        """Run the captured step on the current stream (asynchronous)."""
+        self.graph.replay()
