@@ -22,17 +22,17 @@
 // word at (epoch, 0), so replaying the same launch also starts from zero.
 // Load balance is one chunk, whatever the mix of context lengths.
 //
-// Warp roles (224 threads):
+// Warp roles (256 threads):
 //   warps 0-3  softmax + epilogue: thread t owns TMEM lane t (a token of the
 //              logits tile, a d-element of the output tile);
 //   warp 4     producer: per chunk, TMA tensor loads of each physical block's
-//              K and V rows (4-D tensor map [blocks, block_size, H_kv, d],
-//              128-byte swizzle, two 64-column halves) into a 3-stage ring,
-//              and per segment a TMA load of the group's query rows;
+//              K rows (and, for an e4m3 cache, V rows; 4-D tensor map
+//              [blocks, block_size, H_kv, d], 128-byte swizzle, 128-byte-wide
+//              boxes) into a 3-stage ring and, for bf16, each segment's q rows;
 //   warp 5     TMEM allocation and the single MMA-issuing thread;
 //   warp 6     merge warp: counts finished pieces of split units and merges
-//              a unit's pieces when its last piece is done.
-//
+//              a unit's pieces when its last piece is done;
+//   warp 7     bf16: a second producer for the V rows; e4m3: the q warp.
 // Per chunk c (double-buffered TMEM tiles S[c&1], O[c&1] and smem P[c&1]):
 //   S = K_c q^T         tcgen05.mma M=128 tokens, N=16 (query heads padded),
 //                       K=128 (d); A = K tile (K-major), B = q tile (K-major)
@@ -93,7 +93,13 @@ struct Cfg {
   static constexpr int O_COL = 2 * S_W;
   static constexpr int TMEM_COLS = FP8 ? 256 : 64;
   static constexpr int PTILE_B = NQ * CH * ELT;
-  static constexpr int NTHREADS = FP8 ? 256 : 224;  // fp8: warp 7 prepares q
+  // bf16: two producer warps issue the TMA loads, warp 4 the K rows (and
+  // q) and warp 7 the V rows (measured 4 % faster on the MHA serving mix,
+  // equal elsewhere).  fp8: warp 4 issues both (a second producer measured
+  // slower there) and warp 7 prepares q.
+  static constexpr bool TWO_PROD = !FP8;
+  static constexpr int VPROD = TWO_PROD ? 7 : 4;
+  static constexpr int NTHREADS = 256;
 
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NST * TILE_B;
@@ -114,8 +120,8 @@ struct Cfg {
   static constexpr int OFF_LRED = OFF_RED + 2 * 4 * 8 * 4;   // [4][8] floats, epilogue sums
   static constexpr int OFF_CP = OFF_LRED + 4 * 8 * 4;        // chunk prefix per sequence, [S+1]
   static constexpr int OFF_NLEN = OFF_CP + (kMaxSeqs + 1) * 4;  // clamped context lengths
-  static constexpr int OFF_TAB = OFF_NLEN + kMaxSeqs * 4;       // block-id ring
-  static constexpr int SMEM_BYTES = OFF_TAB + TAB_SLOTS * TAB_W * 4 + 1024;  // + alignment slack
+  static constexpr int OFF_TAB = OFF_NLEN + kMaxSeqs * 4;       // block-id rings (K, V producer)
+  static constexpr int SMEM_BYTES = OFF_TAB + 2 * TAB_SLOTS * TAB_W * 4 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
   static_assert(OFF_BAR % 1024 == 0, "tiles stay 1024-byte aligned");
 };
@@ -361,7 +367,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
     *sm.abort_flag() = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 4 && lane == 0) {
+  if ((warp == 4 || warp == Cf::VPROD) && lane == 0) {
     ptx::prefetch_tmap(&tm_k);
     ptx::prefetch_tmap(&tm_v);
     ptx::prefetch_tmap(&tm_q);
@@ -444,14 +450,17 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
   walk.Ctot = Ctot;
   walk.first_ne = first_ne;
 
-  if (warp == 4) {
-    // ================= producer =================
+  if (warp == 4 || warp == Cf::VPROD) {
+    // ================= producers (K: warp 4, V: warp VPROD) =================
     // Block ids travel through a shared-memory ring filled by 4-byte cp.async
     // copies TAB_AHEAD chunks ahead (lane b copies and later uses box b's id;
     // block_size >= 8 keeps a chunk within 32 boxes), so table reads overlap
     // instead of following one another.
-    const uint32_t tab = sm.base_u32 + OFF_TAB;
-    const int* tab_s = reinterpret_cast<const int*>(sm.base + OFF_TAB);
+    const bool isk = warp == 4;                      // loads K (and q)
+    const bool isv = !Cf::TWO_PROD || warp != 4;     // loads V
+    const int tab_off = OFF_TAB + (isk ? 0 : TAB_SLOTS * TAB_W * 4);
+    const uint32_t tab = sm.base_u32 + tab_off;
+    const int* tab_s = reinterpret_cast<const int*>(sm.base + tab_off);
     auto fetch_ids = [&](const Walk& w, int slot) {
       const int nb = (w.valid() + p.box_tok - 1) >> p.log2_box;
       if (lane < nb)
@@ -479,7 +488,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
       cp_async_wait<TAB_AHEAD - 1>();  // this chunk's ids have landed
       const int phys_in = lane < nbox ? tab_s[(local % TAB_SLOTS) * TAB_W + lane] : 0;
       if (!wait_bar(sm, sm.bar(B_EMPTY + s), ph ^ 1, p.err, 1)) break;
-      if (!FP8 && walk.first_of_segment()) {
+      if (!FP8 && isk && walk.first_of_segment()) {
         const int qs = seg & 1;
         const uint32_t qph = (seg >> 1) & 1;
         if (!wait_bar(sm, sm.bar(B_Q_EMPTY + qs), qph ^ 1, p.err, 2)) break;
@@ -504,19 +513,25 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
         phys = 0;
       }
       if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_K + s), bytes);
-        ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_V + s), bytes);
+        if (isk) ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_K + s), bytes);
+        if (isv) ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_V + s), bytes);
       }
       __syncwarp();
       if (lane < nbox) {
         // a token row of one head is 128 bytes in fp8 (one box) and 256 bytes
         // in bf16 (two 64-column boxes, one per 128-byte column block)
-        ptx::tma_load_4d(kdst + row, &tm_k, sm.bar(B_FULL_K + s), 0, walk.g, off, phys);
-        if (!FP8)
-          ptx::tma_load_4d(kdst + HALF_B + row, &tm_k, sm.bar(B_FULL_K + s), 64, walk.g, off, phys);
-        ptx::tma_load_4d(vdst + row, &tm_v, sm.bar(B_FULL_V + s), 0, walk.g, off, phys);
-        if (!FP8)
-          ptx::tma_load_4d(vdst + HALF_B + row, &tm_v, sm.bar(B_FULL_V + s), 64, walk.g, off, phys);
+        if (isk) {
+          ptx::tma_load_4d(kdst + row, &tm_k, sm.bar(B_FULL_K + s), 0, walk.g, off, phys);
+          if (!FP8)
+            ptx::tma_load_4d(kdst + HALF_B + row, &tm_k, sm.bar(B_FULL_K + s), 64, walk.g, off,
+                             phys);
+        }
+        if (isv) {
+          ptx::tma_load_4d(vdst + row, &tm_v, sm.bar(B_FULL_V + s), 0, walk.g, off, phys);
+          if (!FP8)
+            ptx::tma_load_4d(vdst + HALF_B + row, &tm_v, sm.bar(B_FULL_V + s), 64, walk.g, off,
+                             phys);
+        }
       }
       if (!ahead.done()) {
         fetch_ids(ahead, (local + TAB_AHEAD) % TAB_SLOTS);
@@ -529,10 +544,10 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
     __syncwarp();
     if (lane == 0) {
       for (int l = max(0, local - NST); l < local; ++l) {
-        drain_bar(sm.bar(B_FULL_K + l % NST), (l / NST) & 1);
-        drain_bar(sm.bar(B_FULL_V + l % NST), (l / NST) & 1);
+        if (isk) drain_bar(sm.bar(B_FULL_K + l % NST), (l / NST) & 1);
+        if (isv) drain_bar(sm.bar(B_FULL_V + l % NST), (l / NST) & 1);
       }
-      if (!FP8)
+      if (!FP8 && isk)
         for (int sg = max(0, seg - 2); sg < seg; ++sg)
           drain_bar(sm.bar(B_Q_FULL + (sg & 1)), (sg >> 1) & 1);
     }
