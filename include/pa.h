@@ -272,6 +272,64 @@ pa_status pa_slot_mapping(const int32_t* block_tables, int32_t num_seqs,
                           int32_t num_tokens, int32_t* slot_mapping);
 
 /* ------------------------------------------------------------------------
+ * pa_swap_blocks -- copy whole blocks between two caches of the same block
+ * shape: dst[d] = src[s] for K and V, for every (s, d) pair.  An exhausted
+ * pool must preempt a sequence ([LSB] BlockManager.allocate), and the
+ * serving engine keeps a swap space of host RAM that preempted blocks move
+ * into ([LSB] "The libraries that implement this", the swap-space knob);
+ * they move back when the request resumes.  One cache is normally this GPU's pool and
+ * the other a pinned host buffer of the same block layout (cudaHostAlloc /
+ * torch pin_memory: with unified addressing the kernel reaches it through
+ * its host pointer over the C2C link); both may also be device pools.
+ * One kernel moves all pairs (16-byte vectors, one CTA per pair, K|V and
+ * 32 KiB piece of the block): no per-block copy calls.
+ *
+ *  dst_k, dst_v      destination caches, [dst_num_blocks, B, H_kv, d].
+ *  src_k, src_v      source caches, [src_num_blocks, B, H_kv, d].
+ *  block_shape       B, H_kv, d and dtype (its num_blocks is ignored).
+ *  block_pairs       device (or pinned host), [num_pairs, 2] int32 (src, dst);
+ *                    pairs naming a block outside either cache are skipped.
+ *                    Pairs must not write one destination block twice, and
+ *                    source and destination blocks must not overlap.
+ *  Returns PA_ERR_INVALID on bad sizes / NULL / misaligned pointers; runs
+ *  asynchronously on `stream`; the caller keeps every buffer alive until
+ *  the copy has run.
+ * ---------------------------------------------------------------------- */
+pa_status pa_swap_blocks(void* dst_k, void* dst_v, int32_t dst_num_blocks, const void* src_k,
+                         const void* src_v, int32_t src_num_blocks, pa_cache_desc block_shape,
+                         const int32_t* block_pairs, int32_t num_pairs, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_step_prepare -- a decode step's metadata, built on the device.
+ * [LSB] "From Python bookkeeping to GPU tensors" rebuilds the slot mapping
+ * and block tables on the host every step and copies them over, critical-
+ * path work; here the tables and context lengths stay on the device and one
+ * kernel updates them in place.  Per sequence i, in this order:
+ *   1. every update (seq, idx, block) with seq == i sets
+ *      block_tables[i][idx] = block (idx outside [0, max_blocks) is skipped);
+ *   2. context_lens[i] += advance;
+ *   3. slot_mapping[i] = table[i][(n-1)/B] * B + (n-1) % B for n =
+ *      context_lens[i], the slot of the sequence's newest token ([LSB]
+ *      BlockManager.slot_index), or -1 (pa_reshape_and_cache skips it) when
+ *      n <= 0, (n-1)/B >= max_blocks, the entry is negative, or the slot
+ *      does not fit in int32.
+ *
+ *  block_tables   device, [num_seqs, max_blocks_per_seq] int32, updated.
+ *  context_lens   device, [num_seqs] int32, advanced in place.
+ *  table_updates  device, [num_updates, 3] int32 (seq, logical block,
+ *                 physical block) chosen by the host pool; may be NULL when
+ *                 num_updates == 0.  Updates are not checked against a pool.
+ *  advance        tokens added to every context length first (0 or more).
+ *  slot_mapping   device, [num_seqs] int32, written.
+ *  Returns PA_ERR_INVALID on bad sizes / NULL / misaligned pointers; runs
+ *  asynchronously on `stream` and allocates nothing.
+ * ---------------------------------------------------------------------- */
+pa_status pa_step_prepare(int32_t* block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
+                          int32_t block_size, int32_t* context_lens,
+                          const int32_t* table_updates, int32_t num_updates, int32_t advance,
+                          int32_t* slot_mapping, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Host-side block pool (off the hot path; not thread-safe: one owner).
  * Free queue is FIFO: allocation takes from the head, blocks whose ref count
  * drops to 0 join the tail.  [PKV] "Implementation" (BlockPool: deque free

@@ -61,6 +61,8 @@ SIGNATURES = {
     "pa_write_and_decode": (I32, [P, P, P, I32, P, P, P, P, CacheDesc, P, I32, P, I32, I32,
                                   ctypes.c_float, P, P, P, SIZE, P]),
     "pa_copy_blocks": (I32, [P, P, CacheDesc, P, I32, P]),
+    "pa_step_prepare": (I32, [P, I32, I32, I32, P, P, I32, I32, P, P]),
+    "pa_swap_blocks": (I32, [P, P, I32, P, P, I32, CacheDesc, P, I32, P]),
     "pa_slot_mapping": (I32, [PI32, I32, I32, I32, PI32, PI32, I32, PI32]),
     "pa_pool_create": (P, [I32]),
     "pa_pool_create_ordered": (P, [I32, PI32]),

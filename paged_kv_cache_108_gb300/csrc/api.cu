@@ -389,4 +389,54 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, pa_cache_desc cache,
                      fn);
 }
 
+pa_status pa_swap_blocks(void* dst_k, void* dst_v, int32_t dst_num_blocks, const void* src_k,
+                         const void* src_v, int32_t src_num_blocks, pa_cache_desc block_shape,
+                         const int32_t* block_pairs, int32_t num_pairs, pa_stream_t stream) {
+  const char* fn = "pa_swap_blocks";
+  pa_cache_desc c = block_shape;
+  c.num_blocks = dst_num_blocks;
+  pa_status st = check_cache(c, fn);
+  if (st != PA_OK) return st;
+  c.num_blocks = src_num_blocks;
+  if ((st = check_cache(c, fn)) != PA_OK) return st;
+  if (num_pairs < 0) return pa_fail(PA_ERR_INVALID, "pa_swap_blocks: num_pairs < 0");
+  if (num_pairs == 0) return PA_OK;
+  if (!dst_k || !dst_v || !src_k || !src_v || !block_pairs)
+    return pa_fail(PA_ERR_INVALID, "pa_swap_blocks: NULL pointer");
+  if (!aligned(dst_k, 16) || !aligned(dst_v, 16) || !aligned(src_k, 16) || !aligned(src_v, 16) ||
+      !aligned(block_pairs, 4))
+    return pa_fail(PA_ERR_INVALID, "pa_swap_blocks: misaligned pointer");
+  const int64_t elem = block_shape.dtype == PA_KV_FP8_E4M3 ? 1 : 2;
+  const int64_t block_bytes =
+      (int64_t)block_shape.block_size * block_shape.num_kv_heads * block_shape.head_dim * elem;
+  return cuda_status(pa::launch_copy_blocks_between(dst_k, dst_v, dst_num_blocks, src_k, src_v,
+                                                    src_num_blocks, block_bytes, block_pairs,
+                                                    num_pairs,
+                                                    reinterpret_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+pa_status pa_step_prepare(int32_t* block_tables, int32_t num_seqs, int32_t max_blocks_per_seq,
+                          int32_t block_size, int32_t* context_lens,
+                          const int32_t* table_updates, int32_t num_updates, int32_t advance,
+                          int32_t* slot_mapping, pa_stream_t stream) {
+  const char* fn = "pa_step_prepare";
+  if (num_seqs < 0 || num_updates < 0 || max_blocks_per_seq <= 0 || block_size <= 0)
+    return pa_fail(PA_ERR_INVALID, "pa_step_prepare: bad sizes");
+  if (advance < 0) return pa_fail(PA_ERR_INVALID, "pa_step_prepare: advance < 0");
+  if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX)
+    return pa_fail(PA_ERR_UNSUPPORTED, "pa_step_prepare: max_blocks_per_seq * block_size too large");
+  if (num_seqs == 0) return PA_OK;
+  if (!block_tables || !context_lens || !slot_mapping || (num_updates > 0 && !table_updates))
+    return pa_fail(PA_ERR_INVALID, "pa_step_prepare: NULL pointer");
+  if (!aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(slot_mapping, 4) ||
+      (table_updates && !aligned(table_updates, 4)))
+    return pa_fail(PA_ERR_INVALID, "pa_step_prepare: misaligned pointer");
+  return cuda_status(pa::launch_step_prepare(block_tables, max_blocks_per_seq, block_size,
+                                             context_lens, num_seqs, table_updates, num_updates,
+                                             advance, slot_mapping,
+                                             reinterpret_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
 }  // extern "C"

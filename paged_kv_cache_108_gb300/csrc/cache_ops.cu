@@ -81,20 +81,25 @@ __global__ void __launch_bounds__(256)
 constexpr int kCopyThreads = 256;
 constexpr int64_t kCopyChunk = 32 * 1024;  // bytes per CTA
 
+// Block copies between two caches of the same block shape (the same cache
+// for copy-on-write; a device cache and a pinned host cache for a swap).
+// Grid: (pair, K|V, 32 KiB piece of the block).  Pairs naming a block
+// outside either cache are skipped.
 __global__ void __launch_bounds__(kCopyThreads)
-    copy_blocks_kernel(char* __restrict__ k_cache, char* __restrict__ v_cache,
-                       int64_t block_bytes, int num_blocks,
-                       const int32_t* __restrict__ pairs) {
+    copy_blocks_kernel(char* __restrict__ dst_k, char* __restrict__ dst_v, int dst_blocks,
+                       const char* __restrict__ src_k, const char* __restrict__ src_v,
+                       int src_blocks, int64_t block_bytes, const int32_t* __restrict__ pairs) {
   const int pi = blockIdx.x;
-  char* base = blockIdx.y ? v_cache : k_cache;
+  const char* sbase = blockIdx.y ? src_v : src_k;
+  char* dbase = blockIdx.y ? dst_v : dst_k;
   const int src = pairs[2 * pi];
   const int dst = pairs[2 * pi + 1];
-  if ((unsigned)src >= (unsigned)num_blocks || (unsigned)dst >= (unsigned)num_blocks) return;
+  if ((unsigned)src >= (unsigned)src_blocks || (unsigned)dst >= (unsigned)dst_blocks) return;
   const int64_t off = (int64_t)blockIdx.z * kCopyChunk;
   if (off >= block_bytes) return;
   const int64_t len = min(kCopyChunk, block_bytes - off) / 16;
-  const uint4* s = reinterpret_cast<const uint4*>(base + (int64_t)src * block_bytes + off);
-  uint4* d = reinterpret_cast<uint4*>(base + (int64_t)dst * block_bytes + off);
+  const uint4* s = reinterpret_cast<const uint4*>(sbase + (int64_t)src * block_bytes + off);
+  uint4* d = reinterpret_cast<uint4*>(dbase + (int64_t)dst * block_bytes + off);
   constexpr int U = 8;
   for (int64_t j0 = 0; j0 < len; j0 += (int64_t)U * kCopyThreads) {
     uint4 tmp[U];
@@ -111,7 +116,57 @@ __global__ void __launch_bounds__(kCopyThreads)
   }
 }
 
+// Step metadata on the device ("4.6 PagedAttention & KV-Cache Memory
+// Management", section "From Python bookkeeping to GPU tensors": the slot
+// mapping and block tables are rebuilt every step; here they change in place
+// on the device).  Thread i owns sequence i: it applies the block-table
+// updates addressed to its sequence (the host pool chose the blocks), adds
+// `advance` to its context length, and computes the slot of its newest token,
+//   slot = table[i][(n - 1) / B] * B + (n - 1) % B,
+// or -1 when n <= 0, the position lies past the table, or the entry is < 0.
+__global__ void step_prepare_kernel(int32_t* __restrict__ block_tables, int max_blocks,
+                                    int block_size, int32_t* __restrict__ context_lens,
+                                    int num_seqs, const int32_t* __restrict__ updates,
+                                    int num_updates, int advance,
+                                    int32_t* __restrict__ slot_mapping) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= num_seqs) return;
+  int32_t* row = block_tables + (int64_t)i * max_blocks;
+  for (int u = 0; u < num_updates; ++u) {
+    if (updates[3 * u] != i) continue;
+    const int idx = updates[3 * u + 1];
+    if ((unsigned)idx < (unsigned)max_blocks) row[idx] = updates[3 * u + 2];
+  }
+  int n = context_lens[i];
+  if (advance) {
+    n += advance;
+    context_lens[i] = n;
+  }
+  int slot = -1;
+  if (n > 0) {
+    const int pos = n - 1;
+    const int lb = pos / block_size;
+    if (lb < max_blocks) {
+      const int blk = row[lb];
+      const int64_t sl = (int64_t)blk * block_size + pos % block_size;
+      if (blk >= 0 && sl <= 0x7fffffff) slot = (int)sl;
+    }
+  }
+  slot_mapping[i] = slot;
+}
+
 }  // namespace
+
+cudaError_t launch_step_prepare(int32_t* block_tables, int max_blocks, int block_size,
+                                int32_t* context_lens, int num_seqs, const int32_t* updates,
+                                int num_updates, int advance, int32_t* slot_mapping,
+                                cudaStream_t stream) {
+  const int threads = 128;
+  step_prepare_kernel<<<(num_seqs + threads - 1) / threads, threads, 0, stream>>>(
+      block_tables, max_blocks, block_size, context_lens, num_seqs, updates, num_updates,
+      advance, slot_mapping);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value,
                                      void* k_cache, void* v_cache,
@@ -140,10 +195,20 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value,
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int64_t block_bytes,
                                int num_blocks, const int32_t* pairs, int num_pairs,
                                cudaStream_t stream) {
+  return launch_copy_blocks_between(k_cache, v_cache, num_blocks, k_cache, v_cache, num_blocks,
+                                    block_bytes, pairs, num_pairs, stream);
+}
+
+cudaError_t launch_copy_blocks_between(void* dst_k, void* dst_v, int dst_blocks,
+                                       const void* src_k, const void* src_v, int src_blocks,
+                                       int64_t block_bytes, const int32_t* pairs, int num_pairs,
+                                       cudaStream_t stream) {
   const int64_t chunks = (block_bytes + kCopyChunk - 1) / kCopyChunk;
   dim3 grid(num_pairs, 2, (unsigned)chunks);
   copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(
-      static_cast<char*>(k_cache), static_cast<char*>(v_cache), block_bytes, num_blocks, pairs);
+      static_cast<char*>(dst_k), static_cast<char*>(dst_v), dst_blocks,
+      static_cast<const char*>(src_k), static_cast<const char*>(src_v), src_blocks, block_bytes,
+      pairs);
   return cudaGetLastError();
 }
 

@@ -74,6 +74,16 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value,
                                      const float* v_scale,
                                      cudaStream_t stream);
 
+cudaError_t launch_step_prepare(int32_t* block_tables, int max_blocks, int block_size,
+                                int32_t* context_lens, int num_seqs, const int32_t* updates,
+                                int num_updates, int advance, int32_t* slot_mapping,
+                                cudaStream_t stream);
+
+cudaError_t launch_copy_blocks_between(void* dst_k, void* dst_v, int dst_blocks,
+                                       const void* src_k, const void* src_v, int src_blocks,
+                                       int64_t block_bytes, const int32_t* pairs, int num_pairs,
+                                       cudaStream_t stream);
+
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache,
                                int64_t block_bytes, int num_blocks,
                                const int32_t* pairs, int num_pairs,

@@ -126,6 +126,58 @@ def copy_blocks(k_cache, v_cache, block_pairs, stream=None) -> None:
                                          desc, ptr, n, _stream(stream)))
 
 
+def _any_ptr(t: torch.Tensor, name: str) -> int:
+    """Pointer of a contiguous CUDA tensor or pinned host tensor."""
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or a pinned host tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def swap_blocks(dst_k, dst_v, src_k, src_v, block_pairs, stream=None) -> None:
+    """dst[d] = src[s] for each (s, d) row of ``block_pairs`` [n, 2] int32,
+    between two caches of the same block shape (device pool <-> pinned host
+    swap space, either direction)."""
+    for a, b in ((dst_k, dst_v), (src_k, src_v), (dst_k, src_k)):
+        if a.shape[1:] != b.shape[1:] or a.dtype != b.dtype:
+            raise ValueError("caches must share block shape and dtype")
+    if dst_k.shape != dst_v.shape or src_k.shape != src_v.shape:
+        raise ValueError("K and V caches of a side must have the same shape")
+    shape = cache_desc(dst_k)
+    n = int(block_pairs.shape[0]) if block_pairs.dim() == 2 else int(block_pairs.numel()) // 2
+    if n == 0:
+        return
+    if block_pairs.dtype != torch.int32:
+        raise ValueError("block_pairs must be int32")
+    _lib.check(_lib.lib().pa_swap_blocks(
+        _any_ptr(dst_k, "dst_k"), _any_ptr(dst_v, "dst_v"), int(dst_k.shape[0]),
+        _any_ptr(src_k, "src_k"), _any_ptr(src_v, "src_v"), int(src_k.shape[0]), shape,
+        _any_ptr(block_pairs, "block_pairs"), n, _stream(stream)))
+
+
+def step_prepare(block_tables, context_lens, block_size, slot_mapping, updates=None,
+                 advance=0, stream=None) -> None:
+    """Device-side step metadata: apply ``updates`` ([n, 3] int32 rows of
+    (sequence, logical block, physical block)) to ``block_tables``, add
+    ``advance`` to every context length, and write each sequence's newest
+    token slot into ``slot_mapping`` (-1 where there is none)."""
+    if block_tables.dim() != 2:
+        raise ValueError("block_tables must be [num_seqs, max_blocks_per_seq]")
+    num_seqs, max_blocks = block_tables.shape
+    if context_lens.numel() != num_seqs or slot_mapping.numel() != num_seqs:
+        raise ValueError("context_lens and slot_mapping need one entry per sequence")
+    n_up, up_ptr = 0, None
+    if updates is not None and updates.numel() > 0:
+        if updates.dim() != 2 or updates.shape[1] != 3:
+            raise ValueError("updates must be [n, 3] (sequence, logical block, physical block)")
+        n_up, up_ptr = int(updates.shape[0]), _dev(updates, "updates", torch.int32)
+    _lib.check(_lib.lib().pa_step_prepare(
+        _dev(block_tables, "block_tables", torch.int32), int(num_seqs), int(max_blocks),
+        int(block_size), _dev(context_lens, "context_lens", torch.int32), up_ptr, n_up,
+        int(advance), _dev(slot_mapping, "slot_mapping", torch.int32), _stream(stream)))
+
+
 def write_and_decode(key, value, slot_mapping, out, q, k_cache, v_cache, block_tables,
                      context_lens, scale, k_scale=None, v_scale=None, workspace=None,
                      stream=None):
