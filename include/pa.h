@@ -369,6 +369,42 @@ pa_status pa_pool_free(pa_pool* pool, const int32_t* blocks, int32_t n);
  * out-of-range block. */
 pa_status pa_pool_cow(pa_pool* pool, int32_t block, int32_t* out_dst);
 
+/* Prefix caching across requests, full blocks only.  The pages make the
+ * full block the unit of sharing ([PKV] copy-on-write exercise: vLLM V1
+ * shares only full blocks and each answer writes into its own block) and
+ * point to cross-request reuse as the generalisation of shared prompt blocks
+ * ([LSB] "Copy-on-write for shared prefixes"; "How Paging Unlocks
+ * High-Throughput Serving": a system prompt stored once, reused by thousands
+ * of requests).  The pages do not fix how a block is recognised; this pool
+ * keys a full block by (parent block, the parent's generation, its B token
+ * ids).  A block's generation advances each time it is handed out fresh,
+ * which also drops its own entry, so a match always names the same content.
+ * Freed cached blocks stay in the free queue (in freeing order, evicted
+ * from the head like any free block) until a later prompt matches them.
+ *
+ * pa_pool_enable_prefix_cache: turn caching on for blocks of block_size
+ * tokens (once; PA_ERR_INVALID if already on with another size). */
+pa_status pa_pool_enable_prefix_cache(pa_pool* pool, int32_t block_size);
+/* Blocks for a new sequence whose first num_tokens tokens are `tokens`:
+ * out_blocks[0..ceil(num_tokens / B)) receives the leading full blocks found
+ * in the cache (ref + 1; taken out of the free queue if they were free) and
+ * then fresh blocks from the free-queue head.  Every fresh full block is
+ * registered under its content at once, so the caller writes the K/V of
+ * tokens [*num_cached_tokens, num_tokens) (its prefill) before the pool
+ * serves another request.  *num_cached_tokens is a multiple of B: the
+ * tokens whose K/V the shared blocks already hold.  All-or-nothing:
+ * PA_ERR_OOM leaves the pool unchanged. */
+pa_status pa_pool_alloc_prefix(pa_pool* pool, const int32_t* tokens, int32_t num_tokens,
+                               int32_t* out_blocks, int32_t* num_cached_tokens);
+/* Register a referenced block that has just become full (decode filled its
+ * last slot) under (parent, its B tokens); parent is the sequence's previous
+ * block or -1 for its first block.  A content already cached elsewhere is
+ * not registered twice. */
+pa_status pa_pool_register_block(pa_pool* pool, int32_t block, int32_t parent,
+                                 const int32_t* tokens);
+/* Blocks currently holding a registered entry (referenced or free). */
+int32_t pa_pool_num_cached(const pa_pool* pool);
+
 /* ------------------------------------------------------------------------
  * Diagnostics.
  * ---------------------------------------------------------------------- */

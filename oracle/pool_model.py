@@ -16,6 +16,17 @@ Followed definitions:
   count is decremented, the table entry is remapped, and (src, dst) is
   reported for a device copy; with ref count 1 the write goes in place.
 
+* Prefix caching across requests (``PrefixCachePoolModel``): "Paged KV
+  cache" (ai-infra-handbooks), copy-on-write exercise -- vLLM V1 shares only
+  full blocks and every answer starts writing in its own block; "4.6
+  PagedAttention & KV-Cache Memory Management", section "Copy-on-write for
+  shared prefixes" -- the same machinery generalises to reuse across
+  requests.  The pages do not say how a block is recognised; the reading
+  taken: a full block is the content (parent block, parent generation, its
+  B tokens), a generation advances whenever a block is handed out fresh (its
+  entry dies with it), freed cached blocks wait in the free queue and leave it
+  when matched.  Kept as plain dictionaries keyed by that tuple.
+
 Readings where the pages differ: FIFO (the handbook's deque and its printed
 ``[5, 6, 7, 0]`` example) rather than the llm-stack-book's ``pop()`` from the
 end; all-or-nothing allocation instead of raising after a partial pop.
@@ -115,3 +126,82 @@ class SequenceTablesModel:
 
     def free_seq(self, seq) -> None:
         self.pool.free(self.tables.pop(seq))
+
+
+class PrefixCachePoolModel(BlockPoolModel):
+    """``BlockPoolModel`` plus full-block prefix caching (see module notes)."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        super().__init__(num_blocks, free_order)
+        self.block_size = block_size
+        self.gen = [0] * num_blocks
+        self.entry_of = {}   # (parent, parent_gen, tokens) -> block
+        self.key_of = {}     # block -> its key
+
+    def num_cached(self) -> int:
+        return len(self.key_of)
+
+    def _drop_entry(self, b: int) -> None:
+        key = self.key_of.pop(b, None)
+        if key is not None and self.entry_of.get(key) == b:
+            del self.entry_of[key]
+
+    def _fresh(self) -> int:
+        b = self.free_queue.popleft()
+        self._drop_entry(b)
+        self.gen[b] += 1
+        self.ref_cnt[b] = 1
+        return b
+
+    def allocate(self, n: int):
+        if n > len(self.free_queue):
+            return None
+        return [self._fresh() for _ in range(n)]
+
+    def cow(self, blk: int):
+        if self.ref_cnt[blk] == 1:
+            return blk, blk
+        if not self.free_queue:
+            raise PoolExhausted("no free block for copy-on-write")
+        self.ref_cnt[blk] -= 1
+        return blk, self._fresh()
+
+    def _key(self, parent: int, tokens) -> tuple:
+        return (parent, self.gen[parent] if parent >= 0 else 0, tuple(int(t) for t in tokens))
+
+    def register(self, b: int, parent: int, tokens) -> None:
+        self._drop_entry(b)
+        key = self._key(parent, tokens)
+        if key in self.entry_of:
+            return
+        self.entry_of[key] = b
+        self.key_of[b] = key
+
+    def allocate_prefix(self, tokens):
+        """(blocks, cached_tokens) for a new sequence, or None when short."""
+        B = self.block_size
+        n = len(tokens)
+        nblk, nfull = -(-n // B), n // B
+        hits, parent = [], -1
+        for k in range(nfull):
+            b = self.entry_of.get(self._key(parent, tokens[k * B:(k + 1) * B]))
+            if b is None:
+                break
+            hits.append(b)
+            parent = b
+        free_hits = sum(1 for b in hits if self.ref_cnt[b] == 0)
+        if nblk - len(hits) > len(self.free_queue) - free_hits:
+            return None
+        for b in hits:
+            if self.ref_cnt[b] == 0:
+                self.free_queue.remove(b)
+            self.ref_cnt[b] += 1
+        blocks = list(hits)
+        parent = hits[-1] if hits else -1
+        for k in range(len(hits), nblk):
+            b = self._fresh()
+            blocks.append(b)
+            if k < nfull:
+                self.register(b, parent, tokens[k * B:(k + 1) * B])
+            parent = b
+        return blocks, len(hits) * B

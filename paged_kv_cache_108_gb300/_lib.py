@@ -75,6 +75,10 @@ SIGNATURES = {
     "pa_pool_incref": (I32, [P, PI32, I32]),
     "pa_pool_free": (I32, [P, PI32, I32]),
     "pa_pool_cow": (I32, [P, I32, PI32]),
+    "pa_pool_enable_prefix_cache": (I32, [P, I32]),
+    "pa_pool_alloc_prefix": (I32, [P, PI32, I32, PI32, PI32]),
+    "pa_pool_register_block": (I32, [P, I32, I32, PI32]),
+    "pa_pool_num_cached": (I32, [P]),
     "pa_status_string": (ctypes.c_char_p, [I32]),
     "pa_last_error": (ctypes.c_char_p, []),
     "pa_version": (ctypes.c_char_p, []),

@@ -90,6 +90,36 @@ class BlockPool:
         return int(block), int(dst.value)
 
 
+    # ---- prefix caching across requests (full blocks) ----
+    def enable_prefix_cache(self, block_size: int) -> None:
+        _lib.check(self._lib.pa_pool_enable_prefix_cache(self._h, int(block_size)))
+        self.prefix_block_size = int(block_size)
+
+    def allocate_prefix(self, tokens):
+        """Blocks for a new sequence with prompt ``tokens``: (blocks,
+        cached_tokens), or None if the pool is short; the leading
+        ``cached_tokens`` tokens' K/V are already in the shared blocks."""
+        arr, ptr = _i32_array(tokens)
+        bs = self.prefix_block_size
+        out = np.zeros(max(-(-arr.size // bs), 1), dtype=np.int32)
+        cached = ctypes.c_int32(0)
+        st = self._lib.pa_pool_alloc_prefix(self._h, ptr, arr.size,
+                                            out.ctypes.data_as(_lib.PI32), ctypes.byref(cached))
+        if st == _lib.PA_ERR_OOM:
+            return None
+        _lib.check(st)
+        return out[:-(-arr.size // bs)].tolist(), int(cached.value)
+
+    def register_block(self, block: int, parent: int, tokens) -> None:
+        arr, ptr = _i32_array(tokens)
+        if arr.size != self.prefix_block_size:
+            raise ValueError("a registered block holds exactly block_size tokens")
+        _lib.check(self._lib.pa_pool_register_block(self._h, int(block), int(parent), ptr))
+
+    def num_cached(self) -> int:
+        return self._lib.pa_pool_num_cached(self._h)
+
+
 def slot_mapping(block_tables: np.ndarray, block_size: int, positions, token_seq=None):
     """Slots of tokens at ``positions`` (sequence ``token_seq[i]``, default i)."""
     bt = np.ascontiguousarray(block_tables, dtype=np.int32)
