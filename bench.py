@@ -52,6 +52,9 @@ def parse():
                     help="llama8b: the headline layer (batch 64); longctx: 8 sequences of "
                          "4K..128K tokens; serving: 256 MHA sequences in groups of 8 sharing "
                          "a 1024-token prefix")
+    ap.add_argument("--new-tokens", type=int, default=1,
+                    help="tokens each sequence adds per step (> 1: multi-token step through "
+                         "pa_varlen_attention, e.g. speculative decoding)")
     ap.add_argument("--block-size", type=int, default=16,
                     help="tokens per physical block (llama8b workload: 1, 16, 64, 256)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -126,7 +129,7 @@ class Step:
     """Device-resident state of one decode step of a workload."""
 
     def __init__(self, device, partition=0, kernel=0, kv_dtype="bf16", workload="llama8b",
-                 block_size=16):
+                 block_size=16, new_tokens=1):
         import torch
 
         from paged_kv_cache_108_gb300 import ops, pool, synth
@@ -158,16 +161,26 @@ class Step:
             self.k_cache = torch.randn(shape, generator=gen, device=device, dtype=torch.bfloat16)
             self.v_cache = torch.randn(shape, generator=gen, device=device, dtype=torch.bfloat16)
         S = w.num_seqs
-        self.q = torch.randn((S, H, d), generator=gen, device=device).to(torch.bfloat16)
-        self.k_new = torch.randn((S, hkv, d), generator=gen, device=device).to(torch.bfloat16)
+        T = new_tokens
+        self.new_tokens = T
+        self.q = torch.randn((S * T, H, d), generator=gen, device=device).to(torch.bfloat16)
+        self.k_new = torch.randn((S * T, hkv, d), generator=gen, device=device).to(torch.bfloat16)
         self.v_new = torch.randn((S, hkv, d), generator=gen, device=device).to(torch.bfloat16)
-        self.positions = (w.context_lens - 1).astype(np.int32)
-        slots = pool.slot_mapping(w.block_tables, B, self.positions)
+        # the step's tokens: the last T positions of every context, sequence-major
+        self.token_seq = np.repeat(np.arange(S, dtype=np.int32), T)
+        self.positions = (np.repeat(w.context_lens, T) - T +
+                          np.tile(np.arange(T, dtype=np.int32), S)).astype(np.int32)
+        slots = pool.slot_mapping(w.block_tables, B, self.positions, self.token_seq)
+        self.qsl = torch.arange(0, S * T + 1, T, dtype=torch.int32, device=device)
         self.slots = torch.from_numpy(slots).to(device)
         self.block_tables = torch.from_numpy(w.block_tables).to(device)
         self.context_lens = torch.from_numpy(w.context_lens).to(device)
         self.out = torch.empty_like(self.q)
-        self.ws = ops.alloc_workspace(S, H, d, w.max_blocks, B, partition, device=device)
+        if T == 1:
+            self.ws = ops.alloc_workspace(S, H, d, w.max_blocks, B, partition, device=device)
+        else:
+            n = ops.varlen_workspace_size(S * T, H, d, w.max_blocks, B)
+            self.ws = torch.empty(n, dtype=torch.uint8, device=device)
         # the tensor-core decode (one launch, merge inside) serves this shape
         # unless the SIMT kernel is forced; SIMT adds a combine launch
         simt = kernel == 1
@@ -182,14 +195,15 @@ class Step:
         w = self.w
         tokens = int(np.sum(w.context_lens)) if logical else self.unique_tokens
         kv = tokens * w.num_kv_heads * w.head_dim * self.kv_bytes * 2
-        qo = 2 * w.num_seqs * w.num_heads * w.head_dim * 2
+        qo = 2 * w.num_seqs * self.new_tokens * w.num_heads * w.head_dim * 2
         table = int(sum(math.ceil(n / w.block_size) for n in w.context_lens)) * 4
         return kv + qo + table + w.num_seqs * 4
 
     def write_bytes(self) -> int:
         w = self.w
         # K and V: bf16 tokens read, cache rows written
-        return 2 * w.num_seqs * w.num_kv_heads * w.head_dim * (2 + self.kv_bytes) + w.num_seqs * 4
+        n = w.num_seqs * self.new_tokens
+        return 2 * n * w.num_kv_heads * w.head_dim * (2 + self.kv_bytes) + n * 4
 
     def run_write(self, slots=None, k=None, v=None):
         self.ops.reshape_and_cache(self.k_new if k is None else k, self.v_new if v is None else v,
@@ -199,6 +213,10 @@ class Step:
     def run_step(self, slots=None, k=None, v=None, q=None, bt=None, cl=None):
         """The step as one call: cache write of the new tokens, then decode."""
         w = self.w
+        if self.new_tokens > 1:
+            self.run_write(slots, k, v)
+            self.run_decode(q, bt, cl)
+            return
         self.ops.write_and_decode(self.k_new if k is None else k, self.v_new if v is None else v,
                                   self.slots if slots is None else slots, self.out,
                                   self.q if q is None else q, self.k_cache, self.v_cache,
@@ -208,6 +226,12 @@ class Step:
 
     def run_decode(self, q=None, bt=None, cl=None):
         w = self.w
+        if self.new_tokens > 1:
+            self.ops.varlen_attention(self.out, self.q if q is None else q, self.k_cache,
+                                      self.v_cache, self.block_tables if bt is None else bt,
+                                      self.context_lens if cl is None else cl, self.qsl, w.scale,
+                                      self.k_scale, self.v_scale, workspace=self.ws)
+            return
         self.ops.decode(self.out, self.q if q is None else q, self.k_cache, self.v_cache,
                         self.block_tables if bt is None else bt,
                         self.context_lens if cl is None else cl, w.scale, self.k_scale,
@@ -343,7 +367,7 @@ def run_ours(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     step = Step(device, args.partition, args.kernel, args.kv_dtype, args.workload,
-                args.block_size)
+                args.block_size, args.new_tokens)
     stream = torch.cuda.current_stream()
     # L2 flush: read a buffer 4x the L2 size.  Reading (not writing) leaves
     # only clean lines behind, so the timed kernels do not pay for writing
@@ -430,7 +454,9 @@ def run_ours(args, rank, world, local_rank):
                  "lengths from the pages' seeded request mix)" if step.fp8 else
                  "synthetic (seeded N(0,1) bf16 K/V/q; lengths from the pages' seeded request mix)"),
         "config": {"workload": f"{WORKLOADS[args.workload]}, "
-                               f"{'e4m3 (per-tensor scale)' if step.fp8 else 'bf16'} KV, "
+                               + (f"{step.new_tokens} new tokens per sequence "
+                                  "(pa_varlen_attention), " if step.new_tokens > 1 else "")
+                               + f"{'e4m3 (per-tensor scale)' if step.fp8 else 'bf16'} KV, "
                                f"block {w.block_size}, sum ctx {int(np.sum(w.context_lens))}",
                    "num_seqs": w.num_seqs,
                    "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads,
@@ -449,7 +475,7 @@ def run_ours(args, rank, world, local_rank):
         "us_per_step_p90": round(float(np.percentile(step_ms, 90)) * 1e3, 2),
         "us_decode": round(mean_dec * 1e3, 2),
         "us_write": round(sum(wr_ms) / K * 1e3, 2),
-        "tokens_per_s": round(world * w.num_seqs / (mean_step * 1e-3), 1),
+        "tokens_per_s": round(world * w.num_seqs * step.new_tokens / (mean_step * 1e-3), 1),
         "pct_of_nominal_8tbps": round(100 * achieved / 8000.0, 1),
         "roofline": {"bound": "hbm", "kernel": "pa_decode alone (tcgen05 paged decode; split units merged in-kernel)",
                      "achieved": round(achieved, 2), "peak": peak, "peak_source": peak_src,
@@ -500,9 +526,9 @@ def run_e2e(step, args, device, dist):
     bo = h_out.numel() * h_out.element_size()
 
     h_v["slots"].numpy()[:] = step.pool.slot_mapping(w.block_tables, w.block_size,
-                                                     step.positions)
+                                                     step.positions, step.token_seq)
     graph = None
-    if step.kernel == 0:
+    if step.kernel == 0 and step.new_tokens == 1:
         # the step as one captured graph: packed inputs in, write + decode, output out
         graph = step.ops.StepGraph(d_v["k"], d_v["v"], d_v["slots"], step.out, d_v["q"],
                                    step.k_cache, step.v_cache, d_v["bt"], d_v["cl"], w.scale,
@@ -512,7 +538,7 @@ def run_e2e(step, args, device, dist):
     def one():
         # host slot mapping of the step's new tokens into the pinned staging
         h_v["slots"].numpy()[:] = step.pool.slot_mapping(w.block_tables, w.block_size,
-                                                         step.positions)
+                                                         step.positions, step.token_seq)
         if graph is not None:
             graph.replay()
         else:

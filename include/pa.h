@@ -272,6 +272,40 @@ pa_status pa_slot_mapping(const int32_t* block_tables, int32_t num_seqs,
                           int32_t num_tokens, int32_t* slot_mapping);
 
 /* ------------------------------------------------------------------------
+ * pa_varlen_attention -- paged attention for a step whose requests add any
+ * number of new tokens (multi-token decode, chunked prefill, full prefill).
+ * [PKV] "Paged attention" (paged_attention, query_start_loc): request i's
+ * new tokens are q[qsl[i]:qsl[i+1]], the last num_new tokens of its context
+ * of seq_lens[i] tokens; new token j sits at position seq_len - num_new + j
+ * and attends causally to positions 0..seq_len - num_new + j, query head h
+ * to KV head h / (num_heads / num_kv_heads).  Each new token is computed as
+ * a decode over the first seq_len - num_new + j + 1 tokens of its request
+ * (one virtual sequence per token, the decode kernels of pa_decode), so a
+ * request's context is read once per new token: efficient for a few new
+ * tokens per request, bandwidth-heavy for long prefill chunks.
+ *
+ *  out, q            device, [num_tokens, num_heads, head_dim] bf16.
+ *  block_tables      device, [num_seqs, max_blocks_per_seq] int32.
+ *  seq_lens          device, [num_seqs] int32: context length after this
+ *                    step's write (the new tokens' K/V are already cached).
+ *  query_start_loc   device, [num_seqs + 1] int32, non-decreasing, from 0 to
+ *                    num_tokens (cu_seqlens_q).  A request whose num_new
+ *                    exceeds its seq_len gets zero output rows.
+ *  workspace         device, >= pa_varlen_workspace_size(...) bytes, 256-byte
+ *                    aligned (expanded tables, lengths, decode scratch).
+ *  Other arguments as pa_decode.  At most 65535 new tokens per call.
+ * ---------------------------------------------------------------------- */
+size_t pa_varlen_workspace_size(int32_t num_tokens, int32_t num_heads, int32_t head_dim,
+                                int32_t max_blocks_per_seq, int32_t block_size);
+pa_status pa_varlen_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              pa_cache_desc cache, const int32_t* block_tables,
+                              int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                              const int32_t* query_start_loc, int32_t num_seqs,
+                              int32_t num_tokens, int32_t num_heads, float scale,
+                              const float* k_scale, const float* v_scale, void* workspace,
+                              size_t workspace_bytes, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * pa_swap_blocks -- copy whole blocks between two caches of the same block
  * shape: dst[d] = src[s] for K and V, for every (s, d) pair.  An exhausted
  * pool must preempt a sequence ([LSB] BlockManager.allocate), and the

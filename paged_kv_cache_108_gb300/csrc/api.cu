@@ -389,6 +389,64 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, pa_cache_desc cache,
                      fn);
 }
 
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+size_t pa_varlen_workspace_size(int32_t num_tokens, int32_t num_heads, int32_t head_dim,
+                                int32_t max_blocks_per_seq, int32_t block_size) {
+  if (num_tokens <= 0 || num_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
+      block_size <= 0)
+    return 0;
+  const size_t meta = align256((size_t)num_tokens * max_blocks_per_seq * 4) +
+                      align256((size_t)num_tokens * 4);
+  // the decode part may legitimately need no scratch (no split partitions)
+  return meta + pa_decode_workspace_size(num_tokens, num_heads, head_dim, max_blocks_per_seq,
+                                         block_size);
+}
+
+pa_status pa_varlen_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              pa_cache_desc cache, const int32_t* block_tables,
+                              int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                              const int32_t* query_start_loc, int32_t num_seqs,
+                              int32_t num_tokens, int32_t num_heads, float scale,
+                              const float* k_scale, const float* v_scale, void* workspace,
+                              size_t workspace_bytes, pa_stream_t stream) {
+  const char* fn = "pa_varlen_attention";
+  char buf[192];
+  if (num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq <= 0)
+    return pa_fail(PA_ERR_INVALID, "pa_varlen_attention: bad sizes");
+  if (num_tokens == 0) return PA_OK;
+  if (num_seqs == 0) return pa_fail(PA_ERR_INVALID, "pa_varlen_attention: tokens without requests");
+  if (num_tokens > 65535)
+    return pa_fail(PA_ERR_UNSUPPORTED, "pa_varlen_attention: more than 65535 new tokens");
+  if (!block_tables || !seq_lens || !query_start_loc || !workspace)
+    return pa_fail(PA_ERR_INVALID, "pa_varlen_attention: NULL pointer");
+  if (!aligned(block_tables, 4) || !aligned(seq_lens, 4) || !aligned(query_start_loc, 4) ||
+      !aligned(workspace, 256))
+    return pa_fail(PA_ERR_INVALID, "pa_varlen_attention: misaligned pointer");
+  pa_status st = check_cache(cache, fn);
+  if (st != PA_OK) return st;
+  const size_t need = pa_varlen_workspace_size(num_tokens, num_heads, cache.head_dim,
+                                               max_blocks_per_seq, cache.block_size);
+  if (need == 0 || workspace_bytes < need) {
+    snprintf(buf, sizeof buf, "pa_varlen_attention: workspace of %zu bytes needed", need);
+    return pa_fail(PA_ERR_INVALID, buf);
+  }
+  char* ws = static_cast<char*>(workspace);
+  int32_t* vtables = reinterpret_cast<int32_t*>(ws);
+  const size_t tb = align256((size_t)num_tokens * max_blocks_per_seq * 4);
+  int32_t* vlens = reinterpret_cast<int32_t*>(ws + tb);
+  const size_t meta = tb + align256((size_t)num_tokens * 4);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = pa::launch_varlen_meta(block_tables, max_blocks_per_seq, cache.block_size,
+                                         seq_lens, query_start_loc, num_seqs, num_tokens,
+                                         vtables, vlens, s);
+  if (e != cudaSuccess) return cuda_status(e, fn);
+  // one virtual sequence per new token: its request's table, its causal length
+  return decode_impl(out, q, k_cache, v_cache, cache, vtables, max_blocks_per_seq, vlens,
+                     num_tokens, num_heads, scale, k_scale, v_scale, ws + meta,
+                     workspace_bytes - meta, nullptr, stream, false);
+}
+
 pa_status pa_swap_blocks(void* dst_k, void* dst_v, int32_t dst_num_blocks, const void* src_k,
                          const void* src_v, int32_t src_num_blocks, pa_cache_desc block_shape,
                          const int32_t* block_pairs, int32_t num_pairs, pa_stream_t stream) {

@@ -155,7 +155,53 @@ __global__ void step_prepare_kernel(int32_t* __restrict__ block_tables, int max_
   slot_mapping[i] = slot;
 }
 
+// Varlen (multi-token) attention as decode over one virtual sequence per
+// new token ("Paged KV cache", section "Paged attention": request i's new
+// token j sits at position seq_len - num_new + j and sees positions up to
+// it).  CTA t handles token t: it finds its request i (qsl[i] <= t <
+// qsl[i+1], binary search), writes the causal context length
+// seq_len - num_new + j + 1 (0 when the request's numbers are inconsistent:
+// num_new > seq_len), and copies the first ceil(ctx / B) entries of the
+// request's block-table row into the token's row.
+__global__ void varlen_meta_kernel(const int32_t* __restrict__ block_tables, int max_blocks,
+                                   int block_size, const int32_t* __restrict__ seq_lens,
+                                   const int32_t* __restrict__ qsl, int num_seqs,
+                                   int32_t* __restrict__ vtables, int32_t* __restrict__ vlens) {
+  const int t = blockIdx.x;
+  __shared__ int s_req, s_ctx;
+  if (threadIdx.x == 0) {
+    int a = 0, b = num_seqs - 1;  // last request with qsl[i] <= t
+    while (a < b) {
+      const int m = (a + b + 1) >> 1;
+      if (qsl[m] <= t) a = m; else b = m - 1;
+    }
+    const int num_new = qsl[a + 1] - qsl[a];
+    const int n = seq_lens[a];
+    int ctx = n - num_new + (t - qsl[a]) + 1;
+    if (num_new > n || t >= qsl[a + 1] || ctx < 1) ctx = 0;
+    if ((int64_t)ctx > (int64_t)max_blocks * block_size) ctx = 0;
+    s_req = a;
+    s_ctx = ctx;
+    vlens[t] = ctx;
+  }
+  __syncthreads();
+  const int nb = (s_ctx + block_size - 1) / block_size;
+  const int32_t* src = block_tables + (int64_t)s_req * max_blocks;
+  int32_t* dst = vtables + (int64_t)t * max_blocks;
+  for (int k = threadIdx.x; k < nb; k += blockDim.x) dst[k] = src[k];
+}
+
 }  // namespace
+
+cudaError_t launch_varlen_meta(const int32_t* block_tables, int max_blocks, int block_size,
+                               const int32_t* seq_lens, const int32_t* query_start_loc,
+                               int num_seqs, int num_tokens, int32_t* vtables, int32_t* vlens,
+                               cudaStream_t stream) {
+  varlen_meta_kernel<<<num_tokens, 128, 0, stream>>>(block_tables, max_blocks, block_size,
+                                                     seq_lens, query_start_loc, num_seqs,
+                                                     vtables, vlens);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_step_prepare(int32_t* block_tables, int max_blocks, int block_size,
                                 int32_t* context_lens, int num_seqs, const int32_t* updates,

@@ -74,6 +74,11 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value,
                                      const float* v_scale,
                                      cudaStream_t stream);
 
+cudaError_t launch_varlen_meta(const int32_t* block_tables, int max_blocks, int block_size,
+                               const int32_t* seq_lens, const int32_t* query_start_loc,
+                               int num_seqs, int num_tokens, int32_t* vtables, int32_t* vlens,
+                               cudaStream_t stream);
+
 cudaError_t launch_step_prepare(int32_t* block_tables, int max_blocks, int block_size,
                                 int32_t* context_lens, int num_seqs, const int32_t* updates,
                                 int num_updates, int advance, int32_t* slot_mapping,

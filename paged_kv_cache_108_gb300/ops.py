@@ -135,6 +135,40 @@ def _any_ptr(t: torch.Tensor, name: str) -> int:
     return t.data_ptr()
 
 
+def varlen_workspace_size(num_tokens: int, num_heads: int, head_dim: int,
+                          max_blocks_per_seq: int, block_size: int) -> int:
+    return int(_lib.lib().pa_varlen_workspace_size(num_tokens, num_heads, head_dim,
+                                                   max_blocks_per_seq, block_size))
+
+
+def varlen_attention(out, q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale,
+                     k_scale=None, v_scale=None, workspace=None, stream=None):
+    """Causal paged attention for a step whose requests add several tokens:
+    q/out [num_tokens, H_q, d] (request i's tokens at query_start_loc[i] ..
+    query_start_loc[i+1]-1, the last tokens of its seq_lens[i]-token context)."""
+    _same_cache(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    ks, vs = _scales(desc, k_scale, v_scale)
+    if q.dim() != 3 or out.shape != q.shape:
+        raise ValueError("q and out must both be [num_tokens, num_heads, head_dim]")
+    num_tokens, num_heads, head_dim = q.shape
+    num_seqs = int(seq_lens.numel())
+    if query_start_loc.numel() != num_seqs + 1:
+        raise ValueError("query_start_loc needs num_seqs + 1 entries")
+    max_blocks = int(block_tables.shape[1])
+    if workspace is None:
+        n = varlen_workspace_size(num_tokens, num_heads, head_dim, max_blocks, desc.block_size)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    _lib.check(_lib.lib().pa_varlen_attention(
+        _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), desc, _dev(block_tables, "block_tables", torch.int32),
+        max_blocks, _dev(seq_lens, "seq_lens", torch.int32),
+        _dev(query_start_loc, "query_start_loc", torch.int32), num_seqs, int(num_tokens),
+        int(num_heads), ctypes.c_float(scale), ks, vs, _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
 def swap_blocks(dst_k, dst_v, src_k, src_v, block_pairs, stream=None) -> None:
     """dst[d] = src[s] for each (s, d) row of ``block_pairs`` [n, 2] int32,
     between two caches of the same block shape (device pool <-> pinned host
