@@ -179,7 +179,7 @@ class Step:
         if T == 1:
             self.ws = ops.alloc_workspace(S, H, d, w.max_blocks, B, partition, device=device)
         else:
-            n = ops.varlen_workspace_size(S * T, H, d, w.max_blocks, B)
+            n = ops.decode_multi_workspace_size(S, T, H, d, w.max_blocks, B)
             self.ws = torch.empty(n, dtype=torch.uint8, device=device)
         # the tensor-core decode (one launch, merge inside) serves this shape
         # unless the SIMT kernel is forced; SIMT adds a combine launch
@@ -227,10 +227,10 @@ class Step:
     def run_decode(self, q=None, bt=None, cl=None):
         w = self.w
         if self.new_tokens > 1:
-            self.ops.varlen_attention(self.out, self.q if q is None else q, self.k_cache,
-                                      self.v_cache, self.block_tables if bt is None else bt,
-                                      self.context_lens if cl is None else cl, self.qsl, w.scale,
-                                      self.k_scale, self.v_scale, workspace=self.ws)
+            self.ops.decode_multi(self.out, self.q if q is None else q, self.k_cache,
+                                  self.v_cache, self.block_tables if bt is None else bt,
+                                  self.context_lens if cl is None else cl, self.new_tokens,
+                                  w.scale, self.k_scale, self.v_scale, workspace=self.ws)
             return
         self.ops.decode(self.out, self.q if q is None else q, self.k_cache, self.v_cache,
                         self.block_tables if bt is None else bt,
@@ -455,7 +455,7 @@ def run_ours(args, rank, world, local_rank):
                  "synthetic (seeded N(0,1) bf16 K/V/q; lengths from the pages' seeded request mix)"),
         "config": {"workload": f"{WORKLOADS[args.workload]}, "
                                + (f"{step.new_tokens} new tokens per sequence "
-                                  "(pa_varlen_attention), " if step.new_tokens > 1 else "")
+                                  "(pa_decode_multi), " if step.new_tokens > 1 else "")
                                + f"{'e4m3 (per-tensor scale)' if step.fp8 else 'bf16'} KV, "
                                f"block {w.block_size}, sum ctx {int(np.sum(w.context_lens))}",
                    "num_seqs": w.num_seqs,

@@ -306,6 +306,29 @@ pa_status pa_varlen_attention(void* out, const void* q, const void* k_cache, con
                               size_t workspace_bytes, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * pa_decode_multi -- pa_varlen_attention for the common case in which every
+ * request adds the same number of tokens (multi-token / speculative decode):
+ * q and out are [num_seqs * tokens_per_seq, num_heads, head_dim], request
+ * i's tokens at rows i * tokens_per_seq + j, the last tokens_per_seq
+ * positions of its context_lens[i]-token context, each causal as in
+ * pa_varlen_attention ([PKV] "Paged attention").  When group x
+ * tokens_per_seq fits the tensor-core kernel's columns (16 for bf16, 8 for
+ * e4m3; powers of two) one pass reads each context once and computes all
+ * its (token, head) columns together; otherwise each token runs as its own
+ * decode, as in pa_varlen_attention.
+ *  workspace  >= pa_decode_multi_workspace_size(...) bytes, 256-byte aligned.
+ * ---------------------------------------------------------------------- */
+size_t pa_decode_multi_workspace_size(int32_t num_seqs, int32_t tokens_per_seq,
+                                      int32_t num_heads, int32_t head_dim,
+                                      int32_t max_blocks_per_seq, int32_t block_size);
+pa_status pa_decode_multi(void* out, const void* q, const void* k_cache, const void* v_cache,
+                          pa_cache_desc cache, const int32_t* block_tables,
+                          int32_t max_blocks_per_seq, const int32_t* context_lens,
+                          int32_t num_seqs, int32_t tokens_per_seq, int32_t num_heads,
+                          float scale, const float* k_scale, const float* v_scale,
+                          void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * pa_swap_blocks -- copy whole blocks between two caches of the same block
  * shape: dst[d] = src[s] for K and V, for every (s, d) pair.  An exhausted
  * pool must preempt a sequence ([LSB] BlockManager.allocate), and the

@@ -64,6 +64,9 @@ SIGNATURES = {
     "pa_step_prepare": (I32, [P, I32, I32, I32, P, P, I32, I32, P, P]),
     "pa_swap_blocks": (I32, [P, P, I32, P, P, I32, CacheDesc, P, I32, P]),
     "pa_varlen_workspace_size": (ctypes.c_size_t, [I32, I32, I32, I32, I32]),
+    "pa_decode_multi_workspace_size": (ctypes.c_size_t, [I32, I32, I32, I32, I32, I32]),
+    "pa_decode_multi": (I32, [P, P, P, P, CacheDesc, P, I32, P, I32, I32, I32, ctypes.c_float,
+                              P, P, P, ctypes.c_size_t, P]),
     "pa_varlen_attention": (I32, [P, P, P, P, CacheDesc, P, I32, P, P, I32, I32, I32, ctypes.c_float, P, P,
                                   P, ctypes.c_size_t, P]),
     "pa_slot_mapping": (I32, [PI32, I32, I32, I32, PI32, PI32, I32, PI32]),

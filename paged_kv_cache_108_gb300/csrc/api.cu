@@ -208,7 +208,8 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
                              int32_t num_seqs, int32_t num_heads, float scale,
                              const float* k_scale, const float* v_scale, void* workspace,
                              size_t workspace_bytes, const pa_decode_opts* opts,
-                             pa_stream_t stream, bool prev_writes_cache_only) {
+                             pa_stream_t stream, bool prev_writes_cache_only,
+                             int32_t tokens_per_seq = 1) {
   const char* fn = "pa_decode";
   char buf[224];
   pa_status st = check_cache(cache, fn);
@@ -242,14 +243,17 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
 
   const bool fp8 = cache.dtype == PA_KV_FP8_E4M3;
   const bool tc_ok = kernel != 1 && pa::tc_supported(cache.head_dim, group, fp8, num_seqs,
-                                                      cache.block_size);
+                                                      cache.block_size, tokens_per_seq);
+  if (tokens_per_seq > 1 && !tc_ok)  // the SIMT kernel serves one token per sequence
+    return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: several tokens per sequence need the "
+                                       "tensor-core kernel");
   if (kernel == 2 || (kernel == 0 && tc_ok)) {
     if (!tc_ok)
       return pa_fail(PA_ERR_UNSUPPORTED,
                      "pa_decode: tensor-core kernel needs head_dim 128, "
                      "block_size >= 8 and at most 1024 sequences");
     const int nsm = num_sms();
-    const size_t need = pa::tc_workspace_bytes(num_seqs, num_heads, max_ctx, nsm);
+    const size_t need = pa::tc_workspace_bytes(num_seqs, num_heads, max_ctx, nsm, tokens_per_seq);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) {
       snprintf(buf, sizeof buf, "pa_decode: workspace of %zu bytes (256-byte aligned) needed",
                need);
@@ -273,6 +277,7 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
     a.num_blocks = cache.num_blocks;
     a.block_size = cache.block_size;
     a.num_ctas = nsm;
+    a.tokens_per_seq = tokens_per_seq;
     a.scale = scale;
     a.early_meta = prev_writes_cache_only;
     return cuda_status(pa::launch_decode_tc(a, reinterpret_cast<cudaStream_t>(stream)), fn);
@@ -438,13 +443,81 @@ pa_status pa_varlen_attention(void* out, const void* q, const void* k_cache, con
   const size_t meta = tb + align256((size_t)num_tokens * 4);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = pa::launch_varlen_meta(block_tables, max_blocks_per_seq, cache.block_size,
-                                         seq_lens, query_start_loc, num_seqs, num_tokens,
+                                         seq_lens, query_start_loc, 0, num_seqs, num_tokens,
                                          vtables, vlens, s);
   if (e != cudaSuccess) return cuda_status(e, fn);
   // one virtual sequence per new token: its request's table, its causal length
   return decode_impl(out, q, k_cache, v_cache, cache, vtables, max_blocks_per_seq, vlens,
                      num_tokens, num_heads, scale, k_scale, v_scale, ws + meta,
                      workspace_bytes - meta, nullptr, stream, false);
+}
+
+size_t pa_decode_multi_workspace_size(int32_t num_seqs, int32_t tokens_per_seq,
+                                      int32_t num_heads, int32_t head_dim,
+                                      int32_t max_blocks_per_seq, int32_t block_size) {
+  if (num_seqs <= 0 || tokens_per_seq <= 0 || num_heads <= 0 || head_dim <= 0 ||
+      max_blocks_per_seq <= 0 || block_size <= 0)
+    return 0;
+  const int64_t max_ctx = (int64_t)max_blocks_per_seq * block_size;
+  // either path: one pass over (token, head) columns, or one decode per token
+  const size_t tc = pa::tc_workspace_bytes(num_seqs, num_heads, max_ctx, num_sms(),
+                                           tokens_per_seq);
+  const size_t per_token = pa_varlen_workspace_size(num_seqs * tokens_per_seq, num_heads,
+                                                    head_dim, max_blocks_per_seq, block_size);
+  return tc > per_token ? tc : per_token;
+}
+
+pa_status pa_decode_multi(void* out, const void* q, const void* k_cache, const void* v_cache,
+                          pa_cache_desc cache, const int32_t* block_tables,
+                          int32_t max_blocks_per_seq, const int32_t* context_lens,
+                          int32_t num_seqs, int32_t tokens_per_seq, int32_t num_heads,
+                          float scale, const float* k_scale, const float* v_scale,
+                          void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  const char* fn = "pa_decode_multi";
+  if (tokens_per_seq <= 0) return pa_fail(PA_ERR_INVALID, "pa_decode_multi: tokens_per_seq <= 0");
+  if (tokens_per_seq == 1)
+    return decode_impl(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, num_heads, scale, k_scale, v_scale, workspace,
+                       workspace_bytes, nullptr, stream, false);
+  if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_heads <= 0)
+    return pa_fail(PA_ERR_INVALID, "pa_decode_multi: bad sizes");
+  if (num_seqs == 0) return PA_OK;
+  pa_status st = check_cache(cache, fn);
+  if (st != PA_OK) return st;
+  if (num_heads % cache.num_kv_heads != 0)
+    return pa_fail(PA_ERR_INVALID, "pa_decode_multi: num_heads is not a multiple of num_kv_heads");
+  if ((int64_t)num_seqs * tokens_per_seq > 65535)
+    return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode_multi: more than 65535 new tokens");
+  const int group = num_heads / cache.num_kv_heads;
+  if (pa::tc_supported(cache.head_dim, group, cache.dtype == PA_KV_FP8_E4M3, num_seqs,
+                       cache.block_size, tokens_per_seq))
+    return decode_impl(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, num_heads, scale, k_scale, v_scale, workspace,
+                       workspace_bytes, nullptr, stream, false, tokens_per_seq);
+  // otherwise one virtual decode sequence per new token
+  const int32_t n = num_seqs * tokens_per_seq;
+  if (!block_tables || !context_lens || !workspace)
+    return pa_fail(PA_ERR_INVALID, "pa_decode_multi: NULL pointer");
+  if (!aligned(workspace, 256)) return pa_fail(PA_ERR_INVALID, "pa_decode_multi: misaligned workspace");
+  const size_t need = pa_varlen_workspace_size(n, num_heads, cache.head_dim, max_blocks_per_seq,
+                                               cache.block_size);
+  if (workspace_bytes < need) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "pa_decode_multi: workspace of %zu bytes needed", need);
+    return pa_fail(PA_ERR_INVALID, buf);
+  }
+  char* ws = static_cast<char*>(workspace);
+  int32_t* vtables = reinterpret_cast<int32_t*>(ws);
+  const size_t tb = align256((size_t)n * max_blocks_per_seq * 4);
+  int32_t* vlens = reinterpret_cast<int32_t*>(ws + tb);
+  const size_t meta = tb + align256((size_t)n * 4);
+  cudaError_t e = pa::launch_varlen_meta(block_tables, max_blocks_per_seq, cache.block_size,
+                                         context_lens, nullptr, tokens_per_seq, num_seqs, n,
+                                         vtables, vlens, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_status(e, fn);
+  return decode_impl(out, q, k_cache, v_cache, cache, vtables, max_blocks_per_seq, vlens, n,
+                     num_heads, scale, k_scale, v_scale, ws + meta, workspace_bytes - meta,
+                     nullptr, stream, false);
 }
 
 pa_status pa_swap_blocks(void* dst_k, void* dst_v, int32_t dst_num_blocks, const void* src_k,

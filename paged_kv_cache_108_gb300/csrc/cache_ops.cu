@@ -163,22 +163,34 @@ __global__ void step_prepare_kernel(int32_t* __restrict__ block_tables, int max_
 // seq_len - num_new + j + 1 (0 when the request's numbers are inconsistent:
 // num_new > seq_len), and copies the first ceil(ctx / B) entries of the
 // request's block-table row into the token's row.
+// qsl == nullptr: every request adds `uniform_tokens` tokens (token t
+// belongs to request t / uniform_tokens).
 __global__ void varlen_meta_kernel(const int32_t* __restrict__ block_tables, int max_blocks,
                                    int block_size, const int32_t* __restrict__ seq_lens,
-                                   const int32_t* __restrict__ qsl, int num_seqs,
-                                   int32_t* __restrict__ vtables, int32_t* __restrict__ vlens) {
+                                   const int32_t* __restrict__ qsl, int uniform_tokens,
+                                   int num_seqs, int32_t* __restrict__ vtables,
+                                   int32_t* __restrict__ vlens) {
   const int t = blockIdx.x;
   __shared__ int s_req, s_ctx;
   if (threadIdx.x == 0) {
-    int a = 0, b = num_seqs - 1;  // last request with qsl[i] <= t
-    while (a < b) {
-      const int m = (a + b + 1) >> 1;
-      if (qsl[m] <= t) a = m; else b = m - 1;
+    int a, start, num_new;
+    if (qsl) {
+      a = 0;
+      int b = num_seqs - 1;  // last request with qsl[i] <= t
+      while (a < b) {
+        const int m = (a + b + 1) >> 1;
+        if (qsl[m] <= t) a = m; else b = m - 1;
+      }
+      start = qsl[a];
+      num_new = qsl[a + 1] - qsl[a];
+    } else {
+      a = t / uniform_tokens;
+      start = a * uniform_tokens;
+      num_new = uniform_tokens;
     }
-    const int num_new = qsl[a + 1] - qsl[a];
     const int n = seq_lens[a];
-    int ctx = n - num_new + (t - qsl[a]) + 1;
-    if (num_new > n || t >= qsl[a + 1] || ctx < 1) ctx = 0;
+    int ctx = n - num_new + (t - start) + 1;
+    if (num_new > n || t >= start + num_new || ctx < 1) ctx = 0;
     if ((int64_t)ctx > (int64_t)max_blocks * block_size) ctx = 0;
     s_req = a;
     s_ctx = ctx;
@@ -195,11 +207,11 @@ __global__ void varlen_meta_kernel(const int32_t* __restrict__ block_tables, int
 
 cudaError_t launch_varlen_meta(const int32_t* block_tables, int max_blocks, int block_size,
                                const int32_t* seq_lens, const int32_t* query_start_loc,
-                               int num_seqs, int num_tokens, int32_t* vtables, int32_t* vlens,
-                               cudaStream_t stream) {
+                               int uniform_tokens, int num_seqs, int num_tokens, int32_t* vtables,
+                               int32_t* vlens, cudaStream_t stream) {
   varlen_meta_kernel<<<num_tokens, 128, 0, stream>>>(block_tables, max_blocks, block_size,
-                                                     seq_lens, query_start_loc, num_seqs,
-                                                     vtables, vlens);
+                                                     seq_lens, query_start_loc, uniform_tokens,
+                                                     num_seqs, vtables, vlens);
   return cudaGetLastError();
 }
 

@@ -116,9 +116,9 @@ struct Cfg {
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
   static constexpr int OFF_SQ = OFF_ABORT + 4;     // [3] ints: sequences of the range's ends, first
   static constexpr int OFF_QEXP = OFF_SQ + 12;     // [2] floats: 2^-e of each q tile (fp8)
-  static constexpr int OFF_RED = OFF_QEXP + 8;     // [2][4][8] floats, chunk max
-  static constexpr int OFF_LRED = OFF_RED + 2 * 4 * 8 * 4;   // [4][8] floats, epilogue sums
-  static constexpr int OFF_CP = OFF_LRED + 4 * 8 * 4;        // chunk prefix per sequence, [S+1]
+  static constexpr int OFF_RED = OFF_QEXP + 8;     // [2][4][16] floats, chunk max per column
+  static constexpr int OFF_LRED = OFF_RED + 2 * 4 * 16 * 4;  // [4][16] floats, epilogue sums
+  static constexpr int OFF_CP = OFF_LRED + 4 * 16 * 4;       // chunk prefix per sequence, [S+1]
   static constexpr int OFF_NLEN = OFF_CP + (kMaxSeqs + 1) * 4;  // clamped context lengths
   static constexpr int OFF_TAB = OFF_NLEN + kMaxSeqs * 4;       // block-id rings (K, V producer)
   static constexpr int SMEM_BYTES = OFF_TAB + 2 * TAB_SLOTS * TAB_W * 4 + 1024;  // + alignment slack
@@ -137,7 +137,12 @@ struct Params {
   int num_seqs, num_heads, num_kv_heads, max_blocks, num_blocks, block_size, log2_bs;
   int num_ctas, max_seg, box_tok, log2_box;
   float scale_log2;
-  const void* q;             // [S, H, D] bf16 (read directly by the fp8 kernel's q warp)
+  // Columns of a unit: c = j * gq + i is query head g * gq + i of the
+  // sequence's j-th new token (ntok tokens per sequence, the last ntok
+  // positions of its context; ntok = 1 for decode).  Token j sees keys at
+  // positions < n - ntok + j + 1.
+  int gq, log2_gq, ntok;
+  const void* q;             // [S * ntok, H, D] bf16 (read directly by the fp8 kernel's q warp)
   const float* k_scale;      // fp8: per-tensor dequantisation scales (device scalars)
   const float* v_scale;
   unsigned long long epoch;  // 48-bit tag of this call
@@ -373,10 +378,9 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
     ptx::prefetch_tmap(&tm_q);
   }
   if (warp < 4) {
-    // zero both P tiles (rows >= G stay zero for the whole kernel); the fp8
-    // kernel also zeroes both q tiles, which its q warp fills row by row
-    constexpr int zoff = FP8 ? OFF_Q : OFF_P;
-    constexpr int zbytes = FP8 ? 2 * (QTILE_B + PTILE_B) : 2 * PTILE_B;
+    // zero both q and P tiles: rows past a unit's columns stay zero
+    constexpr int zoff = OFF_Q;
+    constexpr int zbytes = 2 * (QTILE_B + PTILE_B);
     uint4* pz = reinterpret_cast<uint4*>(sm.base + zoff);
     for (int i = tid; i < zbytes / 16; i += 128) pz[i] = make_uint4(0, 0, 0, 0);
     ptx::fence_proxy_async_smem();
@@ -449,6 +453,11 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
   walk.nl = nl;
   walk.Ctot = Ctot;
   walk.first_ne = first_ne;
+  // output row of column h of unit (seq, g): query head g*gq + (h mod gq) of
+  // the sequence's token h / gq
+  auto out_row = [&](int seq, int g, int h) -> int64_t {
+    return ((int64_t)seq * p.ntok + (h >> p.log2_gq)) * H + (int64_t)g * p.gq + (h & (p.gq - 1));
+  };
 
   if (warp == 4 || warp == Cf::VPROD) {
     // ================= producers (K: warp 4, V: warp VPROD) =================
@@ -493,11 +502,14 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
         const uint32_t qph = (seg >> 1) & 1;
         if (!wait_bar(sm, sm.bar(B_Q_EMPTY + qs), qph ^ 1, p.err, 2)) break;
         if (lane == 0) {
+          // the unit's columns: heads g*gq .. g*gq+gq-1 of its ntok tokens
+          // (3-D map [tokens, H, d], box {64, gq, ntok}; row c = j * gq + i)
           const uint32_t dst = sm.base_u32 + OFF_Q + qs * QTILE_B;
-          const int row0 = walk.seq * H + walk.g * G;
-          ptx::mbar_arrive_expect_tx(sm.bar(B_Q_FULL + qs), QTILE_B);
-          ptx::tma_load_2d(dst, &tm_q, sm.bar(B_Q_FULL + qs), 0, row0);
-          ptx::tma_load_2d(dst + QTILE_B / 2, &tm_q, sm.bar(B_Q_FULL + qs), 64, row0);
+          ptx::mbar_arrive_expect_tx(sm.bar(B_Q_FULL + qs), (uint32_t)(2 * G * 128));
+          ptx::tma_load_3d(dst, &tm_q, sm.bar(B_Q_FULL + qs), 0, walk.g * p.gq,
+                           walk.seq * p.ntok);
+          ptx::tma_load_3d(dst + QTILE_B / 2, &tm_q, sm.bar(B_Q_FULL + qs), 64, walk.g * p.gq,
+                           walk.seq * p.ntok);
         }
         ++seg;
       }
@@ -709,21 +721,22 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           const float mn = fmaxf(M[h], ml[h].x);
-          const float rs = fast_exp2(M[h] - mn);  // 0 for the first piece
-          const float w = fast_exp2(ml[h].x - mn);
+          // a piece may hold no visible key for a column (multi-token units)
+          const float msafe = mn == -INFINITY ? 0.f : mn;
+          const float rs = fast_exp2(M[h] - msafe);  // 0 for the first piece
+          const float w = fast_exp2(ml[h].x - msafe);
           Ls[h] = Ls[h] * rs + w * ml[h].y;
 #pragma unroll
           for (int r = 0; r < 4; ++r) a[h][r] = a[h][r] * rs + w * ov[h][r];
           M[h] = mn;
         }
       }
-      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                         ((int64_t)walk.seq * H + (int64_t)walk.g * G) * D + lane;
+      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + lane;
 #pragma unroll
       for (int h = 0; h < G; ++h)
 #pragma unroll
         for (int r = 0; r < 4; ++r)
-          o[(int64_t)h * D + 32 * r] =
+          o[out_row(walk.seq, walk.g, h) * D + 32 * r] =
               __float2bfloat16_rn(FP8 ? (a[h][r] * __ldg(p.v_scale)) / Ls[h] : a[h][r] / Ls[h]);
       if (lane == 0) p.counters[u] = p.epoch << 16;  // count 0: a replay starts afresh
     }
@@ -746,14 +759,16 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
         const int qs = seg & 1;
         if (!wait_bar(sm, sm.bar(B_Q_EMPTY + qs), ((seg >> 1) & 1) ^ 1, p.err, 2)) break;
         ++seg;
-        const uint4* src = reinterpret_cast<const uint4*>(p.q) +
-                           ((int64_t)walk.seq * H + (int64_t)walk.g * G) * (D / 8);
+        const uint4* src = reinterpret_cast<const uint4*>(p.q);
         uint4 v[NV];
         uint32_t amax = 0;  // bit pattern of max |q| (orders like the float)
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
           const int idx = i * 32 + lane;
-          v[i] = idx < NPIECE ? __ldg(src + idx) : make_uint4(0, 0, 0, 0);
+          const int col = idx >> 4;  // column: head g*gq + (col & (gq-1)) of token col / gq
+          const int64_t row = ((int64_t)walk.seq * p.ntok + (col >> p.log2_gq)) * H +
+                              (int64_t)walk.g * p.gq + (col & (p.gq - 1));
+          v[i] = idx < NPIECE ? __ldg(src + row * (D / 8) + (idx & 15)) : make_uint4(0, 0, 0, 0);
           const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
           for (int c = 0; c < 4; ++c)
@@ -835,23 +850,23 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
         float v = ls[h];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == 0) lred[warp * 8 + h] = v;
+        if (lane == 0) lred[warp * 16 + h] = v;
       }
       ptx::bar_sync_named(2, 128);
 #pragma unroll
-      for (int h = 0; h < G; ++h) lt[h] = lred[h] + lred[8 + h] + lred[16 + h] + lred[24 + h];
+      for (int h = 0; h < G; ++h) lt[h] = lred[h] + lred[16 + h] + lred[32 + h] + lred[48 + h];
       ptx::bar_sync_named(2, 128);
       const long long first = in.k - in.j;            // unit's first chunk (global)
       const long long last = first + in.nch - 1;       // unit's last chunk
       const int c0 = cta_of(first, Ktot, C);
       const int c1 = cta_of(last, Ktot, C);
       const int u = in.seq * Hkv + in.g;
-      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                         ((int64_t)in.seq * H + (int64_t)in.g * G) * D + t;
+      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + t;
       if (c0 == c1) {
 #pragma unroll
         for (int h = 0; h < G; ++h)
-          o[(int64_t)h * D] = __float2bfloat16_rn(FP8 ? (acc[h] * vsc) / lt[h] : acc[h] / lt[h]);
+          o[out_row(in.seq, in.g, h) * D] =
+              __float2bfloat16_rn(FP8 ? (acc[h] * vsc) / lt[h] : acc[h] / lt[h]);
       } else {
         // a piece of a split unit: leave the partial for the merge warp
         const int64_t slot = (int64_t)u * p.max_seg + ((int)blockIdx.x - c0);
@@ -867,13 +882,17 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
     auto acc_o = [&](int L, const Info& in, bool use_done) {
       const int b = L & 1;
       const uint32_t bph = (L >> 1) & 1;
-      float ov[FP8 ? 16 : 8];
+      float ov[FP8 || G > 8 ? 16 : 8];
       const bool good = wait_bar(sm, sm.bar(B_O_FULL + b), bph, p.err, 10);
       ptx::tc_fence_after();
       if constexpr (FP8) {
         ptx::tmem_ld_x16(tmem + lane_base + O_COL + 16 * b, ov);
       } else {
-        ptx::tmem_ld_x8(tmem + lane_base + O_COL + 16 * b, ov);
+        if constexpr (G > 8) {
+          ptx::tmem_ld_x16(tmem + lane_base + O_COL + 16 * b, ov);
+        } else {
+          ptx::tmem_ld_x8(tmem + lane_base + O_COL + 16 * b, ov);
+        }
       }
       ptx::tmem_ld_wait();
       ptx::tc_fence_before();
@@ -906,7 +925,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
       // ---- logits of this chunk ----
       // fp8: thread t holds tokens t and 128 + t (halves 0 and 1); per half
       // the three q parts of head h are columns h, 8 + h, 16 + h
-      float sv[FP8 ? 24 : 8], sv1[FP8 ? 24 : 1];
+      float sv[FP8 ? 24 : (G > 8 ? 16 : 8)], sv1[FP8 ? 24 : 1];
       bool good = wait_bar(sm, sm.bar(B_S_FULL + b), bph, p.err, 11);
       ptx::tc_fence_after();
       if constexpr (FP8) {
@@ -926,7 +945,11 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
           sv1[16 + i] = b8[i];
         }
       } else {
-        ptx::tmem_ld_x8(tmem + lane_base + S_W * b, sv);
+        if constexpr (G > 8) {
+          ptx::tmem_ld_x16(tmem + lane_base + S_W * b, sv);
+        } else {
+          ptx::tmem_ld_x8(tmem + lane_base + S_W * b, sv);
+        }
       }
       ptx::tmem_ld_wait();
       ptx::tc_fence_before();
@@ -948,18 +971,23 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
         }
       }
       const int valid = walk.valid();
+      // causal limit: column h (token h / gq of the unit's ntok) sees keys at
+      // positions < n - ntok + h / gq + 1, i.e. chunk rows t < tlim0 + h / gq
+      // (with ntok = 1 that is t < valid)
+      const int tlim0 = walk.n - p.ntok + 1 - walk.j * CH;
       float x[G], x1[G];  // x1: the token of half 1 (fp8 only)
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        x[h] = (good && t < valid) ? sv[h] * sscale : -INFINITY;
-        x1[h] = (FP8 && good && 128 + t < valid) ? sv1[FP8 ? h : 0] * sscale : -INFINITY;
+        const int tl = tlim0 + (h >> p.log2_gq);
+        x[h] = (good && t < tl) ? sv[h] * sscale : -INFINITY;
+        x1[h] = (FP8 && good && 128 + t < tl) ? sv1[FP8 ? h : 0] * sscale : -INFINITY;
       }
       // ---- chunk max per head over the 128 lanes ----
-      float* rb = red + b * 32;
+      float* rb = red + b * 64;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float v = ptx::warp_max_f32(FP8 ? fmaxf(x[h], x1[h]) : x[h]);
-        if (lane == 0) rb[warp * 8 + h] = v;
+        if (lane == 0) rb[warp * 16 + h] = v;
       }
       ptx::bar_sync_named(1, 128);
       if (walk.first_of_segment()) {
@@ -976,15 +1004,17 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
       uint8_t p_hi[NHALF][G], p_lo[NHALF][G];  // fp8: 256 p ~= hi + lo, two e4m3 codes
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const float cmax = fmaxf(fmaxf(rb[h], rb[8 + h]), fmaxf(rb[16 + h], rb[24 + h]));
+        const float cmax = fmaxf(fmaxf(rb[h], rb[16 + h]), fmaxf(rb[32 + h], rb[48 + h]));
         const float m_new = fmaxf(m[h], cmax);
-        alpha[h] = fast_exp2(m[h] - m_new);
+        // a column may have seen no visible key yet (multi-token units)
+        const float msafe = m_new == -INFINITY ? 0.f : m_new;
+        alpha[h] = fast_exp2(m[h] - msafe);
         m[h] = m_new;
-        const float pv = (t < valid) ? fast_exp2(x[h] - m_new) : 0.f;
+        const float pv = fast_exp2(x[h] - msafe);  // 0 for masked keys (x = -inf)
         if constexpr (FP8) {
           // 256 p in [0, 256] keeps e4m3's range; l carries the same factor,
           // so it cancels in acc / l.  The residual is exact (Sterbenz).
-          const float pv1 = (128 + t < valid) ? fast_exp2(x1[h] - m_new) : 0.f;
+          const float pv1 = fast_exp2(x1[h] - msafe);
           const float ps0 = pv * 256.f, ps1 = pv1 * 256.f;
           const uint16_t ch = pack_e4m3x2_rn(ps0, ps1);
           const float2 hv = e4m3x2_to_float2(ch);
@@ -1113,11 +1143,12 @@ cudaError_t launch_g(const TcLaunch& a, const Params& prm, const CUtensorMap& mk
 
 }  // namespace tc
 
-size_t tc_workspace_bytes(int64_t num_seqs, int64_t num_heads, int64_t max_ctx, int num_ctas) {
+size_t tc_workspace_bytes(int64_t num_seqs, int64_t num_heads, int64_t max_ctx, int num_ctas,
+                          int tokens_per_seq) {
   constexpr int64_t ch = tc::Cfg<false>::CH;  // the shorter chunk: an upper bound on pieces
   const int64_t max_chunks = (max_ctx + ch - 1) / ch;
   const int64_t max_seg = max_chunks < num_ctas ? max_chunks : num_ctas;
-  const int64_t rows = num_seqs * num_heads;  // >= units * G
+  const int64_t rows = num_seqs * (tokens_per_seq > 0 ? tokens_per_seq : 1) * num_heads;  // >= units * columns
   size_t off = 256;                                             // error word
   off += ((size_t)rows * 8 + 255) / 256 * 256;                  // merge counters
   off += ((size_t)rows * max_seg * 8 + 255) / 256 * 256;        // (m, l)
@@ -1125,11 +1156,15 @@ size_t tc_workspace_bytes(int64_t num_seqs, int64_t num_heads, int64_t max_ctx, 
   return off;
 }
 
-bool tc_supported(int head_dim, int group, bool fp8, int num_seqs, int block_size) {
+bool tc_supported(int head_dim, int group, bool fp8, int num_seqs, int block_size,
+                  int tokens_per_seq) {
   // block_size >= 8 keeps every TMA destination 1024-byte aligned (whole
-  // 128-byte-swizzle atoms)
-  (void)fp8;  // bf16 and fp8-e4m3 caches alike
-  return head_dim == tc::D && (group == 1 || group == 2 || group == 4 || group == 8) &&
+  // 128-byte-swizzle atoms).  A unit's columns (group x tokens) fill the MMA
+  // N: up to 16 for bf16, 8 for e4m3 (its q takes three rows per column).
+  const int t = tokens_per_seq > 0 ? tokens_per_seq : 1;
+  const int cols = group * t;
+  const bool pow2 = group > 0 && (group & (group - 1)) == 0 && (cols & (cols - 1)) == 0;
+  return head_dim == tc::D && pow2 && group <= 8 && cols <= (fp8 ? 8 : 16) &&
          num_seqs <= tc::kMaxSeqs && block_size >= 8 && tc::encode_fn() != nullptr;
 }
 
@@ -1165,12 +1200,16 @@ cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  const int ntok = a.tokens_per_seq > 0 ? a.tokens_per_seq : 1;
+  const int gq = a.num_heads / a.num_kv_heads;
   {
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)a.num_seqs * a.num_heads};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, NQ};
-    cuuint32_t es[2] = {1, 1};
-    if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.q), dims, strides, box,
+    // q as [tokens, H, d]; a unit's box is {64 of d, its gq heads, its ntok tokens}
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.num_heads,
+                          (cuuint64_t)a.num_seqs * ntok};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.num_heads * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)gq, (cuuint32_t)ntok};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -1186,7 +1225,7 @@ cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream) {
   prm.block_tables = a.block_tables;
   prm.context_lens = a.context_lens;
   char* ws = static_cast<char*>(a.workspace);
-  const int64_t rows = (int64_t)a.num_seqs * a.num_heads;
+  const int64_t rows = (int64_t)a.num_seqs * ntok * a.num_heads;
   prm.num_ctas = a.num_ctas;
   prm.max_seg = (int)(max_chunks < a.num_ctas ? max_chunks : a.num_ctas);
   size_t off = 0;
@@ -1199,6 +1238,13 @@ cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream) {
   prm.ws_o = reinterpret_cast<float*>(ws + off);
   prm.num_seqs = a.num_seqs;
   prm.num_heads = a.num_heads;
+  prm.gq = gq;
+  prm.ntok = ntok;
+  {
+    int lg = 0;
+    while ((1 << lg) < gq) ++lg;
+    prm.log2_gq = lg;
+  }
   prm.num_kv_heads = a.num_kv_heads;
   prm.max_blocks = a.max_blocks;
   prm.num_blocks = a.num_blocks;
@@ -1217,7 +1263,7 @@ cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream) {
     static std::atomic<unsigned long long> next_epoch{0x5eed00000000ull};
     prm.epoch = next_epoch.fetch_add(1, std::memory_order_relaxed) & 0xFFFFFFFFFFFFull;
   }
-  const int G = a.num_heads / a.num_kv_heads;
+  const int G = gq * ntok;  // columns of a unit
   if (a.fp8) {
     switch (G) {
       case 1: return launch_g<1, true>(a, prm, mk, mv, mq, stream);
@@ -1232,6 +1278,7 @@ cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream) {
     case 2: return launch_g<2, false>(a, prm, mk, mv, mq, stream);
     case 4: return launch_g<4, false>(a, prm, mk, mv, mq, stream);
     case 8: return launch_g<8, false>(a, prm, mk, mv, mq, stream);
+    case 16: return launch_g<16, false>(a, prm, mk, mv, mq, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -58,11 +58,14 @@ struct TcLaunch {
   void* workspace;  // >= tc_workspace_bytes(...)
   int num_seqs, num_heads, num_kv_heads, max_blocks, num_blocks, block_size;
   int num_ctas;     // persistent CTAs (one per SM)
+  int tokens_per_seq;  // new tokens per sequence (1: decode); q/out hold S * this rows
   float scale;
   bool early_meta;  // the previous kernel only wrote the cache (see decode_tc.cu)
 };
-bool tc_supported(int head_dim, int group, bool fp8, int num_seqs, int block_size);
-size_t tc_workspace_bytes(int64_t num_seqs, int64_t num_heads, int64_t max_ctx, int num_ctas);
+bool tc_supported(int head_dim, int group, bool fp8, int num_seqs, int block_size,
+                  int tokens_per_seq = 1);
+size_t tc_workspace_bytes(int64_t num_seqs, int64_t num_heads, int64_t max_ctx, int num_ctas,
+                          int tokens_per_seq = 1);
 cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream);
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value,
@@ -76,8 +79,8 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value,
 
 cudaError_t launch_varlen_meta(const int32_t* block_tables, int max_blocks, int block_size,
                                const int32_t* seq_lens, const int32_t* query_start_loc,
-                               int num_seqs, int num_tokens, int32_t* vtables, int32_t* vlens,
-                               cudaStream_t stream);
+                               int uniform_tokens, int num_seqs, int num_tokens, int32_t* vtables,
+                               int32_t* vlens, cudaStream_t stream);
 
 cudaError_t launch_step_prepare(int32_t* block_tables, int max_blocks, int block_size,
                                 int32_t* context_lens, int num_seqs, const int32_t* updates,

@@ -169,6 +169,40 @@ def varlen_attention(out, q, k_cache, v_cache, block_tables, seq_lens, query_sta
     return out
 
 
+def decode_multi_workspace_size(num_seqs, tokens_per_seq, num_heads, head_dim,
+                                max_blocks_per_seq, block_size) -> int:
+    return int(_lib.lib().pa_decode_multi_workspace_size(num_seqs, tokens_per_seq, num_heads,
+                                                         head_dim, max_blocks_per_seq,
+                                                         block_size))
+
+
+def decode_multi(out, q, k_cache, v_cache, block_tables, context_lens, tokens_per_seq, scale,
+                 k_scale=None, v_scale=None, workspace=None, stream=None):
+    """Causal attention for ``tokens_per_seq`` new tokens of every sequence:
+    q/out [num_seqs * tokens_per_seq, H_q, d], sequence i's tokens at rows
+    i * tokens_per_seq + j (the last positions of its context)."""
+    _same_cache(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    ks, vs = _scales(desc, k_scale, v_scale)
+    num_seqs = int(context_lens.numel())
+    if q.dim() != 3 or out.shape != q.shape or q.shape[0] != num_seqs * tokens_per_seq:
+        raise ValueError("q and out must be [num_seqs * tokens_per_seq, num_heads, head_dim]")
+    _, num_heads, head_dim = q.shape
+    max_blocks = int(block_tables.shape[1])
+    if workspace is None:
+        n = decode_multi_workspace_size(num_seqs, tokens_per_seq, num_heads, head_dim,
+                                        max_blocks, desc.block_size)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    _lib.check(_lib.lib().pa_decode_multi(
+        _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), desc, _dev(block_tables, "block_tables", torch.int32),
+        max_blocks, _dev(context_lens, "context_lens", torch.int32), num_seqs,
+        int(tokens_per_seq), int(num_heads), ctypes.c_float(scale), ks, vs,
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return out
+
+
 def swap_blocks(dst_k, dst_v, src_k, src_v, block_pairs, stream=None) -> None:
     """dst[d] = src[s] for each (s, d) row of ``block_pairs`` [n, 2] int32,
     between two caches of the same block shape (device pool <-> pinned host

@@ -119,3 +119,41 @@ def test_one_token_per_request_equals_decode_bit_for_bit():
                torch.from_numpy(c["seq_lens"]).cuda(), 0.08, workspace=ws)
     torch.cuda.synchronize()
     assert np.array_equal(got, out.float().cpu().numpy().astype(np.float64))
+
+
+def _check_multi(c, T, scale):
+    q = harness.to_dev_bits(c["q"], "bf16", "cuda")
+    out = torch.empty_like(q)
+    ops.decode_multi(out, q, c["kc"], c["vc"], torch.from_numpy(c["tables"]).cuda(),
+                     torch.from_numpy(c["seq_lens"]).cuda(), T, scale, c["ks"], c["vs"])
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy().astype(np.float64)
+    ref = varlen.varlen_attention(c["q"], harness.bits_from_dev(c["kc"]),
+                                  harness.bits_from_dev(c["vc"]), c["tables"], c["seq_lens"],
+                                  c["qsl"], scale, c["kscale"], c["vscale"])
+    harness.assert_close(got, ref, c["kv"] == "fp8")
+    return got
+
+
+@requires_gpu
+@pytest.mark.parametrize("T,hq,hkv,kv", [(2, 32, 8, "bf16"), (4, 32, 8, "bf16"),
+                                         (2, 64, 8, "bf16"), (8, 8, 8, "bf16"),
+                                         (16, 8, 8, "bf16"), (2, 32, 8, "fp8"),
+                                         (4, 32, 8, "fp8"), (3, 32, 8, "bf16")])
+def test_multi_token_decode_one_pass_and_fallback(T, hq, hkv, kv):
+    # group x T columns: 8 and 16 run one tensor-core pass; fp8 with 16
+    # columns and T = 3 (12 columns) take the per-token path
+    rng = np.random.default_rng(10 + T)
+    lens = [int(x) for x in rng.integers(T, 2600, size=24)] + [T, T + 1, 129]
+    c = _setup(lens, [T] * len(lens), hq, hkv, 128, 16, kv, seed=11 + T)
+    _check_multi(c, T, 128 ** -0.5)
+
+
+@requires_gpu
+def test_multi_token_split_units_with_masked_columns():
+    # few long sequences: units split over many CTAs, and pieces near a
+    # sequence's end hold keys that some of its tokens must not see
+    lens = [4096, 9000, 130, 16384]
+    c = _setup(lens, [4] * 4, 32, 8, 128, 16, seed=21)
+    got = _check_multi(c, 4, 0.09)
+    assert np.isfinite(got).all()
