@@ -503,8 +503,14 @@ def run_e2e(step, args, device, dist):
     w = step.w
     # The step's inputs travel as one packed pinned buffer (one host->device
     # copy per step); the device-side views point into one staging buffer.
+    # With the captured single-token step the slots are derived in the graph
+    # from the tables and lengths (pa_step_prepare); otherwise the host maps
+    # them every step and they travel with the other inputs.
+    device_slots = step.kernel == 0 and step.new_tokens == 1
     parts = [("q", step.q), ("k", step.k_new), ("v", step.v_new),
-             ("bt", step.block_tables), ("cl", step.context_lens), ("slots", step.slots)]
+             ("bt", step.block_tables), ("cl", step.context_lens)]
+    if not device_slots:
+        parts.append(("slots", step.slots))
     offs, total = {}, 0
     for name, t in parts:
         offs[name] = total
@@ -525,20 +531,25 @@ def run_e2e(step, args, device, dist):
     bi = total
     bo = h_out.numel() * h_out.element_size()
 
-    h_v["slots"].numpy()[:] = step.pool.slot_mapping(w.block_tables, w.block_size,
-                                                     step.positions, step.token_seq)
     graph = None
-    if step.kernel == 0 and step.new_tokens == 1:
-        # the step as one captured graph: packed inputs in, write + decode, output out
-        graph = step.ops.StepGraph(d_v["k"], d_v["v"], d_v["slots"], step.out, d_v["q"],
+    if device_slots:
+        # the step as one captured graph: packed inputs in, slots from the
+        # tables and lengths, write + decode, output out
+        d_slots = torch.empty(w.num_seqs, dtype=torch.int32, device=device)
+        graph = step.ops.StepGraph(d_v["k"], d_v["v"], d_slots, step.out, d_v["q"],
                                    step.k_cache, step.v_cache, d_v["bt"], d_v["cl"], w.scale,
                                    step.k_scale, step.v_scale, step.ws,
-                                   h2d=[(d_in, h_in)], d2h=[(h_out, step.out)])
-
-    def one():
-        # host slot mapping of the step's new tokens into the pinned staging
+                                   h2d=[(d_in, h_in)], d2h=[(h_out, step.out)],
+                                   device_slots=True)
+    else:
         h_v["slots"].numpy()[:] = step.pool.slot_mapping(w.block_tables, w.block_size,
                                                          step.positions, step.token_seq)
+
+    def one():
+        if graph is None:
+            # host slot mapping of the step's new tokens into the pinned staging
+            h_v["slots"].numpy()[:] = step.pool.slot_mapping(w.block_tables, w.block_size,
+                                                             step.positions, step.token_seq)
         if graph is not None:
             graph.replay()
         else:
@@ -564,9 +575,10 @@ def run_e2e(step, args, device, dist):
     return {"value": round(job_throughput(world, sbytes, dt) / 1e9, 2), "unit": "GB/s",
             "us_per_step": round(dt * 1e6, 2), "h2d_bytes_per_step": bi,
             "d2h_bytes_per_step": bo,
-            "path": ("host slot mapping, then one replay of the captured step (H2D of the "
-                     "packed inputs, pa_write_and_decode, D2H of the output), then a stream "
-                     "synchronise" if graph is not None else
+            "path": ("one replay of the captured step (H2D of the packed inputs: q, new K/V, "
+                     "tables, lengths; slots from tables and lengths on the device "
+                     "(pa_step_prepare); pa_write_and_decode; D2H of the output), then a "
+                     "stream synchronise" if graph is not None else
                      "host slot mapping, H2D, the library calls, D2H, stream synchronise")}
 
 

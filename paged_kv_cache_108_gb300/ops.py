@@ -291,7 +291,7 @@ class StepGraph:
 
     def __init__(self, key, value, slot_mapping, out, q, k_cache, v_cache, block_tables,
                  context_lens, scale, k_scale=None, v_scale=None, workspace=None, h2d=(),
-                 d2h=()):
+                 d2h=(), device_slots=False):
         self._h2d = list(h2d)
         self._d2h = list(d2h)
         for dev_t, host_t in self._h2d:
@@ -304,6 +304,9 @@ class StepGraph:
                 raise ValueError("d2h destinations must be pinned host tensors")
         self._args = (key, value, slot_mapping, out, q, k_cache, v_cache, block_tables,
                       context_lens, scale, k_scale, v_scale, workspace)
+        # device_slots: the slots of the new tokens are computed in the graph
+        # from the tables and lengths (pa_step_prepare) instead of being copied in
+        self._device_slots = bool(device_slots)
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
@@ -316,6 +319,9 @@ class StepGraph:
     def _body(self):
         for dev_t, host_t in self._h2d:
             dev_t.copy_(host_t, non_blocking=True)
+        if self._device_slots:
+            key, value, slots, out, q, kc, vc, bt, cl = self._args[:9]
+            step_prepare(bt, cl, kc.shape[1], slots)
         write_and_decode(*self._args)
         for host_t, dev_t in self._d2h:
             host_t.copy_(dev_t, non_blocking=True)

@@ -87,3 +87,28 @@ def test_captured_step_rejects_pageable_staging():
         ops.StepGraph(st["k"], st["v"], st["slots"], out, dev["q"], dev["k_cache"],
                       dev["v_cache"], dev["bt"], dev["cl"], w.scale, workspace=dev["ws"],
                       h2d=[(dev["q"], torch.empty_like(dev["q"], device="cpu"))])
+
+
+@requires_gpu
+def test_captured_step_with_device_slots_matches_host_slots():
+    """device_slots=True: the graph derives the new tokens' slots from the
+    tables and lengths (pa_step_prepare); caches and outputs must equal the
+    eager step fed with host-computed slots, bit for bit."""
+    w = synth.make("graph-devslots", synth.llama8b_lengths(20), 32, 8, 128, 16, seed=73)
+    dev, st = _setup(w)
+    eager_k, eager_v = dev["k_cache"].clone(), dev["v_cache"].clone()
+    out_e = torch.empty_like(dev["q"])
+    ops.write_and_decode(st["k"], st["v"], st["slots"], out_e, dev["q"], eager_k, eager_v,
+                         dev["bt"], dev["cl"], w.scale, workspace=dev["ws"])
+    slots = torch.full_like(st["slots"], -7)
+    out_g = torch.empty_like(dev["q"])
+    h_out = torch.empty(out_g.shape, dtype=torch.bfloat16).pin_memory()
+    g = ops.StepGraph(st["k"], st["v"], slots, out_g, dev["q"], dev["k_cache"], dev["v_cache"],
+                      dev["bt"], dev["cl"], w.scale, workspace=dev["ws"], d2h=[(h_out, out_g)],
+                      device_slots=True)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(slots, st["slots"])
+    assert torch.equal(h_out, out_e.cpu())
+    assert np.array_equal(harness.bits_from_dev(dev["k_cache"]), harness.bits_from_dev(eager_k))
+    assert np.array_equal(harness.bits_from_dev(dev["v_cache"]), harness.bits_from_dev(eager_v))
