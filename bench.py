@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--new-tokens", type=int, default=1,
                     help="tokens each sequence adds per step (> 1: multi-token step through "
                          "pa_varlen_attention, e.g. speculative decoding)")
+    ap.add_argument("--shared-prefix-group", type=int, default=0,
+                    help="decode through pa_decode_shared_prefix with groups of this many "
+                         "sequences (serving workload: 8); 0 = pa_decode")
     ap.add_argument("--block-size", type=int, default=16,
                     help="tokens per physical block (llama8b workload: 1, 16, 64, 256)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -129,7 +132,7 @@ class Step:
     """Device-resident state of one decode step of a workload."""
 
     def __init__(self, device, partition=0, kernel=0, kv_dtype="bf16", workload="llama8b",
-                 block_size=16, new_tokens=1):
+                 block_size=16, new_tokens=1, shared_prefix_group=0):
         import torch
 
         from paged_kv_cache_108_gb300 import ops, pool, synth
@@ -176,7 +179,12 @@ class Step:
         self.block_tables = torch.from_numpy(w.block_tables).to(device)
         self.context_lens = torch.from_numpy(w.context_lens).to(device)
         self.out = torch.empty_like(self.q)
-        if T == 1:
+        self.group = shared_prefix_group
+        if T == 1 and self.group:
+            n = max(ops.decode_shared_prefix_workspace_size(S, self.group, H, d, w.max_blocks, B),
+                    ops.decode_workspace_size(S, H, d, w.max_blocks, B))
+            self.ws = torch.empty(n, dtype=torch.uint8, device=device)
+        elif T == 1:
             self.ws = ops.alloc_workspace(S, H, d, w.max_blocks, B, partition, device=device)
         else:
             n = ops.decode_multi_workspace_size(S, T, H, d, w.max_blocks, B)
@@ -188,6 +196,9 @@ class Step:
         tc = kernel == 2 or (kernel == 0 and d == 128 and B >= 8 and S <= 1024 and G in (1, 2, 4, 8))
         splits = int(np.max(w.context_lens)) > (partition or 256)
         self.launches_per_step = 2 + (1 if not tc and splits else 0)
+        if shared_prefix_group:
+            # metadata, prefix pass, suffix pass, merge -- plus the cache write
+            self.launches_per_step = 5
 
     # algorithmic bytes of one step (what the method must move): K/V rows
     # stored once are read once (shared prefix blocks count once)
@@ -213,7 +224,7 @@ class Step:
     def run_step(self, slots=None, k=None, v=None, q=None, bt=None, cl=None):
         """The step as one call: cache write of the new tokens, then decode."""
         w = self.w
-        if self.new_tokens > 1:
+        if self.new_tokens > 1 or self.group:
             self.run_write(slots, k, v)
             self.run_decode(q, bt, cl)
             return
@@ -226,6 +237,12 @@ class Step:
 
     def run_decode(self, q=None, bt=None, cl=None):
         w = self.w
+        if self.group:
+            self.ops.decode_shared_prefix(self.out, self.q if q is None else q, self.k_cache,
+                                          self.v_cache, self.block_tables if bt is None else bt,
+                                          self.context_lens if cl is None else cl, self.group,
+                                          w.scale, self.k_scale, self.v_scale, workspace=self.ws)
+            return
         if self.new_tokens > 1:
             self.ops.decode_multi(self.out, self.q if q is None else q, self.k_cache,
                                   self.v_cache, self.block_tables if bt is None else bt,
@@ -367,7 +384,7 @@ def run_ours(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     step = Step(device, args.partition, args.kernel, args.kv_dtype, args.workload,
-                args.block_size, args.new_tokens)
+                args.block_size, args.new_tokens, args.shared_prefix_group)
     stream = torch.cuda.current_stream()
     # L2 flush: read a buffer 4x the L2 size.  Reading (not writing) leaves
     # only clean lines behind, so the timed kernels do not pay for writing
@@ -456,6 +473,8 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": f"{WORKLOADS[args.workload]}, "
                                + (f"{step.new_tokens} new tokens per sequence "
                                   "(pa_decode_multi), " if step.new_tokens > 1 else "")
+                               + (f"shared-prefix groups of {step.group} "
+                                  "(pa_decode_shared_prefix), " if step.group else "")
                                + f"{'e4m3 (per-tensor scale)' if step.fp8 else 'bf16'} KV, "
                                f"block {w.block_size}, sum ctx {int(np.sum(w.context_lens))}",
                    "num_seqs": w.num_seqs,
@@ -506,7 +525,7 @@ def run_e2e(step, args, device, dist):
     # With the captured single-token step the slots are derived in the graph
     # from the tables and lengths (pa_step_prepare); otherwise the host maps
     # them every step and they travel with the other inputs.
-    device_slots = step.kernel == 0 and step.new_tokens == 1
+    device_slots = step.kernel == 0 and step.new_tokens == 1 and not step.group
     parts = [("q", step.q), ("k", step.k_new), ("v", step.v_new),
              ("bt", step.block_tables), ("cl", step.context_lens)]
     if not device_slots:

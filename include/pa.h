@@ -329,6 +329,39 @@ pa_status pa_decode_multi(void* out, const void* q, const void* k_cache, const v
                           void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * pa_decode_shared_prefix -- pa_decode for a batch whose consecutive groups
+ * of group_size sequences were forked from a common prefix (parallel
+ * sampling, beam search, or requests sharing a system prompt through the
+ * prefix cache): the shared blocks are read once per group instead of once
+ * per member.  [LSB] "Copy-on-write for shared prefixes" (members' tables
+ * point at the same physical blocks); [LSB] "How Paging Unlocks
+ * High-Throughput Serving" (a prefix stored once and reused).  The pages
+ * share the memory; reading it once is this library's addition, with the
+ * same result as pa_decode.
+ *
+ * Sequence i belongs to group i / group_size.  A group's prefix is found on
+ * the device: the longest run of leading block-table entries equal in all
+ * its members' rows, capped at every member's whole blocks.  Pass 1 attends
+ * each group's prefix once with all members' queries as the tensor-core
+ * kernel's columns; pass 2 attends each sequence's remaining blocks; a
+ * third kernel merges the two results by their log-sum-exp.  Needs the
+ * tensor-core kernel for both passes (group x GQA group <= 16 for bf16, 8
+ * for e4m3); otherwise, and for group_size 1, it runs pa_decode.
+ *  workspace  >= pa_decode_shared_prefix_workspace_size(...), 256-byte aligned.
+ *  Other arguments as pa_decode; num_seqs must be a multiple of group_size.
+ * ---------------------------------------------------------------------- */
+size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t group_size,
+                                              int32_t num_heads, int32_t head_dim,
+                                              int32_t max_blocks_per_seq, int32_t block_size);
+pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
+                                  const void* v_cache, pa_cache_desc cache,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens, int32_t num_seqs,
+                                  int32_t group_size, int32_t num_heads, float scale,
+                                  const float* k_scale, const float* v_scale, void* workspace,
+                                  size_t workspace_bytes, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * pa_swap_blocks -- copy whole blocks between two caches of the same block
  * shape: dst[d] = src[s] for K and V, for every (s, d) pair.  An exhausted
  * pool must preempt a sequence ([LSB] BlockManager.allocate), and the

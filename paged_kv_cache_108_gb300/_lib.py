@@ -65,6 +65,9 @@ SIGNATURES = {
     "pa_swap_blocks": (I32, [P, P, I32, P, P, I32, CacheDesc, P, I32, P]),
     "pa_varlen_workspace_size": (ctypes.c_size_t, [I32, I32, I32, I32, I32]),
     "pa_decode_multi_workspace_size": (ctypes.c_size_t, [I32, I32, I32, I32, I32, I32]),
+    "pa_decode_shared_prefix_workspace_size": (ctypes.c_size_t, [I32, I32, I32, I32, I32, I32]),
+    "pa_decode_shared_prefix": (I32, [P, P, P, P, CacheDesc, P, I32, P, I32, I32, I32,
+                                      ctypes.c_float, P, P, P, ctypes.c_size_t, P]),
     "pa_decode_multi": (I32, [P, P, P, P, CacheDesc, P, I32, P, I32, I32, I32, ctypes.c_float,
                               P, P, P, ctypes.c_size_t, P]),
     "pa_varlen_attention": (I32, [P, P, P, P, CacheDesc, P, I32, P, P, I32, I32, I32, ctypes.c_float, P, P,

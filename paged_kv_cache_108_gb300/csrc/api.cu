@@ -209,7 +209,8 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
                              const float* k_scale, const float* v_scale, void* workspace,
                              size_t workspace_bytes, const pa_decode_opts* opts,
                              pa_stream_t stream, bool prev_writes_cache_only,
-                             int32_t tokens_per_seq = 1) {
+                             int32_t tokens_per_seq = 1, bool non_causal = false,
+                             float* lse = nullptr) {
   const char* fn = "pa_decode";
   char buf[224];
   pa_status st = check_cache(cache, fn);
@@ -278,6 +279,8 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
     a.block_size = cache.block_size;
     a.num_ctas = nsm;
     a.tokens_per_seq = tokens_per_seq;
+    a.non_causal = non_causal;
+    a.lse = lse;
     a.scale = scale;
     a.early_meta = prev_writes_cache_only;
     return cuda_status(pa::launch_decode_tc(a, reinterpret_cast<cudaStream_t>(stream)), fn);
@@ -518,6 +521,95 @@ pa_status pa_decode_multi(void* out, const void* q, const void* k_cache, const v
   return decode_impl(out, q, k_cache, v_cache, cache, vtables, max_blocks_per_seq, vlens, n,
                      num_heads, scale, k_scale, v_scale, ws + meta, workspace_bytes - meta,
                      nullptr, stream, false);
+}
+
+size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t group_size,
+                                              int32_t num_heads, int32_t head_dim,
+                                              int32_t max_blocks_per_seq, int32_t block_size) {
+  if (num_seqs <= 0 || group_size <= 0 || num_seqs % group_size || num_heads <= 0 ||
+      head_dim <= 0 || max_blocks_per_seq <= 0 || block_size <= 0)
+    return 0;
+  const int64_t S = num_seqs, V = num_seqs / group_size, rows = S * num_heads;
+  const int64_t max_ctx = (int64_t)max_blocks_per_seq * block_size;
+  size_t off = align256((size_t)V * max_blocks_per_seq * 4) + align256((size_t)V * 4) +
+               align256((size_t)S * max_blocks_per_seq * 4) + align256((size_t)S * 4);
+  off += 2 * (align256((size_t)rows * head_dim * 2) + align256((size_t)rows * 4));
+  const size_t pre = pa::tc_workspace_bytes(V, num_heads, max_ctx, num_sms(), group_size);
+  const size_t suf = pa_decode_workspace_size(num_seqs, num_heads, head_dim, max_blocks_per_seq,
+                                              block_size);
+  return off + (pre > suf ? pre : suf);
+}
+
+pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache,
+                                  const void* v_cache, pa_cache_desc cache,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* context_lens, int32_t num_seqs,
+                                  int32_t group_size, int32_t num_heads, float scale,
+                                  const float* k_scale, const float* v_scale, void* workspace,
+                                  size_t workspace_bytes, pa_stream_t stream) {
+  const char* fn = "pa_decode_shared_prefix";
+  if (num_seqs < 0 || group_size <= 0 || max_blocks_per_seq <= 0 || num_heads <= 0)
+    return pa_fail(PA_ERR_INVALID, "pa_decode_shared_prefix: bad sizes");
+  if (num_seqs == 0) return PA_OK;
+  if (num_seqs % group_size)
+    return pa_fail(PA_ERR_INVALID, "pa_decode_shared_prefix: num_seqs is not a multiple of group_size");
+  pa_status st = check_cache(cache, fn);
+  if (st != PA_OK) return st;
+  if (num_heads % cache.num_kv_heads != 0)
+    return pa_fail(PA_ERR_INVALID, "pa_decode_shared_prefix: num_heads is not a multiple of num_kv_heads");
+  const int gq = num_heads / cache.num_kv_heads;
+  const bool fp8 = cache.dtype == PA_KV_FP8_E4M3;
+  const int V = num_seqs / group_size;
+  const bool tc = pa::tc_supported(cache.head_dim, gq, fp8, V, cache.block_size, group_size) &&
+                  pa::tc_supported(cache.head_dim, gq, fp8, num_seqs, cache.block_size, 1);
+  if (group_size == 1 || !tc)  // nothing to share, or the passes need the tensor cores
+    return decode_impl(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, num_heads, scale, k_scale, v_scale, workspace,
+                       workspace_bytes, nullptr, stream, false);
+  if (!out || !q || !block_tables || !context_lens || !workspace)
+    return pa_fail(PA_ERR_INVALID, "pa_decode_shared_prefix: NULL pointer");
+  if (!aligned(workspace, 256) || !aligned(out, 16))
+    return pa_fail(PA_ERR_INVALID, "pa_decode_shared_prefix: misaligned pointer");
+  const size_t need = pa_decode_shared_prefix_workspace_size(
+      num_seqs, group_size, num_heads, cache.head_dim, max_blocks_per_seq, cache.block_size);
+  if (workspace_bytes < need) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "pa_decode_shared_prefix: workspace of %zu bytes needed", need);
+    return pa_fail(PA_ERR_INVALID, buf);
+  }
+  const int64_t rows = (int64_t)num_seqs * num_heads;
+  char* ws = static_cast<char*>(workspace);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* p = ws + off;
+    off += align256(bytes);
+    return p;
+  };
+  int32_t* ptables = reinterpret_cast<int32_t*>(take((size_t)V * max_blocks_per_seq * 4));
+  int32_t* plens = reinterpret_cast<int32_t*>(take((size_t)V * 4));
+  int32_t* stables = reinterpret_cast<int32_t*>(take((size_t)num_seqs * max_blocks_per_seq * 4));
+  int32_t* slens = reinterpret_cast<int32_t*>(take((size_t)num_seqs * 4));
+  void* o_pre = take((size_t)rows * cache.head_dim * 2);
+  float* l_pre = reinterpret_cast<float*>(take((size_t)rows * 4));
+  void* o_suf = take((size_t)rows * cache.head_dim * 2);
+  float* l_suf = reinterpret_cast<float*>(take((size_t)rows * 4));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = pa::launch_cascade_meta(block_tables, max_blocks_per_seq, cache.block_size,
+                                          context_lens, num_seqs, group_size, ptables, plens,
+                                          stables, slens, s);
+  if (e != cudaSuccess) return cuda_status(e, fn);
+  // pass 1: each group's shared prefix, read once, its members' queries as columns
+  st = decode_impl(o_pre, q, k_cache, v_cache, cache, ptables, max_blocks_per_seq, plens, V,
+                   num_heads, scale, k_scale, v_scale, ws + off, workspace_bytes - off, nullptr,
+                   stream, false, group_size, true, l_pre);
+  if (st != PA_OK) return st;
+  // pass 2: every sequence's own blocks after the prefix
+  st = decode_impl(o_suf, q, k_cache, v_cache, cache, stables, max_blocks_per_seq, slens,
+                   num_seqs, num_heads, scale, k_scale, v_scale, ws + off, workspace_bytes - off,
+                   nullptr, stream, false, 1, false, l_suf);
+  if (st != PA_OK) return st;
+  return cuda_status(pa::launch_lse_merge(o_pre, l_pre, o_suf, l_suf, out, rows, cache.head_dim, s),
+                     fn);
 }
 
 pa_status pa_swap_blocks(void* dst_k, void* dst_v, int32_t dst_num_blocks, const void* src_k,

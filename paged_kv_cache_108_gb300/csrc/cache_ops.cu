@@ -203,7 +203,92 @@ __global__ void varlen_meta_kernel(const int32_t* __restrict__ block_tables, int
   for (int k = threadIdx.x; k < nb; k += blockDim.x) dst[k] = src[k];
 }
 
+// Shared-prefix (cascade) split of a batch whose consecutive groups of m
+// sequences were forked from a common prefix.  CTA i handles sequence i of
+// group v = i / m (leader L = v * m).  The group's shared prefix is the
+// longest run of leading block-table entries equal in every member's row,
+// capped at each member's whole blocks (a member never attends past its own
+// context); the leader's CTA writes the prefix row (its first P blocks) and
+// length, and every CTA writes its sequence's suffix row (the entries after
+// the prefix) and length n_i - P * B.
+__global__ void cascade_meta_kernel(const int32_t* __restrict__ block_tables, int max_blocks,
+                                    int block_size, const int32_t* __restrict__ context_lens,
+                                    int group, int32_t* __restrict__ ptables,
+                                    int32_t* __restrict__ plens, int32_t* __restrict__ stables,
+                                    int32_t* __restrict__ slens) {
+  const int i = blockIdx.x;
+  const int L = i - i % group;
+  __shared__ int s_pb;
+  if (threadIdx.x == 0) {
+    int pb = max_blocks;
+    for (int j = 0; j < group; ++j) {
+      const int n = context_lens[L + j];
+      pb = min(pb, n > 0 ? n / block_size : 0);
+    }
+    s_pb = pb;
+  }
+  __syncthreads();
+  // first index where some member's row differs from the leader's
+  const int32_t* lead = block_tables + (int64_t)L * max_blocks;
+  for (int k = threadIdx.x; k < s_pb; k += blockDim.x) {
+    bool same = true;
+    for (int j = 1; j < group; ++j) same &= block_tables[(int64_t)(L + j) * max_blocks + k] == lead[k];
+    if (!same) atomicMin(&s_pb, k);
+  }
+  __syncthreads();
+  const int pb = s_pb;
+  if (i == L) {
+    for (int k = threadIdx.x; k < pb; k += blockDim.x) ptables[(int64_t)(L / group) * max_blocks + k] = lead[k];
+    if (threadIdx.x == 0) plens[L / group] = pb * block_size;
+  }
+  const int n = max(context_lens[i], 0);
+  const int nb = (n + block_size - 1) / block_size;
+  const int32_t* row = block_tables + (int64_t)i * max_blocks;
+  for (int k = threadIdx.x; k + pb < nb; k += blockDim.x)
+    stables[(int64_t)i * max_blocks + k] = row[pb + k];
+  if (threadIdx.x == 0) slens[i] = n - pb * block_size;
+}
+
+// out = the two partial results combined by their log2-sum-exp weights
+// (rows with both weights zero, i.e. no key at all, get zeros).
+__global__ void lse_merge_kernel(const __nv_bfloat16* __restrict__ o1,
+                                 const float* __restrict__ l1,
+                                 const __nv_bfloat16* __restrict__ o2,
+                                 const float* __restrict__ l2, __nv_bfloat16* __restrict__ out,
+                                 int64_t rows, int head_dim) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * head_dim) return;
+  const int64_t r = idx / head_dim;
+  const float a = l1[r], b = l2[r];
+  const float m = fmaxf(a, b);
+  float res = 0.f;
+  if (m != -INFINITY) {
+    const float wa = exp2f(a - m), wb = exp2f(b - m);
+    res = (wa * __bfloat162float(o1[idx]) + wb * __bfloat162float(o2[idx])) / (wa + wb);
+  }
+  out[idx] = __float2bfloat16_rn(res);
+}
+
 }  // namespace
+
+cudaError_t launch_cascade_meta(const int32_t* block_tables, int max_blocks, int block_size,
+                                const int32_t* context_lens, int num_seqs, int group,
+                                int32_t* ptables, int32_t* plens, int32_t* stables,
+                                int32_t* slens, cudaStream_t stream) {
+  cascade_meta_kernel<<<num_seqs, 128, 0, stream>>>(block_tables, max_blocks, block_size,
+                                                    context_lens, group, ptables, plens, stables,
+                                                    slens);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge(const void* o1, const float* l1, const void* o2, const float* l2,
+                             void* out, int64_t rows, int head_dim, cudaStream_t stream) {
+  const int64_t n = rows * head_dim;
+  lse_merge_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o1), l1, static_cast<const __nv_bfloat16*>(o2), l2,
+      static_cast<__nv_bfloat16*>(out), rows, head_dim);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_varlen_meta(const int32_t* block_tables, int max_blocks, int block_size,
                                const int32_t* seq_lens, const int32_t* query_start_loc,

@@ -142,6 +142,8 @@ struct Params {
   // positions of its context; ntok = 1 for decode).  Token j sees keys at
   // positions < n - ntok + j + 1.
   int gq, log2_gq, ntok;
+  int causal;                // 0: every column sees all n keys (a shared prefix)
+  float* lse;                // optional [rows]: log2-sum-exp of each output row's logits
   const void* q;             // [S * ntok, H, D] bf16 (read directly by the fp8 kernel's q warp)
   const float* k_scale;      // fp8: per-tensor dequantisation scales (device scalars)
   const float* v_scale;
@@ -440,8 +442,12 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
     // empty sequences get zero rows (spread over the CTAs)
     for (int i = blockIdx.x; i < S; i += gridDim.x) {
       if (nl[i] <= 0) {
-        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + (int64_t)i * H * D;
-        for (int e = tid; e < H * D; e += 128) o[e] = __float2bfloat16_rn(0.f);
+        // all rows of the sequence's tokens: zero output, log2-sum-exp -inf
+        const int64_t rows = (int64_t)p.ntok * H;
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + (int64_t)i * rows * D;
+        for (int64_t e = tid; e < rows * D; e += 128) o[e] = __float2bfloat16_rn(0.f);
+        if (p.lse)
+          for (int64_t r = tid; r < rows; r += 128) p.lse[(int64_t)i * rows + r] = -INFINITY;
       }
     }
   }
@@ -738,6 +744,11 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
         for (int r = 0; r < 4; ++r)
           o[out_row(walk.seq, walk.g, h) * D + 32 * r] =
               __float2bfloat16_rn(FP8 ? (a[h][r] * __ldg(p.v_scale)) / Ls[h] : a[h][r] / Ls[h]);
+      if (p.lse && lane < G) {
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+          if (lane == h) p.lse[out_row(walk.seq, walk.g, h)] = M[h] + __log2f(Ls[h]) - (FP8 ? 8.f : 0.f);
+      }
       if (lane == 0) p.counters[u] = p.epoch << 16;  // count 0: a replay starts afresh
     }
   } else if (warp == 7) {
@@ -867,6 +878,12 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
         for (int h = 0; h < G; ++h)
           o[out_row(in.seq, in.g, h) * D] =
               __float2bfloat16_rn(FP8 ? (acc[h] * vsc) / lt[h] : acc[h] / lt[h]);
+        if (p.lse) {
+          // log2 of the softmax denominator (e4m3: l carries a factor 256)
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            if (t == h) p.lse[out_row(in.seq, in.g, h)] = ms[h] + __log2f(lt[h]) - (FP8 ? 8.f : 0.f);
+        }
       } else {
         // a piece of a split unit: leave the partial for the merge warp
         const int64_t slot = (int64_t)u * p.max_seg + ((int)blockIdx.x - c0);
@@ -974,11 +991,11 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
       // causal limit: column h (token h / gq of the unit's ntok) sees keys at
       // positions < n - ntok + h / gq + 1, i.e. chunk rows t < tlim0 + h / gq
       // (with ntok = 1 that is t < valid)
-      const int tlim0 = walk.n - p.ntok + 1 - walk.j * CH;
+      const int tlim0 = walk.n - (p.causal ? p.ntok - 1 : 0) - walk.j * CH;
       float x[G], x1[G];  // x1: the token of half 1 (fp8 only)
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const int tl = tlim0 + (h >> p.log2_gq);
+        const int tl = tlim0 + (p.causal ? (h >> p.log2_gq) : 0);
         x[h] = (good && t < tl) ? sv[h] * sscale : -INFINITY;
         x1[h] = (FP8 && good && 128 + t < tl) ? sv1[FP8 ? h : 0] * sscale : -INFINITY;
       }
@@ -1240,6 +1257,8 @@ cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream) {
   prm.num_heads = a.num_heads;
   prm.gq = gq;
   prm.ntok = ntok;
+  prm.causal = a.non_causal ? 0 : 1;
+  prm.lse = a.lse;
   {
     int lg = 0;
     while ((1 << lg) < gq) ++lg;

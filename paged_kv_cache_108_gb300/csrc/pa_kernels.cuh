@@ -59,6 +59,8 @@ struct TcLaunch {
   int num_seqs, num_heads, num_kv_heads, max_blocks, num_blocks, block_size;
   int num_ctas;     // persistent CTAs (one per SM)
   int tokens_per_seq;  // new tokens per sequence (1: decode); q/out hold S * this rows
+  bool non_causal;     // all of a sequence's rows see all its keys (shared-prefix pass)
+  float* lse;          // optional per-row log2-sum-exp output
   float scale;
   bool early_meta;  // the previous kernel only wrote the cache (see decode_tc.cu)
 };
@@ -76,6 +78,13 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value,
                                      int num_tokens, const float* k_scale,
                                      const float* v_scale,
                                      cudaStream_t stream);
+
+cudaError_t launch_cascade_meta(const int32_t* block_tables, int max_blocks, int block_size,
+                                const int32_t* context_lens, int num_seqs, int group,
+                                int32_t* ptables, int32_t* plens, int32_t* stables,
+                                int32_t* slens, cudaStream_t stream);
+cudaError_t launch_lse_merge(const void* o1, const float* l1, const void* o2, const float* l2,
+                             void* out, int64_t rows, int head_dim, cudaStream_t stream);
 
 cudaError_t launch_varlen_meta(const int32_t* block_tables, int max_blocks, int block_size,
                                const int32_t* seq_lens, const int32_t* query_start_loc,

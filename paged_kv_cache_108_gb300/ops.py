@@ -203,6 +203,38 @@ def decode_multi(out, q, k_cache, v_cache, block_tables, context_lens, tokens_pe
     return out
 
 
+def decode_shared_prefix_workspace_size(num_seqs, group_size, num_heads, head_dim,
+                                        max_blocks_per_seq, block_size) -> int:
+    return int(_lib.lib().pa_decode_shared_prefix_workspace_size(
+        num_seqs, group_size, num_heads, head_dim, max_blocks_per_seq, block_size))
+
+
+def decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens, group_size,
+                         scale, k_scale=None, v_scale=None, workspace=None, stream=None):
+    """``decode`` for consecutive groups of ``group_size`` sequences forked
+    from a common prefix: the shared blocks are read once per group."""
+    _same_cache(k_cache, v_cache)
+    desc = cache_desc(k_cache)
+    ks, vs = _scales(desc, k_scale, v_scale)
+    if q.dim() != 3 or out.shape != q.shape:
+        raise ValueError("q and out must both be [num_seqs, num_heads, head_dim]")
+    num_seqs, num_heads, head_dim = q.shape
+    max_blocks = int(block_tables.shape[1])
+    if workspace is None:
+        n = max(decode_shared_prefix_workspace_size(num_seqs, group_size, num_heads, head_dim,
+                                                    max_blocks, desc.block_size),
+                decode_workspace_size(num_seqs, num_heads, head_dim, max_blocks,
+                                      desc.block_size))
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    _lib.check(_lib.lib().pa_decode_shared_prefix(
+        _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), desc, _dev(block_tables, "block_tables", torch.int32),
+        max_blocks, _dev(context_lens, "context_lens", torch.int32), num_seqs, int(group_size),
+        num_heads, ctypes.c_float(scale), ks, vs, _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
 def swap_blocks(dst_k, dst_v, src_k, src_v, block_pairs, stream=None) -> None:
     """dst[d] = src[s] for each (s, d) row of ``block_pairs`` [n, 2] int32,
     between two caches of the same block shape (device pool <-> pinned host

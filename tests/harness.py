@@ -191,7 +191,7 @@ def serving_unique_tokens(mix):
     return mix.num_groups * mix.prefix_len + int(np.sum(n - 1 - mix.prefix_len))
 
 
-def serving_product(mix, data, num_blocks, device="cuda", kernel=0):
+def serving_product(mix, data, num_blocks, device="cuda", kernel=0, shared_prefix_group=0):
     """Product path: native pool and tables, cache writes, copy-on-write copies
     and decode on the GPU.  The prefix is written before the copies (it was
     computed before the fork); the suffix and the new token after them."""
@@ -231,7 +231,11 @@ def serving_product(mix, data, num_blocks, device="cuda", kernel=0):
     ws.random_(0, 256)
     ws[:4] = 0
     out = torch.empty_like(q)
-    ops.decode(out, q, kc, vc, bt_d, cl, mix.head_dim ** -0.5, workspace=ws, kernel=kernel)
+    if shared_prefix_group:
+        ops.decode_shared_prefix(out, q, kc, vc, bt_d, cl, shared_prefix_group,
+                                 mix.head_dim ** -0.5)
+    else:
+        ops.decode(out, q, kc, vc, bt_d, cl, mix.head_dim ** -0.5, workspace=ws, kernel=kernel)
     torch.cuda.synchronize()
     return {"tables": bt, "pairs": pr, "slots": (s_pre, s_suf, s_new),
             "k_cache": bits_from_dev(kc), "v_cache": bits_from_dev(vc),
