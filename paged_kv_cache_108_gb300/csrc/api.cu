@@ -183,9 +183,11 @@ size_t pa_decode_workspace_size_ex(int32_t num_seqs, int32_t num_heads, int32_t 
     return 0;
   const int64_t max_ctx = (int64_t)max_blocks_per_seq * block_size;
   size_t need = workspace_layout(num_seqs, num_heads, head_dim, max_ctx, ps).total;
-  if (head_dim == 128) {  // the tensor-core kernel may serve this shape
+  if (head_dim == 128) {  // the tensor-core kernels may serve this shape
     const size_t tc = pa::tc_workspace_bytes(num_seqs, num_heads, max_ctx, num_sms());
     if (tc > need) need = tc;
+    const size_t hp = pa::hp_workspace_bytes(num_seqs, num_heads, num_sms());
+    if (hp > need) need = hp;
   }
   return need;
 }
@@ -237,12 +239,60 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
   if (max_ctx > INT32_MAX / 2)
     return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: max_blocks_per_seq * block_size too large");
   const int kernel = opts ? opts->kernel : 0;
-  if (kernel != 0 && kernel != 1 && kernel != 2) {
+  if (kernel < 0 || kernel > 3) {
     snprintf(buf, sizeof buf, "pa_decode: kernel %d not available in this build", kernel);
     return pa_fail(PA_ERR_UNSUPPORTED, buf);
   }
 
   const bool fp8 = cache.dtype == PA_KV_FP8_E4M3;
+  const bool hp_fits = (kernel == 0 || kernel == 3) &&
+                       pa::hp_supported(cache.head_dim, group, fp8, num_seqs,
+                                        cache.num_kv_heads, cache.block_size, tokens_per_seq);
+  // Automatic choice: the head-packed kernel streams faster (bigger copies)
+  // but its units (sequence x 8 or 16 KV heads) are long, and a unit split
+  // over several CTAs ends in a merge at the CTA's tail.  Measured on GB300
+  // (GQA 4): 64 units (batch 64, ~1900 tokens) 94.5 vs 86.8 us; 256 units
+  // about equal; 512 units 2.5 % faster; 1000 short units 24 % faster.  For
+  // MHA the per-head kernel computes 16 columns for one head, so the
+  // head-packed one wins earlier (128 units: 3 % faster).
+  const int64_t hp_units =
+      hp_fits ? (int64_t)num_seqs * (cache.num_kv_heads / (group >= 2 ? 8 : 16)) : 0;
+  const bool hp_ok = hp_fits && (kernel == 3 || (group == 1 ? 2 * hp_units >= num_sms()
+                                                             : hp_units >= 2 * num_sms()));
+  if (kernel == 3 && !hp_ok)
+    return pa_fail(PA_ERR_UNSUPPORTED,
+                   "pa_decode: head-packed kernel needs a bf16 cache, head_dim 128, GQA group "
+                   "1, 2 or 4, num_kv_heads a multiple of 16 (group 1) or 8, block_size >= "
+                   "8 (group 1) or 16, at most 1024 sequences and one token per sequence");
+  if (hp_ok) {
+    const int nsm = num_sms();
+    const size_t need = pa::hp_workspace_bytes(num_seqs, num_heads, nsm);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) {
+      snprintf(buf, sizeof buf, "pa_decode: workspace of %zu bytes (256-byte aligned) needed",
+               need);
+      return pa_fail(PA_ERR_INVALID, buf);
+    }
+    pa::TcLaunch a{};
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.workspace = workspace;
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = cache.num_kv_heads;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = cache.num_blocks;
+    a.block_size = cache.block_size;
+    a.num_ctas = nsm;
+    a.tokens_per_seq = 1;
+    a.lse = lse;
+    a.scale = scale;
+    a.early_meta = prev_writes_cache_only;
+    return cuda_status(pa::launch_decode_hp(a, reinterpret_cast<cudaStream_t>(stream)), fn);
+  }
   const bool tc_ok = kernel != 1 && pa::tc_supported(cache.head_dim, group, fp8, num_seqs,
                                                       cache.block_size, tokens_per_seq);
   if (tokens_per_seq > 1 && !tc_ok)  // the SIMT kernel serves one token per sequence

@@ -1,0 +1,937 @@
+// Paged decode attention on the tensor cores with the KV heads of a cache
+// block packed into one tile ("head-packed"), for a bf16 cache with
+// head_dim 128.
+//
+// Same mathematics as the other decode kernels ("4.6 PagedAttention &
+// KV-Cache Memory Management", section "The PagedAttention Kernel":
+// block-table gather, GQA head map h -> h / G, online softmax; section
+// "Performance considerations": split long work across CTAs and merge).
+//
+// Why packed heads.  In the cache layout [blocks, block_size, H_kv, d] the
+// rows of HB consecutive KV heads for TT consecutive tokens of one block form
+// one 3-D box, so a single TMA copy {64 of d, TT tokens, HB heads} moves
+// 16 KiB where a per-head tile needs eight 2 KiB copies.  Measured on GB300
+// with a streaming probe (one CTA per SM, no compute): 16 KiB boxes stream at
+// 7.6 TB/s marginal, as fast as plain 32 KiB bulk copies, against 7.0 TB/s
+// for 2 KiB boxes.
+//
+// Tile.  The 128 rows of a K or V tile are (head, token) pairs, head-major:
+// row r = hh * TT + tt (the tensor map lists tokens before heads, so the TMA
+// writes this order).  The MMA columns are the N = HB x G query heads that
+// read those KV heads, column c = hh * G + i.  S = K q^T is computed for all
+// rows and columns; column c keeps only the rows of its own KV head (the
+// other products are discarded, the tensor pipe being nearly idle in
+// decode), and P is block-diagonal, so O = V^T P^T adds only matching rows.
+// A head's TT rows lie in one warp: its max and sum reduce with shuffles.
+//
+// Work split.  A unit is (sequence, group of HB KV heads); its KV is cut into
+// chunks of TT tokens, all chunks are numbered (group, sequence, chunk), and
+// each persistent CTA (one per SM) takes an equal contiguous range (the walk
+// of tc_sched.cuh).  A unit whose chunks fall in one CTA is finished there.
+// A piece of a split unit leaves an unnormalised partial (m, l, o) in a slot
+// of the CTA that computed it -- slot 0 for the unit its range ends in, slot
+// 1 for the unit it starts in -- and the last piece to arrive merges.  The
+// merge warp merges pieces finished while the CTA still has work; a CTA's
+// final piece is merged by its softmax warps, straight from registers when
+// every other piece has already arrived (the usual case: neighbours take
+// their shared units first).
+//
+// Warp roles (256 threads):
+//   warps 0-3  softmax + epilogue: thread t owns TMEM lane t (row t of the
+//              logits tile; element d = t of the output tile);
+//   warp 4     producer: per chunk one block id (a cp.async ring a few chunks
+//              ahead) and four TMA copies (K and V, two 64-column halves)
+//              into a 3-stage ring;
+//   warp 5     TMEM allocation; one thread issues the MMAs and the q tile's
+//              loads (one buffer, reloaded when a unit starts);
+//   warp 6     merge warp;
+//   warp 7     no role after the prologue.
+//
+// Every mbarrier wait gives up after ~2^31 clocks: the thread records an
+// error code in the workspace's first word and marks the CTA aborted, so the
+// kernel always terminates; copies in flight are drained (again with a
+// bound) before TMEM is freed.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pa_device.cuh"
+#include "pa_kernels.cuh"
+#include "tc_ptx.cuh"
+#include "tc_sched.cuh"
+
+namespace pa {
+namespace hp {
+
+using tc::ChunkWalk;
+using tc::Smem;
+using tc::arrive;
+using tc::cta_of;
+using tc::drain_bar;
+using tc::kWaitClocks;
+using tc::range_lo;
+using tc::wait_bar;
+
+constexpr int D = 128;
+constexpr int kMaxSeqs = 1024;
+constexpr int TAB_SLOTS = 4, TAB_AHEAD = 3;  // block-id ring: one id per chunk
+
+// G query heads per KV head (1, 2 or 4).
+template <int G>
+struct Cfg {
+  static constexpr int HB = G >= 2 ? 8 : 16;  // KV heads per tile
+  static constexpr int TT = 128 / HB;         // tokens per chunk
+  static constexpr int N = HB * G;            // MMA columns: the tile's query heads
+  static constexpr int NW = N / 4;            // columns of one softmax warp's heads
+  static constexpr int NST = 3;               // K/V ring stages (192 KiB)
+  static constexpr int TILE_B = 128 * D * 2;  // one K or V tile: 128 rows of 256 bytes
+  static constexpr int HALF_B = 128 * 128;    // one 64-column half of a tile
+  static constexpr int QTILE_B = N * D * 2;
+  static constexpr int QHALF_B = N * 128;
+  static constexpr int PTILE_B = N * 128 * 2;  // P^T: N rows of 128 bf16
+  static constexpr int PHALF_B = N * 128;
+  // TMEM: S[2] then O[2], N columns each
+  static constexpr int TMEM_COLS = 4 * N <= 64 ? 64 : 128;
+  static constexpr int NTHREADS = 256;
+
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + NST * TILE_B;
+  static constexpr int OFF_Q = OFF_V + NST * TILE_B;
+  static constexpr int OFF_P = OFF_Q + QTILE_B;
+  static constexpr int OFF_BAR = OFF_P + 2 * PTILE_B;
+  static constexpr int B_FULL_K = 0, B_FULL_V = NST, B_EMPTY = 2 * NST, B_S_FULL = 3 * NST,
+                       B_S_EMPTY = B_S_FULL + 2, B_P_FULL = B_S_EMPTY + 2,
+                       B_P_EMPTY = B_P_FULL + 2, B_O_FULL = B_P_EMPTY + 2,
+                       B_O_EMPTY = B_O_FULL + 2, B_Q_FULL = B_O_EMPTY + 2,
+                       B_Q_EMPTY = B_Q_FULL + 1, B_EPI = B_Q_EMPTY + 1, NBARS = B_EPI + 2;
+  static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
+  static constexpr int OFF_ABORT = OFF_TMEM + 4;
+  static constexpr int OFF_SQ = OFF_ABORT + 4;      // [3] ints: sequences of the range's ends, first
+  static constexpr int OFF_FLAG = OFF_SQ + 12;      // softmax warps' broadcast word
+  static constexpr int OFF_ALPHA = OFF_FLAG + 4;    // [3][N] floats: per-chunk rescale factors
+  static constexpr int OFF_ML = OFF_ALPHA + 3 * N * 4;  // [N] float2: a piece's (m, l)
+  static constexpr int OFF_CP = OFF_ML + N * 8;          // chunk prefix per sequence, [S+1]
+  static constexpr int OFF_NLEN = OFF_CP + (kMaxSeqs + 1) * 4;  // clamped context lengths
+  static constexpr int OFF_TAB = OFF_NLEN + kMaxSeqs * 4;       // block-id ring
+  static constexpr int SMEM_BYTES = OFF_TAB + TAB_SLOTS * 4 + 1024;  // + alignment slack
+  static_assert(N % 16 == 0 && N <= 32, "MMA N");
+  static_assert(TT <= 32, "a KV head's rows stay in one warp");
+  static_assert(OFF_BAR % 1024 == 0 && PHALF_B % 1024 == 0 && QHALF_B % 1024 == 0,
+                "swizzled tiles stay 1024-byte aligned");
+  static_assert(OFF_ALPHA % 16 == 0 && OFF_ML % 8 == 0, "alignment");
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
+
+struct Params {
+  void* out;                     // [S, H, D] bf16
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int* err;                      // workspace word 0: nonzero if a wait expired / bad id
+  unsigned long long* counters;  // [units] (epoch << 16) | arrivals of finished pieces
+  float2* ws_ml;                 // [num_ctas][2][N] (m, l) of a piece
+  float* ws_o;                   // [num_ctas][2][N][D] unnormalised o of a piece
+  float* lse;                    // optional [S * H]: log2-sum-exp of each output row
+  int num_seqs, num_heads, num_groups, max_blocks, num_blocks, block_size, log2_bs;
+  int num_ctas;
+  float scale_log2;
+  unsigned long long epoch;      // 48-bit tag of this call
+  int early_meta;                // previous kernel wrote only the cache
+};
+
+// Slot of CTA c's partial for the split unit whose last chunk is `last`:
+// 0 if the unit holds the CTA's last chunk, else 1 (the unit its range starts in).
+__device__ __forceinline__ int piece_slot(int c, long long last, long long K, int C) {
+  return range_lo(c + 1, K, C) - 1 <= last ? 0 : 1;
+}
+
+// One piece (m, l, o) folded into a running merge (M, L, a).  Both merge
+// paths (merge warp, softmax warps) use exactly these roundings, so a unit's
+// output does not depend on which CTA merges it.  A piece may hold no
+// visible key for a column (m = -inf).
+__device__ __forceinline__ void merge_weights(float& M, float m, float& rs, float& w) {
+  const float mn = fmaxf(M, m);
+  const float msafe = mn == -INFINITY ? 0.f : mn;
+  rs = fast_exp2(M - msafe);  // 0 for the first piece
+  w = fast_exp2(m - msafe);
+  M = mn;
+}
+__device__ __forceinline__ float merge_fold(float a, float rs, float w, float o) {
+  return __fmaf_rn(a, rs, __fmul_rn(w, o));
+}
+__device__ __forceinline__ void merge_step(float& M, float& L, float& a, float2 ml, float o) {
+  float rs, w;
+  merge_weights(M, ml.x, rs, w);
+  L = merge_fold(L, rs, w, ml.y);
+  a = merge_fold(a, rs, w, o);
+}
+__device__ __forceinline__ void merge_step4(float& M, float& L, float4& a, float2 ml, float4 o) {
+  float rs, w;
+  merge_weights(M, ml.x, rs, w);
+  L = merge_fold(L, rs, w, ml.y);
+  a.x = merge_fold(a.x, rs, w, o.x);
+  a.y = merge_fold(a.y, rs, w, o.y);
+  a.z = merge_fold(a.z, rs, w, o.z);
+  a.w = merge_fold(a.w, rs, w, o.w);
+}
+
+template <int G>
+__global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
+    decode_hp_kernel(const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_q, const Params p) {
+  using Cf = Cfg<G>;
+  constexpr int HB = Cf::HB, TT = Cf::TT, N = Cf::N, NW = Cf::NW, NST = Cf::NST;
+  constexpr int TILE_B = Cf::TILE_B, HALF_B = Cf::HALF_B, QTILE_B = Cf::QTILE_B,
+                QHALF_B = Cf::QHALF_B, PTILE_B = Cf::PTILE_B, PHALF_B = Cf::PHALF_B,
+                TMEM_COLS = Cf::TMEM_COLS, NTHREADS = Cf::NTHREADS;
+  constexpr int OFF_K = Cf::OFF_K, OFF_V = Cf::OFF_V, OFF_Q = Cf::OFF_Q, OFF_P = Cf::OFF_P,
+                OFF_TMEM = Cf::OFF_TMEM, OFF_SQ = Cf::OFF_SQ, OFF_FLAG = Cf::OFF_FLAG,
+                OFF_ALPHA = Cf::OFF_ALPHA, OFF_ML = Cf::OFF_ML, OFF_CP = Cf::OFF_CP,
+                OFF_NLEN = Cf::OFF_NLEN, OFF_TAB = Cf::OFF_TAB;
+  constexpr int B_FULL_K = Cf::B_FULL_K, B_FULL_V = Cf::B_FULL_V, B_EMPTY = Cf::B_EMPTY,
+                B_S_FULL = Cf::B_S_FULL, B_S_EMPTY = Cf::B_S_EMPTY, B_P_FULL = Cf::B_P_FULL,
+                B_P_EMPTY = Cf::B_P_EMPTY, B_O_FULL = Cf::B_O_FULL, B_O_EMPTY = Cf::B_O_EMPTY,
+                B_Q_FULL = Cf::B_Q_FULL, B_Q_EMPTY = Cf::B_Q_EMPTY, B_EPI = Cf::B_EPI,
+                NBARS = Cf::NBARS;
+  using Walk = ChunkWalk<TT>;
+  extern __shared__ unsigned char smem_raw[];
+  Smem sm;
+  {
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t aligned = (raw + 1023u) & ~1023u;
+    sm.base = smem_raw + (aligned - raw);
+    sm.base_u32 = aligned;
+    sm.off_bar = Cf::OFF_BAR;
+    sm.off_abort = Cf::OFF_ABORT;
+  }
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int S = p.num_seqs, H = p.num_heads, HG = p.num_groups;
+  const int cap = p.max_blocks << p.log2_bs;
+  int* cp = reinterpret_cast<int*>(sm.base + OFF_CP);
+  int* nl = reinterpret_cast<int*>(sm.base + OFF_NLEN);
+
+  // ---------------- prologue ----------------
+  // Inputs may come from the previous kernel in the stream.  When that kernel
+  // is known to write only the KV cache, only the producer waits, right
+  // before its first cache load; lengths, tables and q are read at once.
+  if (!p.early_meta) ptx::grid_dependency_wait();
+  const int n_own = tid < S ? min(__ldg(&p.context_lens[tid]), cap) : 0;
+  if (warp == 5) {
+    ptx::tmem_alloc(sm.base_u32 + OFF_TMEM, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < NBARS; ++i) {
+      uint32_t cnt = 1;
+      if ((i >= B_S_EMPTY && i < B_S_EMPTY + 2) || (i >= B_P_FULL && i < B_P_FULL + 2) ||
+          (i >= B_O_EMPTY && i < B_O_EMPTY + 2) || (i >= B_EPI && i < B_EPI + 2))
+        cnt = 128;
+      ptx::mbar_init(sm.bar(i), cnt);
+    }
+    *sm.abort_flag() = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 4 && lane == 0) {
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+  }
+  if (warp == 5 && lane == 0) ptx::prefetch_tmap(&tm_q);
+  if (warp < 4) {
+    // zero both P tiles once: a thread only ever writes its own KV head's
+    // columns of its own row, so the off-diagonal blocks stay zero
+    uint4* pz = reinterpret_cast<uint4*>(sm.base + OFF_P);
+    for (int i = tid; i < 2 * PTILE_B / 16; i += 128) pz[i] = make_uint4(0, 0, 0, 0);
+    ptx::fence_proxy_async_smem();
+  }
+  for (int i = tid; i < S; i += NTHREADS) {
+    const int n = i == tid ? n_own : min(__ldg(&p.context_lens[i]), cap);
+    nl[i] = n;
+    cp[i] = n > 0 ? (n + TT - 1) / TT : 0;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive prefix in place: cp[i] = sum_{i' < i} ceil(n_i' / TT)
+    int carry = 0;
+    for (int base = 0; base < S; base += 32) {
+      const int i = base + lane;
+      const int v = i < S ? cp[i] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (i < S) cp[i] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) cp[S] = carry;
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm.base + OFF_TMEM);
+  const long long Ctot = cp[S];  // chunks of one head group
+  const long long Ktot = Ctot * HG;
+  const int C = (int)(Ktot < p.num_ctas ? Ktot : p.num_ctas);
+  const long long lo = (int)blockIdx.x < C ? range_lo(blockIdx.x, Ktot, C) : 0;
+  const long long hi = (int)blockIdx.x < C ? range_lo(blockIdx.x + 1, Ktot, C) : 0;
+  int* sq = reinterpret_cast<int*>(sm.base + OFF_SQ);
+  if (lo < hi) {
+    const long long r_lo = lo % Ctot, r_hi = (hi - 1) % Ctot;
+    for (int i = tid; i < S; i += NTHREADS) {
+      const int a = cp[i], b = cp[i + 1];
+      if (a <= r_lo && r_lo < b) sq[0] = i;
+      if (a <= r_hi && r_hi < b) sq[1] = i;
+      if (a == 0 && b > 0) sq[2] = i;
+    }
+  }
+  __syncthreads();
+  const int seq_lo = lo < hi ? sq[0] : 0, seq_hi = lo < hi ? sq[1] : 0;
+  const int first_ne = lo < hi ? sq[2] : 0;
+  if (warp < 4) {
+    // empty sequences get zero rows (spread over the CTAs)
+    for (int i = blockIdx.x; i < S; i += gridDim.x) {
+      if (nl[i] <= 0) {
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + (int64_t)i * H * D;
+        for (int e = tid; e < H * D; e += 128) o[e] = __float2bfloat16_rn(0.f);
+        if (p.lse)
+          for (int r = tid; r < H; r += 128) p.lse[(int64_t)i * H + r] = -INFINITY;
+      }
+    }
+  }
+
+  Walk walk;
+  walk.cp = cp;
+  walk.S = S;
+  walk.Hkv = HG;
+  walk.nl = nl;
+  walk.Ctot = Ctot;
+  walk.first_ne = first_ne;
+
+  if (warp == 4) {
+    // ================= producer =================
+    const uint32_t tab = sm.base_u32 + OFF_TAB;
+    const int* tab_s = reinterpret_cast<const int*>(sm.base + OFF_TAB);
+    // lane 0 copies the block id of a chunk TAB_AHEAD chunks ahead
+    auto fetch_id = [&](const Walk& w, int slot) {
+      if (lane == 0)
+        cp_async_4(tab + slot * 4, p.block_tables + (int64_t)w.seq * p.max_blocks +
+                                       ((w.j * TT) >> p.log2_bs));
+    };
+    walk.init(lo, hi, seq_lo, seq_hi);
+    Walk ahead = walk;
+#pragma unroll 1  // one copy of cold code: its first run pays instruction-fetch misses
+    for (int d = 0; d < TAB_AHEAD; ++d) {
+      if (!ahead.done()) {
+        fetch_id(ahead, d);
+        ahead.next();
+      }
+      cp_async_commit();
+    }
+    int local = 0;
+    for (; !walk.done(); walk.next(), ++local) {
+      const int s = local % NST;
+      const uint32_t ph = (local / NST) & 1;
+      cp_async_wait<TAB_AHEAD - 1>();  // this chunk's id has landed (lane 0's copy)
+      int phys = lane == 0 ? tab_s[local % TAB_SLOTS] : 0;
+      phys = __shfl_sync(0xffffffffu, phys, 0);
+      if (!wait_bar(sm, sm.bar(B_EMPTY + s), ph ^ 1, p.err, 1)) break;
+      if (p.early_meta && local == 0) ptx::grid_dependency_wait();
+      if ((unsigned)phys >= (unsigned)p.num_blocks) {
+        if (lane == 0) atomicExch(p.err, 3);  // bad block id: load block 0 instead of faulting
+        phys = 0;
+      }
+      const int tok = (walk.j * TT) & (p.block_size - 1);
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_K + s), (uint32_t)TILE_B);
+        ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_V + s), (uint32_t)TILE_B);
+      }
+      __syncwarp();
+      if (lane < 4) {
+        // lanes 0, 1: K halves; lanes 2, 3: V halves.  Box {64 of d, TT
+        // tokens, HB heads} at (d, token in block, first head, block).
+        const bool isk = lane < 2;
+        const int hf = lane & 1;
+        const uint32_t dst = sm.base_u32 + (isk ? OFF_K : OFF_V) + s * TILE_B + hf * HALF_B;
+        ptx::tma_load_4d(dst, isk ? (const void*)&tm_k : (const void*)&tm_v,
+                         sm.bar((isk ? B_FULL_K : B_FULL_V) + s), hf * 64, tok, walk.g * HB, phys);
+      }
+      if (!ahead.done()) {
+        fetch_id(ahead, (local + TAB_AHEAD) % TAB_SLOTS);
+        ahead.next();
+      }
+      cp_async_commit();
+    }
+    cp_async_wait<0>();
+    // drain: the last loads issued must land before the CTA can exit
+    __syncwarp();
+    if (lane == 0) {
+      for (int l = max(0, local - NST); l < local; ++l) {
+        drain_bar(sm.bar(B_FULL_K + l % NST), (l / NST) & 1);
+        drain_bar(sm.bar(B_FULL_V + l % NST), (l / NST) & 1);
+      }
+    }
+  } else if (warp == 5) {
+    // ================= MMA issuer (and the q tile) =================
+    // Two cursors as in the per-head kernel: the logits MMA of chunk nq and
+    // the PV MMA of chunk npv < nq, each issued as soon as its inputs are
+    // ready.  The q tile has one buffer: when a segment (a unit's piece)
+    // starts, its load is issued once the previous segment's last logits
+    // MMA has completed, and that segment's first logits MMA waits for it.
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(128, N, false);
+      constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, N, true);
+      const uint32_t qbase = sm.base_u32 + OFF_Q;
+      walk.init(lo, hi, seq_lo, seq_hi);
+      int nq = 0, npv = 0, seg = 0;
+      bool q_loading = false, q_ready = false;
+      long long t_idle = clock64();
+      while (true) {
+        bool progress = false;
+        if (!walk.done()) {
+          const bool first = walk.first_of_segment();
+          if (first && !q_ready) {
+            if (!q_loading) {
+              if (seg == 0 || ptx::mbar_test_wait(sm.bar(B_Q_EMPTY), (seg - 1) & 1)) {
+                // the unit's query heads g*N .. g*N+N-1: rows of q as [S*H, d]
+                const int row = walk.seq * H + walk.g * N;
+                ptx::mbar_arrive_expect_tx(sm.bar(B_Q_FULL), (uint32_t)QTILE_B);
+                ptx::tma_load_2d(qbase, &tm_q, sm.bar(B_Q_FULL), 0, row);
+                ptx::tma_load_2d(qbase + QHALF_B, &tm_q, sm.bar(B_Q_FULL), 64, row);
+                q_loading = true;
+                progress = true;
+              }
+            } else if (ptx::mbar_test_wait(sm.bar(B_Q_FULL), seg & 1)) {
+              q_loading = false;
+              q_ready = true;
+              progress = true;
+            }
+          }
+          const int s = nq % NST;
+          const int b = nq & 1;
+          if ((!first || q_ready) && ptx::mbar_test_wait(sm.bar(B_FULL_K + s), (nq / NST) & 1) &&
+              ptx::mbar_test_wait(sm.bar(B_S_EMPTY + b), ((nq >> 1) & 1) ^ 1)) {
+            ptx::tc_fence_after();
+            const uint32_t kbase = sm.base_u32 + OFF_K + s * TILE_B;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t da =
+                  ptx::smem_desc_sw128(kbase + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
+              const uint64_t db =
+                  ptx::smem_desc_sw128(qbase + (kk >> 2) * QHALF_B + (kk & 3) * 32, 16, 1024);
+              ptx::tc_mma_f16(tmem + N * b, da, db, IDESC_QK, kk > 0);
+            }
+            ptx::tc_commit(sm.bar(B_S_FULL + b));
+            if (walk.last_of_segment()) {
+              ptx::tc_commit(sm.bar(B_Q_EMPTY));
+              ++seg;
+              q_ready = false;
+            }
+            walk.next();
+            ++nq;
+            progress = true;
+          }
+        }
+        if (npv < nq) {
+          const int s = npv % NST;
+          const int b = npv & 1;
+          const uint32_t bph = (npv >> 1) & 1;
+          if (ptx::mbar_test_wait(sm.bar(B_P_FULL + b), bph) &&
+              ptx::mbar_test_wait(sm.bar(B_O_EMPTY + b), bph ^ 1) &&
+              ptx::mbar_test_wait(sm.bar(B_FULL_V + s), (npv / NST) & 1)) {
+            ptx::tc_fence_after();
+            const uint32_t vbase = sm.base_u32 + OFF_V + s * TILE_B;
+            const uint32_t pbase = sm.base_u32 + OFF_P + b * PTILE_B;
+            // A = V^T read MN-major from the TMA layout (16 rows per MMA);
+            // B = P^T, K-major, 64 rows per 128-byte swizzled half
+#pragma unroll
+            for (int kk = 0; kk < 128 / 16; ++kk) {
+              const uint64_t da = ptx::smem_desc_sw128(vbase + kk * 2048, HALF_B, 1024);
+              const uint64_t db =
+                  ptx::smem_desc_sw128(pbase + (kk >> 2) * PHALF_B + (kk & 3) * 32, 16, 1024);
+              ptx::tc_mma_f16(tmem + 2 * N + N * b, da, db, IDESC_PV, kk > 0);
+            }
+            ptx::tc_commit(sm.bar(B_O_FULL + b));
+            ptx::tc_commit(sm.bar(B_P_EMPTY + b));
+            ptx::tc_commit(sm.bar(B_EMPTY + s));
+            ++npv;
+            progress = true;
+          }
+        } else if (walk.done()) {
+          break;
+        }
+        if (progress) {
+          t_idle = clock64();
+        } else {
+          if (*sm.abort_flag()) break;
+          if (clock64() - t_idle > kWaitClocks) {
+            *sm.abort_flag() = 1;
+            atomicExch(p.err, 8);
+            break;
+          }
+        }
+      }
+      // drain: every copy and commit this thread issued must land before exit
+      if (q_loading) drain_bar(sm.bar(B_Q_FULL), seg & 1);
+      if (seg > 0) drain_bar(sm.bar(B_Q_EMPTY), (seg - 1) & 1);
+      if (nq > 0) drain_bar(sm.bar(B_S_FULL + ((nq - 1) & 1)), ((nq - 1) >> 1) & 1);
+      if (npv > 0) {
+        const int L = npv - 1;
+        drain_bar(sm.bar(B_EMPTY + L % NST), (L / NST) & 1);
+        drain_bar(sm.bar(B_P_EMPTY + (L & 1)), (L >> 1) & 1);
+        drain_bar(sm.bar(B_O_FULL + (L & 1)), (L >> 1) & 1);
+      }
+    }
+  } else if (warp == 6) {
+    // ================= merge warp =================
+    // Follows the same walk; for each split piece other than the CTA's final
+    // one it waits for the softmax warps' partial, counts the arrival, and if
+    // this was the unit's last piece merges all pieces into the output.
+    // Lane l holds d = 4l .. 4l+3 of 8 columns at a time.
+    walk.init(lo, hi, seq_lo, seq_hi);
+    int e = 0;
+    for (; !walk.done(); walk.next()) {
+      if (!walk.last_of_segment()) continue;
+      {
+        Walk nx = walk;
+        nx.next();
+        if (nx.done()) break;  // the final piece: merged by the softmax warps
+      }
+      const long long first = walk.k - walk.j;
+      const long long last = first + walk.nch - 1;
+      const int c0 = cta_of(first, Ktot, C);
+      const int c1 = cta_of(last, Ktot, C);
+      if (c0 == c1) continue;  // whole unit: the softmax warps wrote the output
+      const bool good = wait_bar(sm, sm.bar(B_EPI + (e++ & 1)), 0, p.err, 14);
+      if (!good) continue;
+      __threadfence();  // the partial written by this CTA is visible before the count
+      const int u = walk.seq * HG + walk.g;
+      int lst = 0;
+      if (lane == 0) lst = (arrive(&p.counters[u], p.epoch) == c1 - c0 + 1);
+      lst = __shfl_sync(0xffffffffu, lst, 0);
+      if (!lst) continue;
+      __threadfence();  // see every other piece's partial
+      const int64_t row0 = (int64_t)walk.seq * H + (int64_t)walk.g * N;
+#pragma unroll 1
+      for (int cb = 0; cb < N; cb += 8) {
+        float M[8], Ls[8];
+        float4 a[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          M[k] = -INFINITY;
+          Ls[k] = 0.f;
+          a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll 2
+        for (int cc = c0; cc <= c1; ++cc) {
+          const int64_t base = ((int64_t)cc * 2 + piece_slot(cc, last, Ktot, C)) * N + cb;
+          float2 ml[8];
+          float4 ov[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            ml[k] = __ldcg(&p.ws_ml[base + k]);
+            ov[k] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (base + k) * D) + lane);
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) merge_step4(M[k], Ls[k], a[k], ml[k], ov[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          __nv_bfloat162 lo2 = __floats2bfloat162_rn(a[k].x / Ls[k], a[k].y / Ls[k]);
+          __nv_bfloat162 hi2 = __floats2bfloat162_rn(a[k].z / Ls[k], a[k].w / Ls[k]);
+          uint2 w2;
+          w2.x = *reinterpret_cast<uint32_t*>(&lo2);
+          w2.y = *reinterpret_cast<uint32_t*>(&hi2);
+          *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                    (row0 + cb + k) * D + 4 * lane) = w2;
+          if (p.lse && lane == k) p.lse[row0 + cb + k] = M[k] + __log2f(Ls[k]);
+        }
+      }
+      if (lane == 0) p.counters[u] = p.epoch << 16;  // count 0: a replay starts afresh
+    }
+  } else if (warp < 4) {
+    // ================= softmax + epilogue (warps 0-3) =================
+    const int t = tid;           // TMEM lane: row (hh, tt) of S; element d of O
+    const int hh = t / TT;       // the row's KV head within the tile
+    const int tt = t % TT;       // the row's token within the chunk
+    const int sel = lane / TT;   // which of this warp's heads
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float* abuf = reinterpret_cast<float*>(sm.base + OFF_ALPHA);
+    float2* mlb = reinterpret_cast<float2*>(sm.base + OFF_ML);
+    volatile int* flag = reinterpret_cast<volatile int*>(sm.base + OFF_FLAG);
+    // running max per column (the same in all TT lanes of a head) and this
+    // row's share of the column sums; dm, dl: those of a just-finished piece
+    float m[G], l[G], dm[G], dl[G];
+    float acc[N];  // o[column][d = t]
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      m[i] = -INFINITY;
+      l[i] = 0.f;
+      dm[i] = -INFINITY;
+      dl[i] = 0.f;
+    }
+#pragma unroll
+    for (int c = 0; c < N; ++c) acc[c] = 0.f;
+    struct Info {
+      int seq, g, nch, j;
+      long long k;
+      bool last;
+    } prev{0, 0, 0, 0, 0, false};
+    int split_epi = 0;  // partials handed to the merge warp
+
+    // A piece of unit `in` is done: its (m, l) per column, then the output
+    // (whole unit), a partial for the merge warp, or -- the CTA's final
+    // piece of a split unit -- the merge itself.
+    auto epilogue = [&](const Info& in, const float* ms, const float* ls, bool final_piece) {
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        float v = ls[i];
+#pragma unroll
+        for (int off = TT / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (tt == 0) mlb[hh * G + i] = make_float2(ms[i], v);
+      }
+      ptx::bar_sync_named(2, 128);
+      float M[N], L[N];
+#pragma unroll
+      for (int c = 0; c < N; ++c) {
+        const float2 v = mlb[c];
+        M[c] = v.x;
+        L[c] = v.y;
+      }
+      const float2 own_ml = mlb[t < N ? t : 0];
+      ptx::bar_sync_named(2, 128);  // all have read mlb before it is rewritten
+      const long long first = in.k - in.j;
+      const long long last = first + in.nch - 1;
+      const int c0 = cta_of(first, Ktot, C);
+      const int c1 = cta_of(last, Ktot, C);
+      const int64_t row0 = (int64_t)in.seq * H + (int64_t)in.g * N;
+      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + t;
+      if (c0 == c1) {
+#pragma unroll
+        for (int c = 0; c < N; ++c) o[(row0 + c) * D] = __float2bfloat16_rn(acc[c] / L[c]);
+        if (p.lse && t < N) p.lse[row0 + t] = own_ml.x + __log2f(own_ml.y);
+        return;
+      }
+      const int u = in.seq * HG + in.g;
+      const int nseg = c1 - c0 + 1;
+      const int64_t mine = ((int64_t)blockIdx.x * 2 + piece_slot(blockIdx.x, last, Ktot, C)) * N;
+      auto write_partial = [&]() {
+#pragma unroll
+        for (int c = 0; c < N; ++c) p.ws_o[(mine + c) * D + t] = acc[c];
+        if (t < N) p.ws_ml[mine + t] = own_ml;
+      };
+      write_partial();
+      if (!final_piece) {
+        ptx::mbar_arrive(sm.bar(B_EPI + (split_epi++ & 1)));
+        return;
+      }
+      // The CTA's final piece.  If every other piece has already arrived this
+      // CTA merges without counting; else it counts like the others and
+      // merges only if it was last.  Either way the merge reads all pieces
+      // from the slots in CTA order with the merge warp's arithmetic, so the
+      // result does not depend on which CTA merges.
+      if (t == 0) {
+        const unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(&p.counters[u]);
+        *flag = ((v >> 16) == p.epoch && (int)(v & 0xFFFFull) == nseg - 1) ? 1 : 0;
+      }
+      __threadfence();
+      ptx::bar_sync_named(2, 128);  // own partial complete; flag visible
+      const bool fast = *flag != 0;
+      ptx::bar_sync_named(2, 128);
+      if (!fast) {
+        if (t == 0) *flag = (arrive(&p.counters[u], p.epoch) == nseg) ? 1 : 0;
+        ptx::bar_sync_named(2, 128);
+        if (*flag == 0) return;
+      }
+      __threadfence();  // see every other piece's partial
+#pragma unroll
+      for (int c = 0; c < N; ++c) {
+        M[c] = -INFINITY;
+        L[c] = 0.f;
+        acc[c] = 0.f;
+      }
+#pragma unroll 1
+      for (int cc = c0; cc <= c1; ++cc) {
+        const int64_t base = ((int64_t)cc * 2 + piece_slot(cc, last, Ktot, C)) * N;
+        float2 ml[N];
+        float ov[N];
+#pragma unroll
+        for (int c = 0; c < N; ++c) {
+          ml[c] = __ldcg(&p.ws_ml[base + c]);
+          ov[c] = __ldcg(&p.ws_o[(base + c) * D + t]);
+        }
+#pragma unroll
+        for (int c = 0; c < N; ++c) merge_step(M[c], L[c], acc[c], ml[c], ov[c]);
+      }
+#pragma unroll
+      for (int c = 0; c < N; ++c) {
+        o[(row0 + c) * D] = __float2bfloat16_rn(acc[c] / L[c]);
+        if (p.lse && t == c) p.lse[row0 + c] = M[c] + __log2f(L[c]);
+      }
+      if (t == 0) p.counters[u] = p.epoch << 16;  // count 0: a replay starts afresh
+    };
+
+    // fold chunk L's PV result into acc with that chunk's rescale factors
+    auto acc_o = [&](int L, const Info& in, bool use_done, bool final_piece) {
+      const int b = L & 1;
+      const uint32_t bph = (L >> 1) & 1;
+      float ov[N];
+      const bool good = wait_bar(sm, sm.bar(B_O_FULL + b), bph, p.err, 10);
+      ptx::tc_fence_after();
+      if constexpr (N == 32) {
+        ptx::tmem_ld_x32(tmem + lane_base + 2 * N + N * b, ov);
+      } else {
+        ptx::tmem_ld_x16(tmem + lane_base + 2 * N + N * b, ov);
+      }
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(sm.bar(B_O_EMPTY + b));
+      const float* al = abuf + (L % 3) * N;
+#pragma unroll
+      for (int c = 0; c < N; ++c) acc[c] = acc[c] * al[c] + (good ? ov[c] : 0.f);
+      if (in.last) {
+        if (use_done) epilogue(in, dm, dl, final_piece);
+        else epilogue(in, m, l, final_piece);
+#pragma unroll
+        for (int c = 0; c < N; ++c) acc[c] = 0.f;
+      }
+    };
+
+    walk.init(lo, hi, seq_lo, seq_hi);
+    int local = 0;
+    for (; !walk.done(); walk.next(), ++local) {
+      const int s = local % NST;
+      const uint32_t ph = (local / NST) & 1;
+      const int b = local & 1;
+      const uint32_t bph = (local >> 1) & 1;
+      // ---- logits of this chunk: this warp's heads' columns ----
+      float sl[NW];
+      bool good = wait_bar(sm, sm.bar(B_S_FULL + b), bph, p.err, 11);
+      ptx::tc_fence_after();
+      if constexpr (NW == 8) {
+        ptx::tmem_ld_x8(tmem + lane_base + N * b + warp * NW, sl);
+      } else {
+        ptx::tmem_ld_x4(tmem + lane_base + N * b + warp * NW, sl);
+      }
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(sm.bar(B_S_EMPTY + b));
+      const int valid = walk.valid();
+      float x[G];
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        float v = sl[i];
+#pragma unroll
+        for (int k = 1; k < 32 / TT; ++k)
+          if (sel == k) v = sl[k * G + i];
+        x[i] = (good && tt < valid) ? v * p.scale_log2 : -INFINITY;
+      }
+      // ---- chunk max per column over its head's TT rows ----
+      float cm[G];
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        cm[i] = x[i];
+#pragma unroll
+        for (int off = TT / 2; off > 0; off >>= 1)
+          cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], off));
+      }
+      if (walk.first_of_segment()) {
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          dm[i] = m[i];
+          dl[i] = l[i];
+          m[i] = -INFINITY;
+          l[i] = 0.f;
+        }
+      }
+      float alpha[G];
+      __nv_bfloat16 pb[G];
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        const float m_new = fmaxf(m[i], cm[i]);
+        const float msafe = m_new == -INFINITY ? 0.f : m_new;
+        alpha[i] = fast_exp2(m[i] - msafe);
+        m[i] = m_new;
+        pb[i] = __float2bfloat16_rn(fast_exp2(x[i] - msafe));  // 0 for masked rows
+        l[i] = l[i] * alpha[i] + __bfloat162float(pb[i]);
+      }
+      if (tt == 0) {
+#pragma unroll
+        for (int i = 0; i < G; ++i) abuf[(local % 3) * N + hh * G + i] = alpha[i];
+      }
+      // ---- P tile (and the V rows past the context end) ----
+      wait_bar(sm, sm.bar(B_P_EMPTY + b), bph ^ 1, p.err, 12);
+      if (valid < TT) {
+        wait_bar(sm, sm.bar(B_FULL_V + s), ph, p.err, 13);
+        if (tt >= valid) {
+          unsigned char* vrow = sm.base + OFF_V + s * TILE_B + t * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int cc = (c + t) & 7;
+            *reinterpret_cast<uint4*>(vrow + cc * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vrow + HALF_B + cc * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      {
+        // P^T[c][r]: row c of 128 bf16, 64 per 128-byte swizzled half
+        unsigned char* pt = sm.base + OFF_P + b * PTILE_B + (t >> 6) * PHALF_B;
+        const int chunk = (t & 63) >> 3;
+        const int byte = (t & 7) * 2;
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          const int c = hh * G + i;
+          *reinterpret_cast<__nv_bfloat16*>(pt + c * 128 + ((chunk ^ (c & 7)) << 4) + byte) = pb[i];
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(sm.bar(B_P_FULL + b));
+      ptx::bar_sync_named(1, 128);  // this chunk's rescale factors are visible
+      // ---- fold the previous chunk's PV result ----
+      if (local > 0) acc_o(local - 1, prev, walk.first_of_segment(), false);
+      prev = Info{walk.seq, walk.g, walk.nch, walk.j, walk.k, walk.last_of_segment()};
+    }
+    if (local > 0) acc_o(local - 1, prev, false, true);
+  }
+
+  // ---------------- teardown ----------------
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---------------- host side ----------------
+
+template <int G>
+cudaError_t launch_g(const Params& prm, const CUtensorMap& mk, const CUtensorMap& mv,
+                     const CUtensorMap& mq, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(decode_hp_kernel<G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<G>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(prm.num_ctas);
+  cfg.blockDim = dim3(Cfg<G>::NTHREADS);
+  cfg.dynamicSmemBytes = Cfg<G>::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  // programmatic dependent launch: the prologue may overlap the previous
+  // kernel; the kernel waits for it (griddepcontrol.wait) before reading inputs
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_hp_kernel<G>, mk, mv, mq, prm);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+int heads_per_tile(int group) { return group >= 2 ? 8 : 16; }
+
+}  // namespace hp
+
+size_t hp_workspace_bytes(int64_t num_seqs, int64_t num_heads, int num_ctas) {
+  constexpr int64_t kMaxN = 32;  // columns of a tile (an upper bound over the variants)
+  size_t off = 256;                                                  // error word
+  off += ((size_t)num_seqs * num_heads * 8 + 255) / 256 * 256;       // merge counters (>= units)
+  off += ((size_t)num_ctas * 2 * kMaxN * 8 + 255) / 256 * 256;       // (m, l) per piece slot
+  off += (size_t)num_ctas * 2 * kMaxN * hp::D * 4;                   // partial o per piece slot
+  return off;
+}
+
+bool hp_supported(int head_dim, int group, bool fp8, int num_seqs, int num_kv_heads,
+                  int block_size, int tokens_per_seq) {
+  // a tile holds HB KV heads x TT tokens of one block: H_kv must be a
+  // multiple of HB and a chunk must not cross a block (TT <= block_size)
+  if (fp8 || head_dim != hp::D || tokens_per_seq != 1) return false;
+  if (group != 1 && group != 2 && group != 4) return false;
+  const int hb = hp::heads_per_tile(group);
+  return num_kv_heads % hb == 0 && block_size >= 128 / hb && num_seqs <= hp::kMaxSeqs &&
+         tc::encode_fn() != nullptr;
+}
+
+cudaError_t launch_decode_hp(const TcLaunch& a, cudaStream_t stream) {
+  using namespace hp;
+  tc::EncodeTiledFn enc = tc::encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const int group = a.num_heads / a.num_kv_heads;
+  const int hb = heads_per_tile(group);
+  const int tt = 128 / hb;
+  const int ncol = hb * group;
+  CUtensorMap mk, mv, mq;
+  {
+    // [blocks, block_size, H_kv, d] listed as (d, token, head, block) so that
+    // a box {64, TT, HB, 1} lands head-major: row = head * TT + token
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)a.block_size, (cuuint64_t)a.num_kv_heads,
+                          (cuuint64_t)a.num_blocks};
+    cuuint64_t strides[3] = {(cuuint64_t)a.num_kv_heads * D * 2, (cuuint64_t)D * 2,
+                             (cuuint64_t)a.block_size * a.num_kv_heads * D * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)tt, (cuuint32_t)hb, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (enc(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.k_cache), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    if (enc(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.v_cache), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // q as [S * H rows, d]; a unit's box is {64 of d, its N query heads}
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)a.num_seqs * a.num_heads};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)ncol};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.q), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  Params prm{};
+  prm.out = a.out;
+  prm.block_tables = a.block_tables;
+  prm.context_lens = a.context_lens;
+  prm.lse = a.lse;
+  char* ws = static_cast<char*>(a.workspace);
+  size_t off = 0;
+  prm.err = reinterpret_cast<int*>(ws + off);
+  off += 256;
+  prm.counters = reinterpret_cast<unsigned long long*>(ws + off);
+  off += ((size_t)a.num_seqs * a.num_heads * 8 + 255) / 256 * 256;
+  prm.ws_ml = reinterpret_cast<float2*>(ws + off);
+  off += ((size_t)a.num_ctas * 2 * 32 * 8 + 255) / 256 * 256;
+  prm.ws_o = reinterpret_cast<float*>(ws + off);
+  prm.num_seqs = a.num_seqs;
+  prm.num_heads = a.num_heads;
+  prm.num_groups = a.num_kv_heads / hb;
+  prm.max_blocks = a.max_blocks;
+  prm.num_blocks = a.num_blocks;
+  prm.block_size = a.block_size;
+  int lb = 0;
+  while ((1 << lb) < a.block_size) ++lb;
+  prm.log2_bs = lb;
+  prm.num_ctas = a.num_ctas;
+  prm.scale_log2 = a.scale * 1.4426950408889634f;
+  prm.early_meta = a.early_meta ? 1 : 0;
+  prm.epoch = tc::next_call_epoch();
+  switch (group) {
+    case 1: return launch_g<1>(prm, mk, mv, mq, stream);
+    case 2: return launch_g<2>(prm, mk, mv, mq, stream);
+    case 4: return launch_g<4>(prm, mk, mv, mq, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pa

@@ -69,6 +69,14 @@ bool tc_supported(int head_dim, int group, bool fp8, int num_seqs, int block_siz
 size_t tc_workspace_bytes(int64_t num_seqs, int64_t num_heads, int64_t max_ctx, int num_ctas,
                           int tokens_per_seq = 1);
 cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream);
+// The head-packed tensor-core kernel (decode_hp.cu): a bf16 cache, one token
+// per sequence, GQA group 1, 2 or 4, H_kv a multiple of its heads per tile
+// (16 for group 1, else 8) and blocks of at least 128 / that many tokens.
+// Takes the same TcLaunch (fp8, tokens_per_seq and non_causal unused).
+bool hp_supported(int head_dim, int group, bool fp8, int num_seqs, int num_kv_heads,
+                  int block_size, int tokens_per_seq);
+size_t hp_workspace_bytes(int64_t num_seqs, int64_t num_heads, int num_ctas);
+cudaError_t launch_decode_hp(const TcLaunch& a, cudaStream_t stream);
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value,
                                      void* k_cache, void* v_cache,
