@@ -71,6 +71,7 @@ using tc::arrive;
 using tc::cta_of;
 using tc::drain_bar;
 using tc::kWaitClocks;
+using tc::piece_slot;
 using tc::range_lo;
 using tc::wait_bar;
 
@@ -139,12 +140,6 @@ struct Params {
   unsigned long long epoch;      // 48-bit tag of this call
   int early_meta;                // previous kernel wrote only the cache
 };
-
-// Slot of CTA c's partial for the split unit whose last chunk is `last`:
-// 0 if the unit holds the CTA's last chunk, else 1 (the unit its range starts in).
-__device__ __forceinline__ int piece_slot(int c, long long last, long long K, int C) {
-  return range_lo(c + 1, K, C) - 1 <= last ? 0 : 1;
-}
 
 // One piece (m, l, o) folded into a running merge (M, L, a).  Both merge
 // paths (merge warp, softmax warps) use exactly these roundings, so a unit's

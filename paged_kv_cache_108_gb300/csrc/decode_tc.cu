@@ -69,6 +69,7 @@ namespace tc {
 constexpr int D = 128;
 constexpr int NQ = 16;                 // MMA N of PV: query heads (bf16), hi/lo rows of P (fp8)
 constexpr int kMaxSeqs = 1024;
+constexpr int kMaxCols = 16;           // columns of a unit (the MMA N of PV)
 constexpr int TAB_SLOTS = 4, TAB_AHEAD = 3, TAB_W = 32;  // block-id ring: 4 chunks x 32 boxes
 
 // Shared-memory layout and roles for a bf16 or an fp8-e4m3 cache.
@@ -132,10 +133,10 @@ struct Params {
   const int32_t* context_lens;
   int* err;        // workspace word 0: nonzero if a wait expired / bad id
   unsigned long long* counters;  // [units] (epoch << 16) | arrivals of finished segments
-  float2* ws_ml;   // [units * max_seg * G]
-  float* ws_o;     // [units * max_seg * G * D]
+  float2* ws_ml;   // [num_ctas][2][G]: (m, l) of a split unit's piece (slot: piece_slot)
+  float* ws_o;     // [num_ctas][2][G][D]: its unnormalised o
   int num_seqs, num_heads, num_kv_heads, max_blocks, num_blocks, block_size, log2_bs;
-  int num_ctas, max_seg, box_tok, log2_box;
+  int num_ctas, box_tok, log2_box;
   float scale_log2;
   // Columns of a unit: c = j * gq + i is query head g * gq + i of the
   // sequence's j-th new token (ntok tokens per sequence, the last ntok
@@ -532,8 +533,9 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
     for (; !walk.done(); walk.next()) {
       if (!walk.last_of_segment()) continue;
       const long long first = walk.k - walk.j;
+      const long long lastc = first + walk.nch - 1;
       const int c0 = cta_of(first, Ktot, C);
-      const int c1 = cta_of(first + walk.nch - 1, Ktot, C);
+      const int c1 = cta_of(lastc, Ktot, C);
       if (c0 == c1) continue;  // whole unit: the softmax warps wrote the output
       const bool good = wait_bar(sm, sm.bar(B_EPI + (e++ & 1)), 0, p.err, 14);
       if (!good) continue;
@@ -545,7 +547,6 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
       last = __shfl_sync(0xffffffffu, last, 0);
       if (!last) continue;
       __threadfence();  // see every other piece's partial
-      const int64_t slot0 = (int64_t)u * p.max_seg;
       float M[G], Ls[G], a[G][4];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
@@ -555,13 +556,14 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
         for (int r = 0; r < 4; ++r) a[h][r] = 0.f;
       }
       for (int jj = 0; jj < nseg; ++jj) {
+        const int64_t sj = (int64_t)(c0 + jj) * 2 + piece_slot(c0 + jj, lastc, Ktot, C);
         float2 ml[G];
         float ov[G][4];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          ml[h] = __ldcg(&p.ws_ml[(slot0 + jj) * G + h]);
+          ml[h] = __ldcg(&p.ws_ml[sj * G + h]);
 #pragma unroll
-          for (int r = 0; r < 4; ++r) ov[h][r] = __ldcg(&p.ws_o[((slot0 + jj) * G + h) * D + lane + 32 * r]);
+          for (int r = 0; r < 4; ++r) ov[h][r] = __ldcg(&p.ws_o[(sj * G + h) * D + lane + 32 * r]);
         }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
@@ -725,7 +727,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
         }
       } else {
         // a piece of a split unit: leave the partial for the merge warp
-        const int64_t slot = (int64_t)u * p.max_seg + ((int)blockIdx.x - c0);
+        const int64_t slot = (int64_t)blockIdx.x * 2 + piece_slot(blockIdx.x, last, Ktot, C);
 #pragma unroll
         for (int h = 0; h < G; ++h) p.ws_o[(slot * G + h) * D + t] = acc[h];
 #pragma unroll
@@ -999,16 +1001,16 @@ cudaError_t launch_g(const TcLaunch& a, const Params& prm, const CUtensorMap& mk
 
 }  // namespace tc
 
-size_t tc_workspace_bytes(int64_t num_seqs, int64_t num_heads, int64_t max_ctx, int num_ctas,
-                          int tokens_per_seq) {
-  constexpr int64_t ch = tc::Cfg<false>::CH;  // the shorter chunk: an upper bound on pieces
-  const int64_t max_chunks = (max_ctx + ch - 1) / ch;
-  const int64_t max_seg = max_chunks < num_ctas ? max_chunks : num_ctas;
-  const int64_t rows = num_seqs * (tokens_per_seq > 0 ? tokens_per_seq : 1) * num_heads;  // >= units * columns
+size_t tc_workspace_bytes(int64_t num_seqs, int64_t num_heads, int64_t /*max_ctx*/,
+                          int num_ctas, int tokens_per_seq) {
+  // partials live in two slots per CTA of up to kMaxCols columns, whatever
+  // the context lengths
+  const int64_t rows = num_seqs * (tokens_per_seq > 0 ? tokens_per_seq : 1) * num_heads;  // >= units
+  const int64_t slots = (int64_t)num_ctas * 2 * tc::kMaxCols;
   size_t off = 256;                                             // error word
   off += ((size_t)rows * 8 + 255) / 256 * 256;                  // merge counters
-  off += ((size_t)rows * max_seg * 8 + 255) / 256 * 256;        // (m, l)
-  off += (size_t)rows * max_seg * tc::D * 4;                    // partial o
+  off += ((size_t)slots * 8 + 255) / 256 * 256;                 // (m, l)
+  off += (size_t)slots * tc::D * 4;                             // partial o
   return off;
 }
 
@@ -1070,9 +1072,6 @@ cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const int64_t max_ctx = (int64_t)a.max_blocks * a.block_size;
-  constexpr int64_t ch = Cfg<false>::CH;  // as in tc_workspace_bytes
-  const int64_t max_chunks = (max_ctx + ch - 1) / ch;
   Params prm{};
   prm.out = a.out;
   prm.q = a.q;
@@ -1083,14 +1082,13 @@ cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream) {
   char* ws = static_cast<char*>(a.workspace);
   const int64_t rows = (int64_t)a.num_seqs * ntok * a.num_heads;
   prm.num_ctas = a.num_ctas;
-  prm.max_seg = (int)(max_chunks < a.num_ctas ? max_chunks : a.num_ctas);
   size_t off = 0;
   prm.err = reinterpret_cast<int*>(ws + off);
   off += 256;
   prm.counters = reinterpret_cast<unsigned long long*>(ws + off);
   off += ((size_t)rows * 8 + 255) / 256 * 256;
   prm.ws_ml = reinterpret_cast<float2*>(ws + off);
-  off += ((size_t)rows * prm.max_seg * 8 + 255) / 256 * 256;
+  off += ((size_t)a.num_ctas * 2 * kMaxCols * 8 + 255) / 256 * 256;
   prm.ws_o = reinterpret_cast<float*>(ws + off);
   prm.num_seqs = a.num_seqs;
   prm.num_heads = a.num_heads;

@@ -73,6 +73,14 @@ __device__ __forceinline__ int cta_of(long long k, long long K, int C) {
   return c;
 }
 
+// Slot of CTA c's partial for the split unit whose last chunk is `last`: 0
+// if the unit holds the CTA's last chunk, else 1 (the unit its range starts
+// in).  A CTA's range has at most these two split units, so partials live in
+// two slots per CTA whatever the batch's shape.
+__device__ __forceinline__ int piece_slot(int c, long long last, long long K, int C) {
+  return range_lo(c + 1, K, C) - 1 <= last ? 0 : 1;
+}
+
 // Walks this CTA's chunk range; identical in every role.  The range is
 // visited as up to three contiguous pieces: the unit it ends in (shared with
 // the next CTA), then the unit it starts in (shared with the previous CTA),
