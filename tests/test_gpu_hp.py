@@ -146,3 +146,17 @@ def test_hp_unsupported_shapes_are_refused(hq, hkv, bs, kv):
     from paged_kv_cache_108_gb300._lib import PaError
     with pytest.raises(PaError, match="head-packed"):
         harness.product_step(w, kernel=HP)
+
+
+@requires_gpu
+def test_automatic_choice_takes_head_packed_for_many_units():
+    # 700 sequences of 8 KV heads: kernel 0 picks the head-packed kernel; the
+    # result must equal the forced choice bit for bit and match the oracle
+    rng = np.random.default_rng(159)
+    lens = [int(x) for x in rng.integers(1, 300, size=700)]
+    w = synth.make("hp-auto", lens, 32, 8, 128, 16, seed=161, num_blocks=16000)
+    auto = harness.product_step(w, kernel=0)
+    forced = harness.product_step(w, kernel=HP)
+    assert auto["err"] == 0 and forced["err"] == 0
+    assert np.array_equal(auto["out"], forced["out"])
+    harness.assert_close(auto["out"], harness.oracle_step(w)["out"], False)

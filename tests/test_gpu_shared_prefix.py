@@ -101,3 +101,13 @@ def test_no_sharing_and_member_ending_at_the_prefix():
     _run_and_check(c, 4, False)                  # no shared block: pass 1 is empty
     d = _grouped(4, 3, 24, [0, 17, 300, 5] * 3, 32, 8, "bf16", seed=6)
     _run_and_check(d, 4, False)                  # a member whose context is the prefix
+
+
+@requires_gpu
+def test_many_gqa_groups_suffix_pass_on_head_packed_kernel():
+    # 320 sequences x 8 KV heads: the suffix pass has 320 units of 8 heads,
+    # enough for the automatic choice to take the head-packed kernel (with
+    # its log2-sum-exp output) while the prefix pass stays per-head
+    rng = np.random.default_rng(21)
+    c = _grouped(8, 40, 10, rng.integers(1, 200, size=320), 32, 8, "bf16", seed=22)
+    _run_and_check(c, 8, False)
