@@ -316,6 +316,33 @@ pa_status pa_varlen_attention(void* out, const void* q, const void* k_cache, con
                               size_t workspace_bytes, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * pa_varlen_attention_ex -- pa_varlen_attention with the method chosen.
+ *  method 1: one decode per new token, as described above (every shape
+ *            pa_decode serves; reads a request's context once per token).
+ *  method 2: tensor-core prefill tiles: a work item is a request's tile of
+ *            128 / G new tokens for one KV head (G = the GQA group), its 128
+ *            (token, query head) rows on the MMA's M side against 128-key
+ *            chunks of the paged context, online softmax with one thread per
+ *            row and O kept in tensor memory; the context is read once per
+ *            tile.  Needs a bf16 cache, head_dim 128, G in {1, 2, 4, 8},
+ *            block_size >= 8 and at most 256 requests, else
+ *            PA_ERR_UNSUPPORTED.  Sets workspace word 0 (int32) to a nonzero
+ *            code if a bounded internal wait expired or a block id was out of
+ *            range; the library never clears it.
+ *  method 0: method 2 where it applies and the step adds at least 16 new
+ *            tokens per request on average, else method 1.
+ *  Other arguments as pa_varlen_attention.
+ * ---------------------------------------------------------------------- */
+pa_status pa_varlen_attention_ex(void* out, const void* q, const void* k_cache,
+                                 const void* v_cache, pa_cache_desc cache,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* seq_lens, const int32_t* query_start_loc,
+                                 int32_t num_seqs, int32_t num_tokens, int32_t num_heads,
+                                 float scale, const float* k_scale, const float* v_scale,
+                                 int32_t method, void* workspace, size_t workspace_bytes,
+                                 pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * pa_decode_multi -- pa_varlen_attention for the common case in which every
  * request adds the same number of tokens (multi-token / speculative decode):
  * q and out are [num_seqs * tokens_per_seq, num_heads, head_dim], request

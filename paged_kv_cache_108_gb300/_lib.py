@@ -72,6 +72,8 @@ SIGNATURES = {
                               P, P, P, ctypes.c_size_t, P]),
     "pa_varlen_attention": (I32, [P, P, P, P, CacheDesc, P, I32, P, P, I32, I32, I32, ctypes.c_float, P, P,
                                   P, ctypes.c_size_t, P]),
+    "pa_varlen_attention_ex": (I32, [P, P, P, P, CacheDesc, P, I32, P, P, I32, I32, I32,
+                                     ctypes.c_float, P, P, I32, P, ctypes.c_size_t, P]),
     "pa_slot_mapping": (I32, [PI32, I32, I32, I32, PI32, PI32, I32, PI32]),
     "pa_pool_create": (P, [I32]),
     "pa_pool_create_ordered": (P, [I32, PI32]),

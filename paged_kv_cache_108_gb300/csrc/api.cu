@@ -468,7 +468,23 @@ pa_status pa_varlen_attention(void* out, const void* q, const void* k_cache, con
                               int32_t num_tokens, int32_t num_heads, float scale,
                               const float* k_scale, const float* v_scale, void* workspace,
                               size_t workspace_bytes, pa_stream_t stream) {
+  return pa_varlen_attention_ex(out, q, k_cache, v_cache, cache, block_tables,
+                                max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
+                                num_tokens, num_heads, scale, k_scale, v_scale, 0, workspace,
+                                workspace_bytes, stream);
+}
+
+pa_status pa_varlen_attention_ex(void* out, const void* q, const void* k_cache,
+                                 const void* v_cache, pa_cache_desc cache,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* seq_lens, const int32_t* query_start_loc,
+                                 int32_t num_seqs, int32_t num_tokens, int32_t num_heads,
+                                 float scale, const float* k_scale, const float* v_scale,
+                                 int32_t method, void* workspace, size_t workspace_bytes,
+                                 pa_stream_t stream) {
   const char* fn = "pa_varlen_attention";
+  if (method < 0 || method > 2)
+    return pa_fail(PA_ERR_INVALID, "pa_varlen_attention: method must be 0, 1 or 2");
   char buf[192];
   if (num_seqs < 0 || num_tokens < 0 || max_blocks_per_seq <= 0)
     return pa_fail(PA_ERR_INVALID, "pa_varlen_attention: bad sizes");
@@ -489,12 +505,46 @@ pa_status pa_varlen_attention(void* out, const void* q, const void* k_cache, con
     snprintf(buf, sizeof buf, "pa_varlen_attention: workspace of %zu bytes needed", need);
     return pa_fail(PA_ERR_INVALID, buf);
   }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool fp8 = cache.dtype == PA_KV_FP8_E4M3;
+  const int group = num_heads % cache.num_kv_heads == 0 ? num_heads / cache.num_kv_heads : 0;
+  const bool tiles_fit = group > 0 && pa::prefill_supported(cache.head_dim, group, fp8, num_seqs,
+                                                            cache.block_size);
+  if (method == 2 && !tiles_fit)
+    return pa_fail(PA_ERR_UNSUPPORTED,
+                   "pa_varlen_attention: prefill tiles need a bf16 cache, head_dim 128, GQA "
+                   "group 1, 2, 4 or 8, block_size >= 8 and at most 256 requests");
+  if (method == 2 || (method == 0 && tiles_fit && num_tokens >= 16 * num_seqs)) {
+    if (!out || !q || !k_cache || !v_cache)
+      return pa_fail(PA_ERR_INVALID, "pa_varlen_attention: NULL pointer");
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+      return pa_fail(PA_ERR_INVALID, "pa_varlen_attention: misaligned pointer");
+    if (!std::isfinite(scale)) return pa_fail(PA_ERR_INVALID, "pa_varlen_attention: scale is not finite");
+    pa::PrefillLaunch a{};
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.query_start_loc = query_start_loc;
+    a.workspace = workspace;
+    a.num_seqs = num_seqs;
+    a.num_tokens = num_tokens;
+    a.num_heads = num_heads;
+    a.num_kv_heads = cache.num_kv_heads;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = cache.num_blocks;
+    a.block_size = cache.block_size;
+    a.num_ctas = num_sms();
+    a.scale = scale;
+    return cuda_status(pa::launch_prefill_tc(a, s), fn);
+  }
   char* ws = static_cast<char*>(workspace);
   int32_t* vtables = reinterpret_cast<int32_t*>(ws);
   const size_t tb = align256((size_t)num_tokens * max_blocks_per_seq * 4);
   int32_t* vlens = reinterpret_cast<int32_t*>(ws + tb);
   const size_t meta = tb + align256((size_t)num_tokens * 4);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = pa::launch_varlen_meta(block_tables, max_blocks_per_seq, cache.block_size,
                                          seq_lens, query_start_loc, 0, num_seqs, num_tokens,
                                          vtables, vlens, s);

@@ -73,6 +73,26 @@ cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream);
 // per sequence, GQA group 1, 2 or 4, H_kv a multiple of its heads per tile
 // (16 for group 1, else 8) and blocks of at least 128 / that many tokens.
 // Takes the same TcLaunch (fp8, tokens_per_seq and non_causal unused).
+// Causal varlen attention for prefill chunks on the tensor cores
+// (prefill_tc.cu): bf16 cache, head_dim 128, GQA group 1, 2, 4 or 8, at most
+// 256 requests, blocks of at least 8 tokens.  workspace word 0 is the error
+// word (an expired bounded wait or an out-of-range block id).
+struct PrefillLaunch {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  void* workspace;
+  int num_seqs, num_tokens, num_heads, num_kv_heads, max_blocks, num_blocks, block_size;
+  int num_ctas;
+  float scale;
+};
+bool prefill_supported(int head_dim, int group, bool fp8, int num_seqs, int block_size);
+cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream);
+
 bool hp_supported(int head_dim, int group, bool fp8, int num_seqs, int num_kv_heads,
                   int block_size, int tokens_per_seq);
 size_t hp_workspace_bytes(int64_t num_seqs, int64_t num_heads, int num_ctas);

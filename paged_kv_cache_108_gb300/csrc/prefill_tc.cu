@@ -1,0 +1,643 @@
+// Causal paged attention for prefill chunks on the 5th-generation tensor
+// cores, for a bf16 cache with head_dim 128: the tensor-core path of
+// pa_varlen_attention.
+//
+// What it computes is the varlen paged attention of "Paged attention"
+// (query_start_loc, seq_lens, causal limit): request r's new tokens are
+// q[qsl[r] .. qsl[r+1]), the last T_r positions of its seq_lens[r]-token
+// context (their K/V already written to the cache), and new token j attends
+// to keys 0 .. seq_len - T_r + j; query head h reads KV head h / G.
+//
+// Where the decode kernels put a few query heads on the MMA's N side and
+// stream the context once per step, a prefill tile has many queries: a work
+// item is (request, tile of 128 / G new tokens, KV head), whose 128 query
+// rows -- token-major, row = token * G + head-in-group -- sit on the MMA's M
+// side and share every K/V chunk:
+//   S = Q K^T   tcgen05.mma M=128 rows, N=128 keys, K=128 (d); A = the q tile
+//               (one 3-D TMA box {64 of d, G heads, 128 / G tokens} per
+//               64-column half, rows past the batch zero-filled), B = the K
+//               chunk (the decode kernels' 4-D block boxes);
+//   softmax     thread t owns row t: its 128 logits come from TMEM lane t,
+//               so max and sum need no exchange;
+//   O += P V    M=128 rows, N=128 (d), K=128 keys; A = P (bf16, smem), B = the
+//               V chunk read MN-major straight from the TMA layout; O lives in
+//               TMEM across the item's chunks.
+// O is rescaled only when a row's running max grows by more than 2^8 (p
+// stays below 256, exactly representable in bf16's range); otherwise later
+// chunks keep the old reference max, which the final division by the sum
+// of the same p cancels.  Keys past a row's causal limit get p = 0 (a select,
+// so stale cache bytes never reach the result); V rows past the item's last
+// key are zeroed in smem.
+//
+// Warp roles (192 threads): warps 0-3 softmax and epilogue; warp 4 producer
+// (q tile per item, K/V chunks into a 2-stage ring); warp 5 TMEM allocation
+// and the MMA-issuing thread.  Items go to the persistent CTAs in turn; every
+// role decodes the same item list.  Every mbarrier wait is bounded (error
+// word in the workspace, CTA aborted), as in the decode kernels.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pa_device.cuh"
+#include "pa_kernels.cuh"
+#include "tc_ptx.cuh"
+#include "tc_sched.cuh"
+
+namespace pa {
+namespace pf {
+
+using tc::Smem;
+using tc::drain_bar;
+using tc::kWaitClocks;
+using tc::wait_bar;
+
+constexpr int D = 128;
+constexpr int CHK = 128;                  // keys per chunk
+constexpr int NST = 2;                    // K/V ring stages
+constexpr int kMaxReqs = 256;
+constexpr int TILE_B = CHK * D * 2;       // one K or V chunk: 32 KiB
+constexpr int HALF_B = 128 * 128;         // one 64-column half of a 128-row tile
+constexpr int QTILE_B = 128 * D * 2;      // the q tile: 128 rows
+constexpr int PTILE_B = 128 * CHK * 2;    // P: 128 rows x 128 keys bf16
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + NST * TILE_B;
+constexpr int OFF_Q = OFF_V + NST * TILE_B;
+constexpr int OFF_P = OFF_Q + QTILE_B;
+constexpr int OFF_BAR = OFF_P + 2 * PTILE_B;
+constexpr int B_FULL_K = 0, B_FULL_V = NST, B_EMPTY = 2 * NST, B_Q_FULL = 3 * NST,
+              B_Q_EMPTY = B_Q_FULL + 1, B_S_FULL = B_Q_EMPTY + 1, B_S_EMPTY = B_S_FULL + 2,
+              B_P_FULL = B_S_EMPTY + 2, B_P_EMPTY = B_P_FULL + 2, B_O_FULL = B_P_EMPTY + 2,
+              B_O_EMPTY = B_O_FULL + 2, NBARS = B_O_EMPTY + 1;
+constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
+constexpr int OFF_ABORT = OFF_TMEM + 4;
+constexpr int OFF_TP = OFF_ABORT + 4;                   // tile prefix per request, [R+1]
+constexpr int SMEM_BYTES = OFF_TP + (kMaxReqs + 1) * 4 + 1024;  // + alignment slack
+constexpr int NTHREADS = 192;
+constexpr int TMEM_COLS = 512;  // S[2] at 0 and 128, O at 256
+constexpr int S_COL = 0, O_COL = 256;
+constexpr float kRescaleLog2 = 8.f;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+static_assert(OFF_BAR % 1024 == 0, "tiles stay 1024-byte aligned");
+
+struct Params {
+  void* out;                    // [num_tokens, H, D] bf16
+  const int32_t* block_tables;  // [R, max_blocks]
+  const int32_t* seq_lens;      // [R]
+  const int32_t* qsl;           // [R + 1]
+  int* err;                     // workspace word 0
+  int num_seqs, num_tokens, num_heads, num_kv_heads, max_blocks, num_blocks, block_size, log2_bs;
+  int box_tok, log2_box;
+  float scale_log2;
+};
+
+// One work item: request r, query tile qt (tokens qt*MQ ..), KV head g.
+struct Item {
+  int r, qt, g;
+  int q0;      // first q row of the request
+  int T;       // its new tokens
+  int ctx;     // keys before its first new token (seq_len - T)
+  int ntok;    // new tokens in this tile
+  int kv_end;  // keys the tile's last token sees
+  int nch;     // K/V chunks (0: the request's rows are zero, T > seq_len)
+};
+
+template <int G>
+__device__ __forceinline__ Item item_of(long long i, const int* tp, int R, const Params& p) {
+  constexpr int MQ = 128 / G;
+  Item it;
+  const long long tile = i / p.num_kv_heads;
+  it.g = (int)(i - tile * p.num_kv_heads);
+  int lo = 0, hi = R;  // the request holding this tile: tp[r] <= tile < tp[r+1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tp[mid] <= tile) lo = mid;
+    else hi = mid;
+  }
+  it.r = lo;
+  it.qt = (int)(tile - tp[lo]);
+  it.q0 = __ldg(&p.qsl[lo]);
+  it.T = __ldg(&p.qsl[lo + 1]) - it.q0;
+  const int sl = __ldg(&p.seq_lens[lo]);
+  it.ctx = sl - it.T;
+  it.ntok = min(MQ, it.T - it.qt * MQ);
+  it.kv_end = it.ctx + it.qt * MQ + it.ntok;
+  const int cap = p.max_blocks << p.log2_bs;
+  it.nch = (it.ctx < 0 || it.kv_end > cap) ? 0 : (it.kv_end + CHK - 1) / CHK;
+  return it;
+}
+
+template <int G>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_q, const Params p) {
+  constexpr int MQ = 128 / G;  // new tokens per tile
+  extern __shared__ unsigned char smem_raw[];
+  Smem sm;
+  {
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t aligned = (raw + 1023u) & ~1023u;
+    sm.base = smem_raw + (aligned - raw);
+    sm.base_u32 = aligned;
+    sm.off_bar = OFF_BAR;
+    sm.off_abort = OFF_ABORT;
+  }
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int R = p.num_seqs;
+  int* tp = reinterpret_cast<int*>(sm.base + OFF_TP);
+
+  // ---------------- prologue ----------------
+  ptx::grid_dependency_wait();
+  if (warp == 5) {
+    ptx::tmem_alloc(sm.base_u32 + OFF_TMEM, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < NBARS; ++i) {
+      uint32_t cnt = 1;
+      if ((i >= B_S_EMPTY && i < B_S_EMPTY + 2) || (i >= B_P_FULL && i < B_P_FULL + 2) ||
+          i == B_O_EMPTY)
+        cnt = 128;
+      ptx::mbar_init(sm.bar(i), cnt);
+    }
+    *sm.abort_flag() = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 4 && lane == 0) {
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+    ptx::prefetch_tmap(&tm_q);
+  }
+  // tiles per request, then an exclusive prefix (warp 0)
+  for (int r = tid; r < R; r += NTHREADS) {
+    const int T = __ldg(&p.qsl[r + 1]) - __ldg(&p.qsl[r]);
+    tp[r] = T > 0 ? (T + MQ - 1) / MQ : 0;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < R; base += 32) {
+      const int i = base + lane;
+      const int v = i < R ? tp[i] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (i < R) tp[i] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tp[R] = carry;
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm.base + OFF_TMEM);
+  const long long total = (long long)tp[R] * p.num_kv_heads;  // work items
+
+  if (warp == 4) {
+    // ================= producer =================
+    int qk = 0;        // items with chunks so far (q tile loads)
+    long long ck = 0;  // chunks so far
+    for (long long i = blockIdx.x; i < total; i += gridDim.x) {
+      const Item it = item_of<G>(i, tp, R, p);
+      if (it.nch == 0) continue;
+      if (qk > 0 && !wait_bar(sm, sm.bar(B_Q_EMPTY), (qk - 1) & 1, p.err, 21)) break;
+      if (lane == 0) {
+        // rows token * G + i: box {64 of d, G heads, MQ tokens} per half
+        const uint32_t dst = sm.base_u32 + OFF_Q;
+        const int row = it.q0 + it.qt * MQ;
+        ptx::mbar_arrive_expect_tx(sm.bar(B_Q_FULL), (uint32_t)QTILE_B);
+        ptx::tma_load_3d(dst, &tm_q, sm.bar(B_Q_FULL), 0, it.g * G, row);
+        ptx::tma_load_3d(dst + HALF_B, &tm_q, sm.bar(B_Q_FULL), 64, it.g * G, row);
+      }
+      ++qk;
+      bool ok = true;
+      for (int j = 0; j < it.nch; ++j, ++ck) {
+        const int s = (int)(ck % NST);
+        const uint32_t ph = (uint32_t)(ck / NST) & 1;
+        const int keys = min(CHK, it.kv_end - j * CHK);
+        const int nbox = (keys + p.box_tok - 1) >> p.log2_box;
+        // the chunk's block ids, read while the stage drains
+        int phys = 0;
+        if (lane < nbox)
+          phys = __ldg(&p.block_tables[(int64_t)it.r * p.max_blocks +
+                                       ((j * CHK + lane * p.box_tok) >> p.log2_bs)]);
+        if (!wait_bar(sm, sm.bar(B_EMPTY + s), ph ^ 1, p.err, 22)) {
+          ok = false;
+          break;
+        }
+        if (lane < nbox && (unsigned)phys >= (unsigned)p.num_blocks) {
+          atomicExch(p.err, 3);  // bad block id: load block 0 instead of faulting
+          phys = 0;
+        }
+        const uint32_t bytes = (uint32_t)nbox * p.box_tok * (uint32_t)(D * 2);
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_K + s), bytes);
+          ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_V + s), bytes);
+        }
+        __syncwarp();
+        if (lane < nbox) {
+          const uint32_t row = (uint32_t)(lane * p.box_tok) * 128u;
+          const int off = (j * CHK + lane * p.box_tok) & (p.block_size - 1);
+          const uint32_t kdst = sm.base_u32 + OFF_K + s * TILE_B + row;
+          const uint32_t vdst = sm.base_u32 + OFF_V + s * TILE_B + row;
+          ptx::tma_load_4d(kdst, &tm_k, sm.bar(B_FULL_K + s), 0, it.g, off, phys);
+          ptx::tma_load_4d(kdst + HALF_B, &tm_k, sm.bar(B_FULL_K + s), 64, it.g, off, phys);
+          ptx::tma_load_4d(vdst, &tm_v, sm.bar(B_FULL_V + s), 0, it.g, off, phys);
+          ptx::tma_load_4d(vdst + HALF_B, &tm_v, sm.bar(B_FULL_V + s), 64, it.g, off, phys);
+        }
+      }
+      if (!ok) break;
+    }
+    // drain: the last loads issued must land before the CTA can exit
+    __syncwarp();
+    if (lane == 0) {
+      for (long long l = ck > NST ? ck - NST : 0; l < ck; ++l) {
+        drain_bar(sm.bar(B_FULL_K + (int)(l % NST)), (uint32_t)(l / NST) & 1);
+        drain_bar(sm.bar(B_FULL_V + (int)(l % NST)), (uint32_t)(l / NST) & 1);
+      }
+      if (qk > 0) drain_bar(sm.bar(B_Q_FULL), (qk - 1) & 1);
+    }
+  } else if (warp == 5) {
+    // ================= MMA issuer =================
+    // Two cursors over the same chunk sequence: the logits MMA of chunk nq
+    // (needs its K chunk, a free S buffer and, at an item's first chunk, the
+    // q tile) and the PV MMA of chunk npv < nq (needs P, the V chunk and, at
+    // an item's first chunk, O read out by the previous item's epilogue).
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32_ab(128, CHK, false, false);
+      constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32_ab(128, D, false, true);
+      const uint32_t qbase = sm.base_u32 + OFF_Q;
+      // QK cursor
+      long long qi = blockIdx.x;  // item
+      Item qit{};
+      int qj = 0, qk = 0;  // chunk in item, items with chunks so far
+      bool q_ready = false;
+      auto next_q_item = [&]() {
+        while (qi < total) {
+          qit = item_of<G>(qi, tp, R, p);
+          if (qit.nch > 0) return;
+          qi += gridDim.x;
+        }
+      };
+      next_q_item();
+      // PV cursor
+      long long pi = blockIdx.x;
+      Item pit{};
+      int pj = 0, pk = 0;
+      auto next_p_item = [&]() {
+        while (pi < total) {
+          pit = item_of<G>(pi, tp, R, p);
+          if (pit.nch > 0) return;
+          pi += gridDim.x;
+        }
+      };
+      next_p_item();
+      long long nq = 0, npv = 0;
+      long long t_idle = clock64();
+      while (true) {
+        bool progress = false;
+        if (qi < total) {
+          if (qj == 0 && !q_ready && ptx::mbar_test_wait(sm.bar(B_Q_FULL), qk & 1)) {
+            q_ready = true;
+            progress = true;
+          }
+          const int s = (int)(nq % NST);
+          const int b = (int)(nq & 1);
+          if (q_ready && ptx::mbar_test_wait(sm.bar(B_FULL_K + s), (uint32_t)(nq / NST) & 1) &&
+              ptx::mbar_test_wait(sm.bar(B_S_EMPTY + b), ((uint32_t)(nq >> 1) & 1) ^ 1)) {
+            ptx::tc_fence_after();
+            const uint32_t kbase = sm.base_u32 + OFF_K + s * TILE_B;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t da =
+                  ptx::smem_desc_sw128(qbase + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
+              const uint64_t db =
+                  ptx::smem_desc_sw128(kbase + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
+              ptx::tc_mma_f16(tmem + S_COL + CHK * b, da, db, IDESC_QK, kk > 0);
+            }
+            ptx::tc_commit(sm.bar(B_S_FULL + b));
+            ++nq;
+            if (++qj == qit.nch) {
+              ptx::tc_commit(sm.bar(B_Q_EMPTY));  // the q tile may be reloaded
+              qj = 0;
+              ++qk;
+              q_ready = false;
+              qi += gridDim.x;
+              next_q_item();
+            }
+            progress = true;
+          }
+        }
+        if (npv < nq) {
+          const int s = (int)(npv % NST);
+          const int b = (int)(npv & 1);
+          const uint32_t bph = (uint32_t)(npv >> 1) & 1;
+          const bool o_free = pj > 0 || pk == 0 || ptx::mbar_test_wait(sm.bar(B_O_EMPTY), (pk - 1) & 1);
+          if (o_free && ptx::mbar_test_wait(sm.bar(B_P_FULL + b), bph) &&
+              ptx::mbar_test_wait(sm.bar(B_FULL_V + s), (uint32_t)(npv / NST) & 1)) {
+            ptx::tc_fence_after();
+            const uint32_t vbase = sm.base_u32 + OFF_V + s * TILE_B;
+            const uint32_t pbase = sm.base_u32 + OFF_P + b * PTILE_B;
+            // A = P, K-major (64 keys per 128-byte swizzled half); B = V read
+            // MN-major (16 keys per MMA, d halves HALF_B apart)
+#pragma unroll
+            for (int kk = 0; kk < CHK / 16; ++kk) {
+              const uint64_t da =
+                  ptx::smem_desc_sw128(pbase + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
+              const uint64_t db = ptx::smem_desc_sw128(vbase + kk * 2048, HALF_B, 1024);
+              ptx::tc_mma_f16(tmem + O_COL, da, db, IDESC_PV, pj > 0 || kk > 0);
+            }
+            ptx::tc_commit(sm.bar(B_O_FULL + b));
+            ptx::tc_commit(sm.bar(B_P_EMPTY + b));
+            ptx::tc_commit(sm.bar(B_EMPTY + s));
+            ++npv;
+            if (++pj == pit.nch) {
+              pj = 0;
+              ++pk;
+              pi += gridDim.x;
+              next_p_item();
+            }
+            progress = true;
+          }
+        } else if (qi >= total) {
+          break;
+        }
+        if (progress) {
+          t_idle = clock64();
+        } else {
+          if (*sm.abort_flag()) break;
+          if (clock64() - t_idle > kWaitClocks) {
+            *sm.abort_flag() = 1;
+            atomicExch(p.err, 28);
+            break;
+          }
+        }
+      }
+      // drain: every commit this thread issued must land before exit
+      if (nq > 0) drain_bar(sm.bar(B_S_FULL + (int)((nq - 1) & 1)), (uint32_t)((nq - 1) >> 1) & 1);
+      if (qk > 0) drain_bar(sm.bar(B_Q_EMPTY), (qk - 1) & 1);
+      if (npv > 0) {
+        const long long L = npv - 1;
+        drain_bar(sm.bar(B_EMPTY + (int)(L % NST)), (uint32_t)(L / NST) & 1);
+        drain_bar(sm.bar(B_P_EMPTY + (int)(L & 1)), (uint32_t)(L >> 1) & 1);
+        drain_bar(sm.bar(B_O_FULL + (int)(L & 1)), (uint32_t)(L >> 1) & 1);
+      }
+    }
+  } else if (warp < 4) {
+    // ================= softmax + epilogue (warps 0-3) =================
+    const int t = tid;       // TMEM lane = q tile row
+    const int tok = t / G;   // the row's token within the tile
+    const int hd = t % G;    // its query head within the KV head's group
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    long long ck = 0;
+    for (long long i = blockIdx.x; i < total; i += gridDim.x) {
+      const Item it = item_of<G>(i, tp, R, p);
+      const int rt = it.qt * MQ + tok;  // the row's token within the request
+      const bool row_ok = tok < it.ntok;
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                            ((int64_t)(it.q0 + rt) * p.num_heads + it.g * G + hd) * D;
+      if (it.nch == 0) {
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      const int lim = row_ok ? it.ctx + rt + 1 : 0;  // keys < lim are visible to the row
+      float m_ref = -INFINITY, l = 0.f;
+      bool good = true;
+      for (int j = 0; j < it.nch; ++j, ++ck) {
+        const int b = (int)(ck & 1);
+        const uint32_t bph = (uint32_t)(ck >> 1) & 1;
+        const int s = (int)(ck % NST);
+        const uint32_t ph = (uint32_t)(ck / NST) & 1;
+        // ---- logits of the row for this chunk ----
+        float sv[4][32];
+        good = wait_bar(sm, sm.bar(B_S_FULL + b), bph, p.err, 23) && good;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          ptx::tmem_ld_x32(tmem + lane_base + S_COL + CHK * b + 32 * q4, sv[q4]);
+        ptx::tmem_ld_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(sm.bar(B_S_EMPTY + b));
+        const int kl = lim - j * CHK;  // visible keys of this chunk
+        float cm = -INFINITY;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float x = (good && q4 * 32 + e < kl) ? sv[q4][e] * p.scale_log2 : -INFINITY;
+            sv[q4][e] = x;
+            cm = fmaxf(cm, x);
+          }
+        if (cm > m_ref + kRescaleLog2) {
+          if (m_ref != -INFINITY) {
+            // rescale the row of O (chunks before this one): after their PV
+            const float alpha = fast_exp2(m_ref - cm);
+            const long long L = ck - 1;
+            wait_bar(sm, sm.bar(B_O_FULL + (int)(L & 1)), (uint32_t)(L >> 1) & 1, p.err, 24);
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              float o[32];
+              ptx::tmem_ld_x32(tmem + lane_base + O_COL + 32 * q4, o);
+              ptx::tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] *= alpha;
+              ptx::tmem_st_x32(tmem + lane_base + O_COL + 32 * q4, o);
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            l *= alpha;
+          }
+          m_ref = cm;
+        }
+        const float msafe = m_ref == -INFINITY ? 0.f : m_ref;
+        // ---- P row (and the V rows past the item's last key) ----
+        wait_bar(sm, sm.bar(B_P_EMPTY + b), bph ^ 1, p.err, 25);
+        if (j == it.nch - 1) {
+          const int kc = it.kv_end - j * CHK;
+          if (kc < CHK) {
+            wait_bar(sm, sm.bar(B_FULL_V + s), ph, p.err, 26);
+            if (t >= kc) {
+              unsigned char* vrow = sm.base + OFF_V + s * TILE_B + t * 128;
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const int cc = (c + t) & 7;
+                *reinterpret_cast<uint4*>(vrow + cc * 16) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(vrow + HALF_B + cc * 16) = make_uint4(0, 0, 0, 0);
+              }
+            }
+          }
+        }
+        unsigned char* prow = sm.base + OFF_P + b * PTILE_B + t * 128;
+#pragma unroll
+        for (int c8 = 0; c8 < 16; ++c8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const int e = (c8 & 3) * 8 + 2 * e2;
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(fast_exp2(sv[c8 >> 2][e] - msafe),
+                                                            fast_exp2(sv[c8 >> 2][e + 1] - msafe));
+            l += __low2float(pb) + __high2float(pb);
+            w[e2] = *reinterpret_cast<const uint32_t*>(&pb);
+          }
+          // 128-byte swizzle: 16-byte piece (c8 & 7) of the row's half c8 >> 3
+          *reinterpret_cast<uint4*>(prow + (c8 >> 3) * HALF_B + (((c8 & 7) ^ (t & 7)) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(sm.bar(B_P_FULL + b));
+      }
+      // ---- epilogue: the row of O after the item's last PV ----
+      {
+        const long long L = ck - 1;
+        wait_bar(sm, sm.bar(B_O_FULL + (int)(L & 1)), (uint32_t)(L >> 1) & 1, p.err, 27);
+        ptx::tc_fence_after();
+        const float inv_ok = row_ok && l > 0.f ? 1.f : 0.f;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float o[32];
+          ptx::tmem_ld_x32(tmem + lane_base + O_COL + 32 * q4, o);
+          ptx::tmem_ld_wait();
+          if (inv_ok != 0.f) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e2 = 0; e2 < 4; ++e2) {
+                const int e = c * 8 + 2 * e2;
+                const __nv_bfloat162 ob = __floats2bfloat162_rn(o[e] / l, o[e + 1] / l);
+                w[e2] = *reinterpret_cast<const uint32_t*>(&ob);
+              }
+              reinterpret_cast<uint4*>(orow)[q4 * 4 + c] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(sm.bar(B_O_EMPTY));
+      }
+    }
+  }
+
+  // ---------------- teardown ----------------
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---------------- host side ----------------
+
+template <int G>
+cudaError_t launch_g(const Params& prm, const CUtensorMap& mk, const CUtensorMap& mv,
+                     const CUtensorMap& mq, int num_ctas, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_ctas);
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<G>, mk, mv, mq, prm);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace pf
+
+bool prefill_supported(int head_dim, int group, bool fp8, int num_seqs, int block_size) {
+  // block_size >= 8 keeps every K/V box 1024-byte aligned in smem (whole
+  // 128-byte-swizzle atoms), as in the decode kernels
+  return !fp8 && head_dim == pf::D && (group == 1 || group == 2 || group == 4 || group == 8) &&
+         num_seqs <= pf::kMaxReqs && block_size >= 8 && tc::encode_fn() != nullptr;
+}
+
+cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream) {
+  using namespace pf;
+  tc::EncodeTiledFn enc = tc::encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const int group = a.num_heads / a.num_kv_heads;
+  const int box_tok = a.block_size < 128 ? a.block_size : 128;
+  CUtensorMap mk, mv, mq;
+  {
+    // [blocks, block_size, H_kv, d] as in the decode kernels: a box is one
+    // 64-column half of box_tok tokens of one KV head
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)a.num_kv_heads, (cuuint64_t)a.block_size,
+                          (cuuint64_t)a.num_blocks};
+    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)a.num_kv_heads * D * 2,
+                             (cuuint64_t)a.block_size * a.num_kv_heads * D * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)box_tok, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (enc(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.k_cache), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    if (enc(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.v_cache), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // q as [num_tokens, H, d]; a tile's box is {64 of d, G heads, 128 / G
+    // tokens}: rows token * G + head, tokens past the batch read as zeros
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.num_heads, (cuuint64_t)a.num_tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.num_heads * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)(128 / group)};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  Params prm{};
+  prm.out = a.out;
+  prm.block_tables = a.block_tables;
+  prm.seq_lens = a.seq_lens;
+  prm.qsl = a.query_start_loc;
+  prm.err = static_cast<int*>(a.workspace);
+  prm.num_seqs = a.num_seqs;
+  prm.num_tokens = a.num_tokens;
+  prm.num_heads = a.num_heads;
+  prm.num_kv_heads = a.num_kv_heads;
+  prm.max_blocks = a.max_blocks;
+  prm.num_blocks = a.num_blocks;
+  prm.block_size = a.block_size;
+  int lb = 0;
+  while ((1 << lb) < a.block_size) ++lb;
+  prm.log2_bs = lb;
+  prm.box_tok = box_tok;
+  int lx = 0;
+  while ((1 << lx) < box_tok) ++lx;
+  prm.log2_box = lx;
+  prm.scale_log2 = a.scale * 1.4426950408889634f;
+  switch (group) {
+    case 1: return launch_g<1>(prm, mk, mv, mq, a.num_ctas, stream);
+    case 2: return launch_g<2>(prm, mk, mv, mq, a.num_ctas, stream);
+    case 4: return launch_g<4>(prm, mk, mv, mq, a.num_ctas, stream);
+    case 8: return launch_g<8>(prm, mk, mv, mq, a.num_ctas, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pa

@@ -142,10 +142,12 @@ def varlen_workspace_size(num_tokens: int, num_heads: int, head_dim: int,
 
 
 def varlen_attention(out, q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale,
-                     k_scale=None, v_scale=None, workspace=None, stream=None):
+                     k_scale=None, v_scale=None, workspace=None, stream=None, method=0):
     """Causal paged attention for a step whose requests add several tokens:
     q/out [num_tokens, H_q, d] (request i's tokens at query_start_loc[i] ..
-    query_start_loc[i+1]-1, the last tokens of its seq_lens[i]-token context)."""
+    query_start_loc[i+1]-1, the last tokens of its seq_lens[i]-token context).
+    method: 0 automatic, 1 one decode per new token, 2 tensor-core prefill
+    tiles (pa_varlen_attention_ex)."""
     _same_cache(k_cache, v_cache)
     desc = cache_desc(k_cache)
     ks, vs = _scales(desc, k_scale, v_scale)
@@ -159,12 +161,12 @@ def varlen_attention(out, q, k_cache, v_cache, block_tables, seq_lens, query_sta
     if workspace is None:
         n = varlen_workspace_size(num_tokens, num_heads, head_dim, max_blocks, desc.block_size)
         workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
-    _lib.check(_lib.lib().pa_varlen_attention(
+    _lib.check(_lib.lib().pa_varlen_attention_ex(
         _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16), _dev(k_cache, "k_cache"),
         _dev(v_cache, "v_cache"), desc, _dev(block_tables, "block_tables", torch.int32),
         max_blocks, _dev(seq_lens, "seq_lens", torch.int32),
         _dev(query_start_loc, "query_start_loc", torch.int32), num_seqs, int(num_tokens),
-        int(num_heads), ctypes.c_float(scale), ks, vs, _dev(workspace, "workspace"),
+        int(num_heads), ctypes.c_float(scale), ks, vs, int(method), _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
 
