@@ -36,6 +36,7 @@ if ROOT not in sys.path:
 METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak) and µs/step"
 L2_FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def parse():
@@ -84,6 +85,10 @@ def job_throughput(world, bytes_per_replica_step, seconds_per_step):
 
 
 # ---------------------------------------------------------------- workload
+
+# steps adding at least this many tokens per sequence run as prefill chunks
+# (pa_varlen_attention: tensor-core prefill tiles, a tensor-bound roofline)
+PREFILL_TOKENS = 16
 
 WORKLOADS = {
     "llama8b": "llama8b-layer decode, batch 64, 32q/8kv heads, d=128",
@@ -168,7 +173,7 @@ class Step:
         self.new_tokens = T
         self.q = torch.randn((S * T, H, d), generator=gen, device=device).to(torch.bfloat16)
         self.k_new = torch.randn((S * T, hkv, d), generator=gen, device=device).to(torch.bfloat16)
-        self.v_new = torch.randn((S, hkv, d), generator=gen, device=device).to(torch.bfloat16)
+        self.v_new = torch.randn((S * T, hkv, d), generator=gen, device=device).to(torch.bfloat16)
         # the step's tokens: the last T positions of every context, sequence-major
         self.token_seq = np.repeat(np.arange(S, dtype=np.int32), T)
         self.positions = (np.repeat(w.context_lens, T) - T +
@@ -186,6 +191,9 @@ class Step:
             self.ws = torch.empty(n, dtype=torch.uint8, device=device)
         elif T == 1:
             self.ws = ops.alloc_workspace(S, H, d, w.max_blocks, B, partition, device=device)
+        elif T >= PREFILL_TOKENS:
+            n = ops.varlen_workspace_size(S * T, H, d, w.max_blocks, B)
+            self.ws = torch.empty(n, dtype=torch.uint8, device=device)
         else:
             n = ops.decode_multi_workspace_size(S, T, H, d, w.max_blocks, B)
             self.ws = torch.empty(n, dtype=torch.uint8, device=device)
@@ -199,6 +207,8 @@ class Step:
         if shared_prefix_group:
             # metadata, prefix pass, suffix pass, merge -- plus the cache write
             self.launches_per_step = 5
+        if T >= PREFILL_TOKENS:
+            self.launches_per_step = 2  # cache write, prefill tiles
 
     # algorithmic bytes of one step (what the method must move): K/V rows
     # stored once are read once (shared prefix blocks count once)
@@ -209,6 +219,13 @@ class Step:
         qo = 2 * w.num_seqs * self.new_tokens * w.num_heads * w.head_dim * 2
         table = int(sum(math.ceil(n / w.block_size) for n in w.context_lens)) * 4
         return kv + qo + table + w.num_seqs * 4
+
+    # causal attention flops of one step: per query head, 4 d per visible
+    # (new token, key) pair -- the tensor-core prefill tiles' algorithmic work
+    def decode_flops(self) -> float:
+        w, T = self.w, self.new_tokens
+        pairs = sum(int(n - T) * T + T * (T + 1) // 2 for n in w.context_lens)
+        return 4.0 * w.head_dim * w.num_heads * pairs
 
     def write_bytes(self) -> int:
         w = self.w
@@ -243,6 +260,12 @@ class Step:
                                           self.context_lens if cl is None else cl, self.group,
                                           w.scale, self.k_scale, self.v_scale, workspace=self.ws)
             return
+        if self.new_tokens >= PREFILL_TOKENS:
+            self.ops.varlen_attention(self.out, self.q if q is None else q, self.k_cache,
+                                      self.v_cache, self.block_tables if bt is None else bt,
+                                      self.context_lens if cl is None else cl, self.qsl,
+                                      w.scale, self.k_scale, self.v_scale, workspace=self.ws)
+            return
         if self.new_tokens > 1:
             self.ops.decode_multi(self.out, self.q if q is None else q, self.k_cache,
                                   self.v_cache, self.block_tables if bt is None else bt,
@@ -265,6 +288,15 @@ def measured_peak():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:  # noqa: BLE001
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:  # noqa: BLE001
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def recorded_traffic(step_bytes, kv_dtype="bf16"):
@@ -451,7 +483,8 @@ def run_ours(args, rank, world, local_rank):
         e2e = run_e2e(step, args, device, dist)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    # the oracle baseline samples decode units: single-token steps only
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and step.new_tokens == 1:
         cpu = cpu_baseline_oracle(step)
 
     if rank != 0:
@@ -460,6 +493,25 @@ def run_ours(args, rank, world, local_rank):
     dbytes = step.decode_bytes()
     sbytes = dbytes + step.write_bytes()
     achieved = dbytes / (mean_dec * 1e-3) / 1e9
+    if step.new_tokens >= PREFILL_TOKENS:
+        # prefill chunks are a dense contraction: causal attention flops per
+        # second against the measured bf16 tensor peak (burst: the call is
+        # timed on its own)
+        tpk, tsrc = measured_tensor_peak()
+        tf = step.decode_flops() / (mean_dec * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": "pa_varlen_attention alone (tensor-core "
+                    "prefill tiles)", "achieved": round(tf, 2), "peak": tpk, "peak_source": tsrc,
+                    "unit": "TFLOP/s", "frac": round(tf / tpk, 4), "traffic": None,
+                    "algorithmic_flops": step.decode_flops()}
+    else:
+        roofline = {"bound": "hbm", "kernel": "pa_decode alone (tcgen05 paged decode; split "
+                    "units merged in-kernel)", "achieved": round(achieved, 2), "peak": peak,
+                    "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                    # the ncu record covers the headline decode at block 16 only
+                    "traffic": (recorded_traffic(dbytes, args.kv_dtype)
+                                if args.workload == "llama8b" and args.block_size == 16
+                                and step.new_tokens == 1 and not step.group else None),
+                    "algorithmic_bytes": dbytes}
     value = job_throughput(world, sbytes, mean_step * 1e-3) / 1e9
     w = step.w
     line = {
@@ -472,7 +524,9 @@ def run_ours(args, rank, world, local_rank):
                  "synthetic (seeded N(0,1) bf16 K/V/q; lengths from the pages' seeded request mix)"),
         "config": {"workload": f"{WORKLOADS[args.workload]}, "
                                + (f"{step.new_tokens} new tokens per sequence "
-                                  "(pa_decode_multi), " if step.new_tokens > 1 else "")
+                                  + ("(chunked prefill, pa_varlen_attention tiles), "
+                                     if step.new_tokens >= PREFILL_TOKENS else
+                                     "(pa_decode_multi), ") if step.new_tokens > 1 else "")
                                + (f"shared-prefix groups of {step.group} "
                                   "(pa_decode_shared_prefix), " if step.group else "")
                                + f"{'e4m3 (per-tensor scale)' if step.fp8 else 'bf16'} KV, "
@@ -496,14 +550,7 @@ def run_ours(args, rank, world, local_rank):
         "us_write": round(sum(wr_ms) / K * 1e3, 2),
         "tokens_per_s": round(world * w.num_seqs * step.new_tokens / (mean_step * 1e-3), 1),
         "pct_of_nominal_8tbps": round(100 * achieved / 8000.0, 1),
-        "roofline": {"bound": "hbm", "kernel": "pa_decode alone (tcgen05 paged decode; split units merged in-kernel)",
-                     "achieved": round(achieved, 2), "peak": peak, "peak_source": peak_src,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     # the ncu record covers the headline layer at block 16 only
-                     "traffic": (recorded_traffic(dbytes, args.kv_dtype)
-                                 if args.workload == "llama8b" and args.block_size == 16
-                                 else None),
-                     "algorithmic_bytes": dbytes},
+        "roofline": roofline,
         "gpu_launches": K * 2 * step.launches_per_step,
         "clocks": clk.summary(),
     }

@@ -63,6 +63,18 @@ def _same_cache(k_cache, v_cache):
         raise ValueError("k_cache and v_cache must have the same shape and dtype")
 
 
+def _check_meta(desc, q, block_tables, lens, num_seqs, lens_name="context_lens"):
+    """Sizes the library cannot check through its raw pointers: one table row
+    and one length per sequence, q's head_dim equal to the cache's."""
+    if block_tables.dim() != 2 or block_tables.shape[0] != num_seqs:
+        raise ValueError(f"block_tables must be [{num_seqs}, max_blocks_per_seq], "
+                         f"got {list(block_tables.shape)}")
+    if lens.numel() != num_seqs:
+        raise ValueError(f"{lens_name} needs {num_seqs} entries, got {lens.numel()}")
+    if q.shape[-1] != desc.head_dim:
+        raise ValueError(f"q's head_dim {q.shape[-1]} differs from the cache's {desc.head_dim}")
+
+
 def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, k_scale=None,
                       v_scale=None, stream=None) -> None:
     """Write key/value [N, H_kv, d] (bf16) into the caches at ``slot_mapping``."""
@@ -70,6 +82,10 @@ def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, k_scale=None,
     desc = cache_desc(k_cache)
     ks, vs = _scales(desc, k_scale, v_scale)
     n = int(slot_mapping.numel())
+    want = (n, desc.num_kv_heads, desc.head_dim)
+    if tuple(key.shape) != want or tuple(value.shape) != want:
+        raise ValueError(f"key and value must be {list(want)} (one row per slot), "
+                         f"got {list(key.shape)} and {list(value.shape)}")
     _lib.check(_lib.lib().pa_reshape_and_cache(
         _dev(key, "key", torch.bfloat16), _dev(value, "value", torch.bfloat16),
         _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), desc,
@@ -100,8 +116,7 @@ def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, k_scale=
     if q.dim() != 3 or out.shape != q.shape:
         raise ValueError("q and out must both be [num_seqs, num_heads, head_dim]")
     num_seqs, num_heads, _ = q.shape
-    if block_tables.dim() != 2 or block_tables.shape[0] != num_seqs:
-        raise ValueError("block_tables must be [num_seqs, max_blocks_per_seq]")
+    _check_meta(desc, q, block_tables, context_lens, num_seqs)
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr = _dev(workspace, "workspace")
@@ -157,6 +172,7 @@ def varlen_attention(out, q, k_cache, v_cache, block_tables, seq_lens, query_sta
     num_seqs = int(seq_lens.numel())
     if query_start_loc.numel() != num_seqs + 1:
         raise ValueError("query_start_loc needs num_seqs + 1 entries")
+    _check_meta(desc, q, block_tables, seq_lens, num_seqs, "seq_lens")
     max_blocks = int(block_tables.shape[1])
     if workspace is None:
         n = varlen_workspace_size(num_tokens, num_heads, head_dim, max_blocks, desc.block_size)
@@ -190,6 +206,7 @@ def decode_multi(out, q, k_cache, v_cache, block_tables, context_lens, tokens_pe
     if q.dim() != 3 or out.shape != q.shape or q.shape[0] != num_seqs * tokens_per_seq:
         raise ValueError("q and out must be [num_seqs * tokens_per_seq, num_heads, head_dim]")
     _, num_heads, head_dim = q.shape
+    _check_meta(desc, q, block_tables, context_lens, num_seqs)
     max_blocks = int(block_tables.shape[1])
     if workspace is None:
         n = decode_multi_workspace_size(num_seqs, tokens_per_seq, num_heads, head_dim,
@@ -221,6 +238,7 @@ def decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens, g
     if q.dim() != 3 or out.shape != q.shape:
         raise ValueError("q and out must both be [num_seqs, num_heads, head_dim]")
     num_seqs, num_heads, head_dim = q.shape
+    _check_meta(desc, q, block_tables, context_lens, num_seqs)
     max_blocks = int(block_tables.shape[1])
     if workspace is None:
         n = max(decode_shared_prefix_workspace_size(num_seqs, group_size, num_heads, head_dim,
@@ -290,6 +308,11 @@ def write_and_decode(key, value, slot_mapping, out, q, k_cache, v_cache, block_t
     if q.dim() != 3 or out.shape != q.shape:
         raise ValueError("q and out must both be [num_seqs, num_heads, head_dim]")
     num_seqs, num_heads, _ = q.shape
+    _check_meta(desc, q, block_tables, context_lens, num_seqs)
+    want = (int(slot_mapping.numel()), desc.num_kv_heads, desc.head_dim)
+    if tuple(key.shape) != want or tuple(value.shape) != want:
+        raise ValueError(f"key and value must be {list(want)} (one row per slot), "
+                         f"got {list(key.shape)} and {list(value.shape)}")
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr = _dev(workspace, "workspace")
