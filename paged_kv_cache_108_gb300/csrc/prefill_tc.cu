@@ -17,8 +17,8 @@
 //               (one 3-D TMA box {64 of d, G heads, 128 / G tokens} per
 //               64-column half, rows past the batch zero-filled), B = the K
 //               chunk (the decode kernels' 4-D block boxes);
-//   softmax     thread t owns row t: its 128 logits come from TMEM lane t,
-//               so max and sum need no exchange;
+//   softmax     two threads per row, 64 logits each from TMEM lane row; the
+//               pair exchanges its half-row max through shared memory;
 //   O += P V    M=128 rows, N=128 (d), K=128 keys; A = P (bf16, smem), B = the
 //               V chunk read MN-major straight from the TMA layout; O lives in
 //               TMEM across the item's chunks.
@@ -29,9 +29,10 @@
 // so stale cache bytes never reach the result); V rows past the item's last
 // key are zeroed in smem.
 //
-// Warp roles (192 threads): warps 0-3 softmax and epilogue; warp 4 producer
-// (q tile per item, K/V chunks into a 2-stage ring); warp 5 TMEM allocation
-// and the MMA-issuing thread.  Items go to the persistent CTAs in turn; every
+// Warp roles (320 threads): warps 0-7 softmax and epilogue, two threads per
+// row (64 keys and 64 output columns each); warp 8 producer (q tile per
+// item, K/V chunks into a 2-stage ring); warp 9 TMEM allocation and the
+// MMA-issuing thread.  Items go to the persistent CTAs in turn; every
 // role decodes the same item list.  Every mbarrier wait is bounded (error
 // word in the workspace, CTA aborted), as in the decode kernels.
 #include <cuda.h>
@@ -72,9 +73,13 @@ constexpr int B_FULL_K = 0, B_FULL_V = NST, B_EMPTY = 2 * NST, B_Q_FULL = 3 * NS
               B_O_EMPTY = B_O_FULL + 2, NBARS = B_O_EMPTY + 1;
 constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 4;
-constexpr int OFF_TP = OFF_ABORT + 4;                   // tile prefix per request, [R+1]
-constexpr int SMEM_BYTES = OFF_TP + (kMaxReqs + 1) * 4 + 1024;  // + alignment slack
-constexpr int NTHREADS = 192;
+// tile prefix per request, [R+1]; 16 bits suffice: at most 65535 new tokens
+constexpr int OFF_TP = OFF_ABORT + 4;
+constexpr int OFF_XCH = (OFF_TP + (kMaxReqs + 1) * 2 + 15) / 16 * 16;  // [256] floats
+constexpr int SMEM_BYTES = OFF_XCH + 256 * 4 + 1024;                  // + alignment slack
+constexpr int NSOFT = 256;  // softmax threads: two per q tile row
+constexpr int NTHREADS = NSOFT + 64;
+constexpr int PROD_WARP = NSOFT / 32, MMA_WARP = PROD_WARP + 1;
 constexpr int TMEM_COLS = 512;  // S[2] at 0 and 128, O at 256
 constexpr int S_COL = 0, O_COL = 256;
 constexpr float kRescaleLog2 = 8.f;
@@ -104,7 +109,8 @@ struct Item {
 };
 
 template <int G>
-__device__ __forceinline__ Item item_of(long long i, const int* tp, int R, const Params& p) {
+__device__ __forceinline__ Item item_of(long long i, const uint16_t* tp, int R,
+                                        const Params& p) {
   constexpr int MQ = 128 / G;
   Item it;
   const long long tile = i / p.num_kv_heads;
@@ -148,11 +154,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int R = p.num_seqs;
-  int* tp = reinterpret_cast<int*>(sm.base + OFF_TP);
+  uint16_t* tp = reinterpret_cast<uint16_t*>(sm.base + OFF_TP);
 
   // ---------------- prologue ----------------
   ptx::grid_dependency_wait();
-  if (warp == 5) {
+  if (warp == MMA_WARP) {
     ptx::tmem_alloc(sm.base_u32 + OFF_TMEM, TMEM_COLS);
     ptx::tmem_relinquish();
   }
@@ -161,13 +167,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       uint32_t cnt = 1;
       if ((i >= B_S_EMPTY && i < B_S_EMPTY + 2) || (i >= B_P_FULL && i < B_P_FULL + 2) ||
           i == B_O_EMPTY)
-        cnt = 128;
+        cnt = NSOFT;
       ptx::mbar_init(sm.bar(i), cnt);
     }
     *sm.abort_flag() = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == PROD_WARP && lane == 0) {
     ptx::prefetch_tmap(&tm_k);
     ptx::prefetch_tmap(&tm_v);
     ptx::prefetch_tmap(&tm_q);
@@ -175,7 +181,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // tiles per request, then an exclusive prefix (warp 0)
   for (int r = tid; r < R; r += NTHREADS) {
     const int T = __ldg(&p.qsl[r + 1]) - __ldg(&p.qsl[r]);
-    tp[r] = T > 0 ? (T + MQ - 1) / MQ : 0;
+    tp[r] = (uint16_t)(T > 0 ? (T + MQ - 1) / MQ : 0);
   }
   __syncthreads();
   if (warp == 0) {
@@ -189,10 +195,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int o = __shfl_up_sync(0xffffffffu, incl, off);
         if (lane >= off) incl += o;
       }
-      if (i < R) tp[i] = carry + incl - v;
+      if (i < R) tp[i] = (uint16_t)(carry + incl - v);
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) tp[R] = carry;
+    if (lane == 0) tp[R] = (uint16_t)carry;
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -200,7 +206,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm.base + OFF_TMEM);
   const long long total = (long long)tp[R] * p.num_kv_heads;  // work items
 
-  if (warp == 4) {
+  if (warp == PROD_WARP) {
     // ================= producer =================
     int qk = 0;        // items with chunks so far (q tile loads)
     long long ck = 0;  // chunks so far
@@ -264,7 +270,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       if (qk > 0) drain_bar(sm.bar(B_Q_FULL), (qk - 1) & 1);
     }
-  } else if (warp == 5) {
+  } else if (warp == MMA_WARP) {
     // ================= MMA issuer =================
     // Two cursors over the same chunk sequence: the logits MMA of chunk nq
     // (needs its K chunk, a free S buffer and, at an item's first chunk, the
@@ -390,23 +396,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         drain_bar(sm.bar(B_O_FULL + (int)(L & 1)), (uint32_t)(L >> 1) & 1);
       }
     }
-  } else if (warp < 4) {
-    // ================= softmax + epilogue (warps 0-3) =================
-    const int t = tid;       // TMEM lane = q tile row
-    const int tok = t / G;   // the row's token within the tile
-    const int hd = t % G;    // its query head within the KV head's group
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  } else {
+    // ================= softmax + epilogue (warps 0-7) =================
+    // Two threads per q tile row: thread t takes keys (and O columns)
+    // half * 64 .. half * 64 + 63 of row t & 127; warps w and w + 4 read the
+    // same TMEM lanes.  The pair exchanges its half-row max (and, at the end,
+    // its half-row sum) through shared memory.
+    const int row = tid & 127;
+    const int half = tid >> 7;
+    const int tok = row / G;   // the row's token within the tile
+    const int hd = row % G;    // its query head within the KV head's group
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    float* xch = reinterpret_cast<float*>(sm.base + OFF_XCH);
+    auto partner = [&](float v) -> float {
+      ptx::bar_sync_named(1, NSOFT);  // the previous exchange has been read
+      xch[tid] = v;
+      ptx::bar_sync_named(2, NSOFT);
+      return xch[tid ^ 128];
+    };
     long long ck = 0;
     for (long long i = blockIdx.x; i < total; i += gridDim.x) {
       const Item it = item_of<G>(i, tp, R, p);
       const int rt = it.qt * MQ + tok;  // the row's token within the request
       const bool row_ok = tok < it.ntok;
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                            ((int64_t)(it.q0 + rt) * p.num_heads + it.g * G + hd) * D;
+                            ((int64_t)(it.q0 + rt) * p.num_heads + it.g * G + hd) * D + half * 64;
       if (it.nch == 0) {
         if (row_ok) {
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < 8; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -418,41 +436,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t bph = (uint32_t)(ck >> 1) & 1;
         const int s = (int)(ck % NST);
         const uint32_t ph = (uint32_t)(ck / NST) & 1;
-        // ---- logits of the row for this chunk ----
-        float sv[4][32];
+        // ---- this thread's 64 logits of the row ----
+        float sv[2][32];
         good = wait_bar(sm, sm.bar(B_S_FULL + b), bph, p.err, 23) && good;
         ptx::tc_fence_after();
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          ptx::tmem_ld_x32(tmem + lane_base + S_COL + CHK * b + 32 * q4, sv[q4]);
+        for (int q2 = 0; q2 < 2; ++q2)
+          ptx::tmem_ld_x32(tmem + lane_base + S_COL + CHK * b + half * 64 + 32 * q2, sv[q2]);
         ptx::tmem_ld_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(sm.bar(B_S_EMPTY + b));
-        const int kl = lim - j * CHK;  // visible keys of this chunk
-        float cm = -INFINITY;
+        const int kl = lim - j * CHK - half * 64;  // visible keys among this thread's 64
+        float hm = -INFINITY;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
+        for (int q2 = 0; q2 < 2; ++q2)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const float x = (good && q4 * 32 + e < kl) ? sv[q4][e] * p.scale_log2 : -INFINITY;
-            sv[q4][e] = x;
-            cm = fmaxf(cm, x);
+            const float x = (good && q2 * 32 + e < kl) ? sv[q2][e] * p.scale_log2 : -INFINITY;
+            sv[q2][e] = x;
+            hm = fmaxf(hm, x);
           }
+        const float cm = fmaxf(hm, partner(hm));  // the row's chunk max, same in both
         if (cm > m_ref + kRescaleLog2) {
           if (m_ref != -INFINITY) {
-            // rescale the row of O (chunks before this one): after their PV
+            // rescale this half of the row of O (earlier chunks): after their PV
             const float alpha = fast_exp2(m_ref - cm);
             const long long L = ck - 1;
             wait_bar(sm, sm.bar(B_O_FULL + (int)(L & 1)), (uint32_t)(L >> 1) & 1, p.err, 24);
             ptx::tc_fence_after();
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q2 = 0; q2 < 2; ++q2) {
               float o[32];
-              ptx::tmem_ld_x32(tmem + lane_base + O_COL + 32 * q4, o);
+              const uint32_t ta = tmem + lane_base + O_COL + half * 64 + 32 * q2;
+              ptx::tmem_ld_x32(ta, o);
               ptx::tmem_ld_wait();
 #pragma unroll
               for (int e = 0; e < 32; ++e) o[e] *= alpha;
-              ptx::tmem_st_x32(tmem + lane_base + O_COL + 32 * q4, o);
+              ptx::tmem_st_x32(ta, o);
             }
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
@@ -461,26 +481,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           m_ref = cm;
         }
         const float msafe = m_ref == -INFINITY ? 0.f : m_ref;
-        // ---- P row (and the V rows past the item's last key) ----
+        // ---- P (and the V rows past the item's last key) ----
         wait_bar(sm, sm.bar(B_P_EMPTY + b), bph ^ 1, p.err, 25);
         if (j == it.nch - 1) {
           const int kc = it.kv_end - j * CHK;
           if (kc < CHK) {
             wait_bar(sm, sm.bar(B_FULL_V + s), ph, p.err, 26);
-            if (t >= kc) {
-              unsigned char* vrow = sm.base + OFF_V + s * TILE_B + t * 128;
+            if (row >= kc) {
+              // this thread's 64 columns of V row `row`
+              unsigned char* vrow = sm.base + OFF_V + s * TILE_B + half * HALF_B + row * 128;
 #pragma unroll
               for (int c = 0; c < 8; ++c) {
-                const int cc = (c + t) & 7;
+                const int cc = (c + row) & 7;
                 *reinterpret_cast<uint4*>(vrow + cc * 16) = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(vrow + HALF_B + cc * 16) = make_uint4(0, 0, 0, 0);
               }
             }
           }
         }
-        unsigned char* prow = sm.base + OFF_P + b * PTILE_B + t * 128;
+        // keys half * 64 ..: the row's 128-byte half `half` of the P tile
+        unsigned char* prow = sm.base + OFF_P + b * PTILE_B + half * HALF_B + row * 128;
 #pragma unroll
-        for (int c8 = 0; c8 < 16; ++c8) {
+        for (int c8 = 0; c8 < 8; ++c8) {
           uint32_t w[4];
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) {
@@ -490,35 +511,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             l += __low2float(pb) + __high2float(pb);
             w[e2] = *reinterpret_cast<const uint32_t*>(&pb);
           }
-          // 128-byte swizzle: 16-byte piece (c8 & 7) of the row's half c8 >> 3
-          *reinterpret_cast<uint4*>(prow + (c8 >> 3) * HALF_B + (((c8 & 7) ^ (t & 7)) << 4)) =
+          *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) =
               make_uint4(w[0], w[1], w[2], w[3]);
         }
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(sm.bar(B_P_FULL + b));
       }
-      // ---- epilogue: the row of O after the item's last PV ----
+      // ---- epilogue: this half of the row of O after the item's last PV ----
       {
         const long long L = ck - 1;
         wait_bar(sm, sm.bar(B_O_FULL + (int)(L & 1)), (uint32_t)(L >> 1) & 1, p.err, 27);
         ptx::tc_fence_after();
-        const float inv_ok = row_ok && l > 0.f ? 1.f : 0.f;
+        const float lsum = l + partner(l);
+        const bool store = row_ok && lsum > 0.f;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q2 = 0; q2 < 2; ++q2) {
           float o[32];
-          ptx::tmem_ld_x32(tmem + lane_base + O_COL + 32 * q4, o);
+          ptx::tmem_ld_x32(tmem + lane_base + O_COL + half * 64 + 32 * q2, o);
           ptx::tmem_ld_wait();
-          if (inv_ok != 0.f) {
+          if (store) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               uint32_t w[4];
 #pragma unroll
               for (int e2 = 0; e2 < 4; ++e2) {
                 const int e = c * 8 + 2 * e2;
-                const __nv_bfloat162 ob = __floats2bfloat162_rn(o[e] / l, o[e + 1] / l);
+                const __nv_bfloat162 ob = __floats2bfloat162_rn(o[e] / lsum, o[e + 1] / lsum);
                 w[e2] = *reinterpret_cast<const uint32_t*>(&ob);
               }
-              reinterpret_cast<uint4*>(orow)[q4 * 4 + c] = make_uint4(w[0], w[1], w[2], w[3]);
+              reinterpret_cast<uint4*>(orow)[q2 * 4 + c] = make_uint4(w[0], w[1], w[2], w[3]);
             }
           }
         }
@@ -531,7 +552,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // ---------------- teardown ----------------
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == MMA_WARP) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
