@@ -325,7 +325,7 @@ pa_status pa_varlen_attention(void* out, const void* q, const void* k_cache, con
  *            chunks of the paged context, online softmax with one thread per
  *            row and O kept in tensor memory; the context is read once per
  *            tile.  Needs a bf16 cache, head_dim 128, G in {1, 2, 4, 8},
- *            block_size >= 8 and at most 256 requests, else
+ *            block_size >= 8, at most 256 requests and scale > 0, else
  *            PA_ERR_UNSUPPORTED.  Sets workspace word 0 (int32) to a nonzero
  *            code if a bounded internal wait expired or a block id was out of
  *            range; the library never clears it.

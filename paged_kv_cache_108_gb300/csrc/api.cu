@@ -508,12 +508,13 @@ pa_status pa_varlen_attention_ex(void* out, const void* q, const void* k_cache,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool fp8 = cache.dtype == PA_KV_FP8_E4M3;
   const int group = num_heads % cache.num_kv_heads == 0 ? num_heads / cache.num_kv_heads : 0;
-  const bool tiles_fit = group > 0 && pa::prefill_supported(cache.head_dim, group, fp8, num_seqs,
-                                                            cache.block_size);
+  const bool tiles_fit = group > 0 && scale > 0.f &&
+                         pa::prefill_supported(cache.head_dim, group, fp8, num_seqs,
+                                               cache.block_size);
   if (method == 2 && !tiles_fit)
     return pa_fail(PA_ERR_UNSUPPORTED,
                    "pa_varlen_attention: prefill tiles need a bf16 cache, head_dim 128, GQA "
-                   "group 1, 2, 4 or 8, block_size >= 8 and at most 256 requests");
+                   "group 1, 2, 4 or 8, block_size >= 8, at most 256 requests and scale > 0");
   if (method == 2 || (method == 0 && tiles_fit && num_tokens >= 16 * num_seqs)) {
     if (!out || !q || !k_cache || !v_cache)
       return pa_fail(PA_ERR_INVALID, "pa_varlen_attention: NULL pointer");

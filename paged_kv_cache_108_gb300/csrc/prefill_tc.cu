@@ -23,9 +23,12 @@
 //               V chunk read MN-major straight from the TMA layout; O lives in
 //               TMEM across the item's chunks.
 // O is rescaled only when a row's running max grows by more than 2^8 (p
-// stays below 256, exactly representable in bf16's range); otherwise later
-// chunks keep the old reference max, which the final division by the sum
-// of the same p cancels.  Keys past a row's causal limit get p = 0 (a select,
+// stays below 256, well inside bf16's range); otherwise later chunks keep
+// the old reference max, which the final division by the sum of the same p
+// cancels.  The sum adds each p before its bf16 rounding (the MMA's P is
+// rounded): a relative difference below bf16's rounding error.  The scale
+// must be positive (the max is taken over the raw logits and the scale
+// folded into one FMA per logit).  Keys past a row's causal limit get p = 0 (a select,
 // so stale cache bytes never reach the result); V rows past the item's last
 // key are zeroed in smem.
 //
@@ -66,7 +69,7 @@ constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + NST * TILE_B;
 constexpr int OFF_Q = OFF_V + NST * TILE_B;
 constexpr int OFF_P = OFF_Q + QTILE_B;
-constexpr int OFF_BAR = OFF_P + 2 * PTILE_B;
+constexpr int OFF_BAR = OFF_P + PTILE_B;  // one P buffer (the softmax rarely waits for it)
 constexpr int B_FULL_K = 0, B_FULL_V = NST, B_EMPTY = 2 * NST, B_Q_FULL = 3 * NST,
               B_Q_EMPTY = B_Q_FULL + 1, B_S_FULL = B_Q_EMPTY + 1, B_S_EMPTY = B_S_FULL + 2,
               B_P_FULL = B_S_EMPTY + 2, B_P_EMPTY = B_P_FULL + 2, B_O_FULL = B_P_EMPTY + 2,
@@ -75,8 +78,8 @@ constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 4;
 // tile prefix per request, [R+1]; 16 bits suffice: at most 65535 new tokens
 constexpr int OFF_TP = OFF_ABORT + 4;
-constexpr int OFF_XCH = (OFF_TP + (kMaxReqs + 1) * 2 + 15) / 16 * 16;  // [256] floats
-constexpr int SMEM_BYTES = OFF_XCH + 256 * 4 + 1024;                  // + alignment slack
+constexpr int OFF_XCH = (OFF_TP + (kMaxReqs + 1) * 2 + 15) / 16 * 16;  // [2][256] floats
+constexpr int SMEM_BYTES = OFF_XCH + 2 * 256 * 4 + 1024;              // + alignment slack
 constexpr int NSOFT = 256;  // softmax threads: two per q tile row
 constexpr int NTHREADS = NSOFT + 64;
 constexpr int PROD_WARP = NSOFT / 32, MMA_WARP = PROD_WARP + 1;
@@ -346,11 +349,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int b = (int)(npv & 1);
           const uint32_t bph = (uint32_t)(npv >> 1) & 1;
           const bool o_free = pj > 0 || pk == 0 || ptx::mbar_test_wait(sm.bar(B_O_EMPTY), (pk - 1) & 1);
-          if (o_free && ptx::mbar_test_wait(sm.bar(B_P_FULL + b), bph) &&
+          if (o_free && ptx::mbar_test_wait(sm.bar(B_P_FULL), (uint32_t)(npv & 1)) &&
               ptx::mbar_test_wait(sm.bar(B_FULL_V + s), (uint32_t)(npv / NST) & 1)) {
             ptx::tc_fence_after();
             const uint32_t vbase = sm.base_u32 + OFF_V + s * TILE_B;
-            const uint32_t pbase = sm.base_u32 + OFF_P + b * PTILE_B;
+            const uint32_t pbase = sm.base_u32 + OFF_P;
             // A = P, K-major (64 keys per 128-byte swizzled half); B = V read
             // MN-major (16 keys per MMA, d halves HALF_B apart)
 #pragma unroll
@@ -361,7 +364,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               ptx::tc_mma_f16(tmem + O_COL, da, db, IDESC_PV, pj > 0 || kk > 0);
             }
             ptx::tc_commit(sm.bar(B_O_FULL + b));
-            ptx::tc_commit(sm.bar(B_P_EMPTY + b));
+            ptx::tc_commit(sm.bar(B_P_EMPTY));
             ptx::tc_commit(sm.bar(B_EMPTY + s));
             ++npv;
             if (++pj == pit.nch) {
@@ -392,7 +395,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (npv > 0) {
         const long long L = npv - 1;
         drain_bar(sm.bar(B_EMPTY + (int)(L % NST)), (uint32_t)(L / NST) & 1);
-        drain_bar(sm.bar(B_P_EMPTY + (int)(L & 1)), (uint32_t)(L >> 1) & 1);
+        drain_bar(sm.bar(B_P_EMPTY), (uint32_t)(L & 1));
         drain_bar(sm.bar(B_O_FULL + (int)(L & 1)), (uint32_t)(L >> 1) & 1);
       }
     }
@@ -408,11 +411,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int hd = row % G;    // its query head within the KV head's group
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     float* xch = reinterpret_cast<float*>(sm.base + OFF_XCH);
+    int xe = 0;  // exchanges so far: they alternate between two buffers, so a
+                 // buffer is rewritten only after a later barrier, which the
+                 // partner passes after its read
     auto partner = [&](float v) -> float {
-      ptx::bar_sync_named(1, NSOFT);  // the previous exchange has been read
-      xch[tid] = v;
-      ptx::bar_sync_named(2, NSOFT);
-      return xch[tid ^ 128];
+      float* xb = xch + (xe++ & 1) * NSOFT;
+      xb[tid] = v;
+      ptx::bar_sync_named(1, NSOFT);
+      return xb[tid ^ 128];
     };
     long long ck = 0;
     for (long long i = blockIdx.x; i < total; i += gridDim.x) {
@@ -446,17 +452,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ptx::tmem_ld_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(sm.bar(B_S_EMPTY + b));
+        // every row of a full tile sees every key of a chunk that ends before
+        // the tile's first token: no mask (the common case on long contexts)
+        const bool whole = it.ntok == MQ && (j + 1) * CHK <= it.ctx + it.qt * MQ + 1;
         const int kl = lim - j * CHK - half * 64;  // visible keys among this thread's 64
-        float hm = -INFINITY;
+        float hm = -INFINITY;  // max of the raw logits (scale > 0)
+        if (whole) {
 #pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2)
+          for (int q2 = 0; q2 < 2; ++q2)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float x = (good && q2 * 32 + e < kl) ? sv[q2][e] * p.scale_log2 : -INFINITY;
-            sv[q2][e] = x;
-            hm = fmaxf(hm, x);
-          }
-        const float cm = fmaxf(hm, partner(hm));  // the row's chunk max, same in both
+            for (int e = 0; e < 32; ++e) hm = fmaxf(hm, sv[q2][e]);
+        } else {
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float x = (good && q2 * 32 + e < kl) ? sv[q2][e] : -INFINITY;
+              sv[q2][e] = x;
+              hm = fmaxf(hm, x);
+            }
+        }
+        // the row's chunk max in log2 units, the same in both threads
+        const float cm = fmaxf(hm, partner(hm)) * p.scale_log2;
         if (cm > m_ref + kRescaleLog2) {
           if (m_ref != -INFINITY) {
             // rescale this half of the row of O (earlier chunks): after their PV
@@ -482,7 +499,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         const float msafe = m_ref == -INFINITY ? 0.f : m_ref;
         // ---- P (and the V rows past the item's last key) ----
-        wait_bar(sm, sm.bar(B_P_EMPTY + b), bph ^ 1, p.err, 25);
+        wait_bar(sm, sm.bar(B_P_EMPTY), (uint32_t)(ck & 1) ^ 1, p.err, 25);
         if (j == it.nch - 1) {
           const int kc = it.kv_end - j * CHK;
           if (kc < CHK) {
@@ -499,23 +516,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
         // keys half * 64 ..: the row's 128-byte half `half` of the P tile
-        unsigned char* prow = sm.base + OFF_P + b * PTILE_B + half * HALF_B + row * 128;
+        unsigned char* prow = sm.base + OFF_P + half * HALF_B + row * 128;
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
           uint32_t w[4];
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) {
             const int e = (c8 & 3) * 8 + 2 * e2;
-            const __nv_bfloat162 pb = __floats2bfloat162_rn(fast_exp2(sv[c8 >> 2][e] - msafe),
-                                                            fast_exp2(sv[c8 >> 2][e + 1] - msafe));
-            l += __low2float(pb) + __high2float(pb);
+            // p = 2^(s * scale - m): one FMA per logit (masked logits are -inf)
+            const float p0 = fast_exp2(fmaf(sv[c8 >> 2][e], p.scale_log2, -msafe));
+            const float p1 = fast_exp2(fmaf(sv[c8 >> 2][e + 1], p.scale_log2, -msafe));
+            l += p0 + p1;  // before the bf16 rounding the MMA sees: within its error
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
             w[e2] = *reinterpret_cast<const uint32_t*>(&pb);
           }
           *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) =
               make_uint4(w[0], w[1], w[2], w[3]);
         }
         ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(sm.bar(B_P_FULL + b));
+        ptx::mbar_arrive(sm.bar(B_P_FULL));
       }
       // ---- epilogue: this half of the row of O after the item's last PV ----
       {
