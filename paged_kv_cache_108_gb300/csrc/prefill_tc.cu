@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto partner = [&](float v) -> float {
       float* xb = xch + (xe++ & 1) * NSOFT;
       xb[tid] = v;
-      ptx::bar_sync_named(1, NSOFT);
+      ptx::bar_sync_named(1 + (warp & 3), 64);  // warps w and w + 4 only
       return xb[tid ^ 128];
     };
     long long ck = 0;
@@ -456,12 +456,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // the tile's first token: no mask (the common case on long contexts)
         const bool whole = it.ntok == MQ && (j + 1) * CHK <= it.ctx + it.qt * MQ + 1;
         const int kl = lim - j * CHK - half * 64;  // visible keys among this thread's 64
-        float hm = -INFINITY;  // max of the raw logits (scale > 0)
+        // max of the raw logits (scale > 0), four independent chains
+        float hm4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (whole) {
 #pragma unroll
           for (int q2 = 0; q2 < 2; ++q2)
 #pragma unroll
-            for (int e = 0; e < 32; ++e) hm = fmaxf(hm, sv[q2][e]);
+            for (int e = 0; e < 32; ++e) hm4[e & 3] = fmaxf(hm4[e & 3], sv[q2][e]);
         } else {
 #pragma unroll
           for (int q2 = 0; q2 < 2; ++q2)
@@ -469,9 +470,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int e = 0; e < 32; ++e) {
               const float x = (good && q2 * 32 + e < kl) ? sv[q2][e] : -INFINITY;
               sv[q2][e] = x;
-              hm = fmaxf(hm, x);
+              hm4[e & 3] = fmaxf(hm4[e & 3], x);
             }
         }
+        const float hm = fmaxf(fmaxf(hm4[0], hm4[1]), fmaxf(hm4[2], hm4[3]));
         // the row's chunk max in log2 units, the same in both threads
         const float cm = fmaxf(hm, partner(hm)) * p.scale_log2;
         if (cm > m_ref + kRescaleLog2) {
@@ -517,6 +519,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         // keys half * 64 ..: the row's 128-byte half `half` of the P tile
         unsigned char* prow = sm.base + OFF_P + half * HALF_B + row * 128;
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};  // this chunk's sum, four chains
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
           uint32_t w[4];
@@ -526,13 +529,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // p = 2^(s * scale - m): one FMA per logit (masked logits are -inf)
             const float p0 = fast_exp2(fmaf(sv[c8 >> 2][e], p.scale_log2, -msafe));
             const float p1 = fast_exp2(fmaf(sv[c8 >> 2][e + 1], p.scale_log2, -msafe));
-            l += p0 + p1;  // before the bf16 rounding the MMA sees: within its error
+            l4[e2] += p0 + p1;  // before the bf16 rounding the MMA sees: within its error
             const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
             w[e2] = *reinterpret_cast<const uint32_t*>(&pb);
           }
           *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) =
               make_uint4(w[0], w[1], w[2], w[3]);
         }
+        l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(sm.bar(B_P_FULL));
       }
