@@ -32,10 +32,11 @@
 // so stale cache bytes never reach the result); V rows past the item's last
 // key are zeroed in smem.
 //
-// Warp roles (320 threads): warps 0-7 softmax and epilogue, two threads per
-// row (64 keys and 64 output columns each); warp 8 producer (q tile per
-// item, K/V chunks into a 2-stage ring); warp 9 TMEM allocation and the
-// MMA-issuing thread.  Items go to the persistent CTAs in turn; every
+// Warp roles (352 threads): warps 0-7 softmax and epilogue, two threads per
+// row (64 keys and 64 output columns each); warp 8 producer of the q tiles
+// and the K chunks (3-stage ring, a stage freed when its logits MMA
+// completes); warp 9 TMEM allocation and the MMA-issuing thread; warp 10
+// producer of the V chunks (2-stage ring, freed after the PV MMA).  Items go to the persistent CTAs in turn; every
 // role decodes the same item list.  Every mbarrier wait is bounded (error
 // word in the workspace, CTA aborted), as in the decode kernels.
 #include <cuda.h>
@@ -59,30 +60,33 @@ using tc::wait_bar;
 
 constexpr int D = 128;
 constexpr int CHK = 128;                  // keys per chunk
-constexpr int NST = 2;                    // K/V ring stages
+// K and V rings: a K chunk is free once its logits MMA completes, a V chunk
+// only after its PV MMA, so K runs one stage further ahead
+constexpr int NSTK = 3, NSTV = 2;
 constexpr int kMaxReqs = 256;
 constexpr int TILE_B = CHK * D * 2;       // one K or V chunk: 32 KiB
 constexpr int HALF_B = 128 * 128;         // one 64-column half of a 128-row tile
 constexpr int QTILE_B = 128 * D * 2;      // the q tile: 128 rows
 constexpr int PTILE_B = 128 * CHK * 2;    // P: 128 rows x 128 keys bf16
 constexpr int OFF_K = 0;
-constexpr int OFF_V = OFF_K + NST * TILE_B;
-constexpr int OFF_Q = OFF_V + NST * TILE_B;
+constexpr int OFF_V = OFF_K + NSTK * TILE_B;
+constexpr int OFF_Q = OFF_V + NSTV * TILE_B;
 constexpr int OFF_P = OFF_Q + QTILE_B;
 constexpr int OFF_BAR = OFF_P + PTILE_B;  // one P buffer (the softmax rarely waits for it)
-constexpr int B_FULL_K = 0, B_FULL_V = NST, B_EMPTY = 2 * NST, B_Q_FULL = 3 * NST,
+constexpr int B_FULL_K = 0, B_FULL_V = B_FULL_K + NSTK, B_EMPTY_K = B_FULL_V + NSTV,
+              B_EMPTY_V = B_EMPTY_K + NSTK, B_Q_FULL = B_EMPTY_V + NSTV,
               B_Q_EMPTY = B_Q_FULL + 1, B_S_FULL = B_Q_EMPTY + 1, B_S_EMPTY = B_S_FULL + 2,
-              B_P_FULL = B_S_EMPTY + 2, B_P_EMPTY = B_P_FULL + 2, B_O_FULL = B_P_EMPTY + 2,
+              B_P_FULL = B_S_EMPTY + 2, B_P_EMPTY = B_P_FULL + 1, B_O_FULL = B_P_EMPTY + 1,
               B_O_EMPTY = B_O_FULL + 2, NBARS = B_O_EMPTY + 1;
 constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 4;
 // tile prefix per request, [R+1]; 16 bits suffice: at most 65535 new tokens
 constexpr int OFF_TP = OFF_ABORT + 4;
-constexpr int OFF_XCH = (OFF_TP + (kMaxReqs + 1) * 2 + 15) / 16 * 16;  // [2][256] floats
-constexpr int SMEM_BYTES = OFF_XCH + 2 * 256 * 4 + 1024;              // + alignment slack
+constexpr int OFF_XCH = (OFF_TP + (kMaxReqs + 1) * 2 + 15) / 16 * 16;  // [256] floats
+constexpr int SMEM_BYTES = OFF_XCH + 256 * 4 + 1024;                  // + alignment slack
 constexpr int NSOFT = 256;  // softmax threads: two per q tile row
-constexpr int NTHREADS = NSOFT + 64;
-constexpr int PROD_WARP = NSOFT / 32, MMA_WARP = PROD_WARP + 1;
+constexpr int NTHREADS = NSOFT + 96;
+constexpr int PROD_WARP = NSOFT / 32, MMA_WARP = PROD_WARP + 1, VPROD_WARP = MMA_WARP + 1;
 constexpr int TMEM_COLS = 512;  // S[2] at 0 and 128, O at 256
 constexpr int S_COL = 0, O_COL = 256;
 constexpr float kRescaleLog2 = 8.f;
@@ -168,8 +172,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (tid == 0) {
     for (int i = 0; i < NBARS; ++i) {
       uint32_t cnt = 1;
-      if ((i >= B_S_EMPTY && i < B_S_EMPTY + 2) || (i >= B_P_FULL && i < B_P_FULL + 2) ||
-          i == B_O_EMPTY)
+      if ((i >= B_S_EMPTY && i < B_S_EMPTY + 2) || i == B_P_FULL || i == B_O_EMPTY)
         cnt = NSOFT;
       ptx::mbar_init(sm.bar(i), cnt);
     }
@@ -209,27 +212,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm.base + OFF_TMEM);
   const long long total = (long long)tp[R] * p.num_kv_heads;  // work items
 
-  if (warp == PROD_WARP) {
-    // ================= producer =================
+  if (warp == PROD_WARP || warp == VPROD_WARP) {
+    // ================= producers (K and the q tiles: warp 8; V: warp 10) ====
+    const bool isk = warp == PROD_WARP;
+    const int nst = isk ? NSTK : NSTV;
+    const uint32_t ring = sm.base_u32 + (isk ? OFF_K : OFF_V);
+    const void* tm = isk ? (const void*)&tm_k : (const void*)&tm_v;
+    const int b_full = isk ? B_FULL_K : B_FULL_V, b_empty = isk ? B_EMPTY_K : B_EMPTY_V;
     int qk = 0;        // items with chunks so far (q tile loads)
     long long ck = 0;  // chunks so far
     for (long long i = blockIdx.x; i < total; i += gridDim.x) {
       const Item it = item_of<G>(i, tp, R, p);
       if (it.nch == 0) continue;
-      if (qk > 0 && !wait_bar(sm, sm.bar(B_Q_EMPTY), (qk - 1) & 1, p.err, 21)) break;
-      if (lane == 0) {
-        // rows token * G + i: box {64 of d, G heads, MQ tokens} per half
-        const uint32_t dst = sm.base_u32 + OFF_Q;
-        const int row = it.q0 + it.qt * MQ;
-        ptx::mbar_arrive_expect_tx(sm.bar(B_Q_FULL), (uint32_t)QTILE_B);
-        ptx::tma_load_3d(dst, &tm_q, sm.bar(B_Q_FULL), 0, it.g * G, row);
-        ptx::tma_load_3d(dst + HALF_B, &tm_q, sm.bar(B_Q_FULL), 64, it.g * G, row);
+      if (isk) {
+        if (qk > 0 && !wait_bar(sm, sm.bar(B_Q_EMPTY), (qk - 1) & 1, p.err, 21)) break;
+        if (lane == 0) {
+          // rows token * G + i: box {64 of d, G heads, MQ tokens} per half
+          const uint32_t dst = sm.base_u32 + OFF_Q;
+          const int row = it.q0 + it.qt * MQ;
+          ptx::mbar_arrive_expect_tx(sm.bar(B_Q_FULL), (uint32_t)QTILE_B);
+          ptx::tma_load_3d(dst, &tm_q, sm.bar(B_Q_FULL), 0, it.g * G, row);
+          ptx::tma_load_3d(dst + HALF_B, &tm_q, sm.bar(B_Q_FULL), 64, it.g * G, row);
+        }
       }
       ++qk;
       bool ok = true;
       for (int j = 0; j < it.nch; ++j, ++ck) {
-        const int s = (int)(ck % NST);
-        const uint32_t ph = (uint32_t)(ck / NST) & 1;
+        const int s = (int)(ck % nst);
+        const uint32_t ph = (uint32_t)(ck / nst) & 1;
         const int keys = min(CHK, it.kv_end - j * CHK);
         const int nbox = (keys + p.box_tok - 1) >> p.log2_box;
         // the chunk's block ids, read while the stage drains
@@ -237,7 +247,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane < nbox)
           phys = __ldg(&p.block_tables[(int64_t)it.r * p.max_blocks +
                                        ((j * CHK + lane * p.box_tok) >> p.log2_bs)]);
-        if (!wait_bar(sm, sm.bar(B_EMPTY + s), ph ^ 1, p.err, 22)) {
+        if (!wait_bar(sm, sm.bar(b_empty + s), ph ^ 1, p.err, 22)) {
           ok = false;
           break;
         }
@@ -245,21 +255,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           atomicExch(p.err, 3);  // bad block id: load block 0 instead of faulting
           phys = 0;
         }
-        const uint32_t bytes = (uint32_t)nbox * p.box_tok * (uint32_t)(D * 2);
-        if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_K + s), bytes);
-          ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_V + s), bytes);
-        }
+        if (lane == 0)
+          ptx::mbar_arrive_expect_tx(sm.bar(b_full + s),
+                                     (uint32_t)nbox * p.box_tok * (uint32_t)(D * 2));
         __syncwarp();
         if (lane < nbox) {
-          const uint32_t row = (uint32_t)(lane * p.box_tok) * 128u;
+          const uint32_t dst = ring + s * TILE_B + (uint32_t)(lane * p.box_tok) * 128u;
           const int off = (j * CHK + lane * p.box_tok) & (p.block_size - 1);
-          const uint32_t kdst = sm.base_u32 + OFF_K + s * TILE_B + row;
-          const uint32_t vdst = sm.base_u32 + OFF_V + s * TILE_B + row;
-          ptx::tma_load_4d(kdst, &tm_k, sm.bar(B_FULL_K + s), 0, it.g, off, phys);
-          ptx::tma_load_4d(kdst + HALF_B, &tm_k, sm.bar(B_FULL_K + s), 64, it.g, off, phys);
-          ptx::tma_load_4d(vdst, &tm_v, sm.bar(B_FULL_V + s), 0, it.g, off, phys);
-          ptx::tma_load_4d(vdst + HALF_B, &tm_v, sm.bar(B_FULL_V + s), 64, it.g, off, phys);
+          ptx::tma_load_4d(dst, tm, sm.bar(b_full + s), 0, it.g, off, phys);
+          ptx::tma_load_4d(dst + HALF_B, tm, sm.bar(b_full + s), 64, it.g, off, phys);
         }
       }
       if (!ok) break;
@@ -267,11 +271,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // drain: the last loads issued must land before the CTA can exit
     __syncwarp();
     if (lane == 0) {
-      for (long long l = ck > NST ? ck - NST : 0; l < ck; ++l) {
-        drain_bar(sm.bar(B_FULL_K + (int)(l % NST)), (uint32_t)(l / NST) & 1);
-        drain_bar(sm.bar(B_FULL_V + (int)(l % NST)), (uint32_t)(l / NST) & 1);
-      }
-      if (qk > 0) drain_bar(sm.bar(B_Q_FULL), (qk - 1) & 1);
+      for (long long l = ck > nst ? ck - nst : 0; l < ck; ++l)
+        drain_bar(sm.bar(b_full + (int)(l % nst)), (uint32_t)(l / nst) & 1);
+      if (isk && qk > 0) drain_bar(sm.bar(B_Q_FULL), (qk - 1) & 1);
     }
   } else if (warp == MMA_WARP) {
     // ================= MMA issuer =================
@@ -317,9 +319,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             q_ready = true;
             progress = true;
           }
-          const int s = (int)(nq % NST);
+          const int s = (int)(nq % NSTK);
           const int b = (int)(nq & 1);
-          if (q_ready && ptx::mbar_test_wait(sm.bar(B_FULL_K + s), (uint32_t)(nq / NST) & 1) &&
+          if (q_ready && ptx::mbar_test_wait(sm.bar(B_FULL_K + s), (uint32_t)(nq / NSTK) & 1) &&
               ptx::mbar_test_wait(sm.bar(B_S_EMPTY + b), ((uint32_t)(nq >> 1) & 1) ^ 1)) {
             ptx::tc_fence_after();
             const uint32_t kbase = sm.base_u32 + OFF_K + s * TILE_B;
@@ -332,6 +334,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               ptx::tc_mma_f16(tmem + S_COL + CHK * b, da, db, IDESC_QK, kk > 0);
             }
             ptx::tc_commit(sm.bar(B_S_FULL + b));
+            ptx::tc_commit(sm.bar(B_EMPTY_K + s));  // the K chunk may be reloaded
             ++nq;
             if (++qj == qit.nch) {
               ptx::tc_commit(sm.bar(B_Q_EMPTY));  // the q tile may be reloaded
@@ -345,12 +348,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
         if (npv < nq) {
-          const int s = (int)(npv % NST);
+          const int s = (int)(npv % NSTV);
           const int b = (int)(npv & 1);
           const uint32_t bph = (uint32_t)(npv >> 1) & 1;
           const bool o_free = pj > 0 || pk == 0 || ptx::mbar_test_wait(sm.bar(B_O_EMPTY), (pk - 1) & 1);
           if (o_free && ptx::mbar_test_wait(sm.bar(B_P_FULL), (uint32_t)(npv & 1)) &&
-              ptx::mbar_test_wait(sm.bar(B_FULL_V + s), (uint32_t)(npv / NST) & 1)) {
+              ptx::mbar_test_wait(sm.bar(B_FULL_V + s), (uint32_t)(npv / NSTV) & 1)) {
             ptx::tc_fence_after();
             const uint32_t vbase = sm.base_u32 + OFF_V + s * TILE_B;
             const uint32_t pbase = sm.base_u32 + OFF_P;
@@ -365,7 +368,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             ptx::tc_commit(sm.bar(B_O_FULL + b));
             ptx::tc_commit(sm.bar(B_P_EMPTY));
-            ptx::tc_commit(sm.bar(B_EMPTY + s));
+            ptx::tc_commit(sm.bar(B_EMPTY_V + s));
             ++npv;
             if (++pj == pit.nch) {
               pj = 0;
@@ -390,11 +393,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       // drain: every commit this thread issued must land before exit
-      if (nq > 0) drain_bar(sm.bar(B_S_FULL + (int)((nq - 1) & 1)), (uint32_t)((nq - 1) >> 1) & 1);
+      if (nq > 0) {
+        drain_bar(sm.bar(B_S_FULL + (int)((nq - 1) & 1)), (uint32_t)((nq - 1) >> 1) & 1);
+        drain_bar(sm.bar(B_EMPTY_K + (int)((nq - 1) % NSTK)), (uint32_t)((nq - 1) / NSTK) & 1);
+      }
       if (qk > 0) drain_bar(sm.bar(B_Q_EMPTY), (qk - 1) & 1);
       if (npv > 0) {
         const long long L = npv - 1;
-        drain_bar(sm.bar(B_EMPTY + (int)(L % NST)), (uint32_t)(L / NST) & 1);
+        drain_bar(sm.bar(B_EMPTY_V + (int)(L % NSTV)), (uint32_t)(L / NSTV) & 1);
         drain_bar(sm.bar(B_P_EMPTY), (uint32_t)(L & 1));
         drain_bar(sm.bar(B_O_FULL + (int)(L & 1)), (uint32_t)(L >> 1) & 1);
       }
@@ -411,14 +417,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int hd = row % G;    // its query head within the KV head's group
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     float* xch = reinterpret_cast<float*>(sm.base + OFF_XCH);
-    int xe = 0;  // exchanges so far: they alternate between two buffers, so a
-                 // buffer is rewritten only after a later barrier, which the
-                 // partner passes after its read
+    // warps w and w + 4 only: the first barrier keeps a slot from being
+    // rewritten before the partner has read the previous value
     auto partner = [&](float v) -> float {
-      float* xb = xch + (xe++ & 1) * NSOFT;
-      xb[tid] = v;
-      ptx::bar_sync_named(1 + (warp & 3), 64);  // warps w and w + 4 only
-      return xb[tid ^ 128];
+      ptx::bar_sync_named(1 + (warp & 3), 64);
+      xch[tid] = v;
+      ptx::bar_sync_named(5 + (warp & 3), 64);
+      return xch[tid ^ 128];
     };
     long long ck = 0;
     for (long long i = blockIdx.x; i < total; i += gridDim.x) {
@@ -440,8 +445,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int j = 0; j < it.nch; ++j, ++ck) {
         const int b = (int)(ck & 1);
         const uint32_t bph = (uint32_t)(ck >> 1) & 1;
-        const int s = (int)(ck % NST);
-        const uint32_t ph = (uint32_t)(ck / NST) & 1;
+        const int s = (int)(ck % NSTV);  // the V stage of this chunk
+        const uint32_t ph = (uint32_t)(ck / NSTV) & 1;
         // ---- this thread's 64 logits of the row ----
         float sv[2][32];
         good = wait_bar(sm, sm.bar(B_S_FULL + b), bph, p.err, 23) && good;
