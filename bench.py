@@ -133,6 +133,14 @@ def build_workload(name, block_size, kv_dtype):
     return w, unique
 
 
+def causal_pairs(context_lens, new_tokens) -> int:
+    """(new token, visible key) pairs of a step in which every sequence adds
+    its last ``new_tokens`` positions: token j of a sequence of n sees the
+    n - T + j + 1 keys up to and including itself."""
+    T = int(new_tokens)
+    return sum(int(n - T) * T + T * (T + 1) // 2 for n in context_lens)
+
+
 class Step:
     """Device-resident state of one decode step of a workload."""
 
@@ -223,9 +231,8 @@ class Step:
     # causal attention flops of one step: per query head, 4 d per visible
     # (new token, key) pair -- the tensor-core prefill tiles' algorithmic work
     def decode_flops(self) -> float:
-        w, T = self.w, self.new_tokens
-        pairs = sum(int(n - T) * T + T * (T + 1) // 2 for n in w.context_lens)
-        return 4.0 * w.head_dim * w.num_heads * pairs
+        w = self.w
+        return 4.0 * w.head_dim * w.num_heads * causal_pairs(w.context_lens, self.new_tokens)
 
     def write_bytes(self) -> int:
         w = self.w
