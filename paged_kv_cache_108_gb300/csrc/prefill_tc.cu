@@ -36,9 +36,12 @@
 // row (64 keys and 64 output columns each); warp 8 producer of the q tiles
 // and the K chunks (3-stage ring, a stage freed when its logits MMA
 // completes); warp 9 TMEM allocation and the MMA-issuing thread; warp 10
-// producer of the V chunks (2-stage ring, freed after the PV MMA).  Items go to the persistent CTAs in turn; every
-// role decodes the same item list.  Every mbarrier wait is bounded (error
-// word in the workspace, CTA aborted), as in the decode kernels.
+// producer of the V chunks (2-stage ring, freed after the PV MMA).  The K
+// producer takes work items from a counter in the workspace (word 1, zeroed
+// by the host before the launch) and publishes them through a 4-slot ring
+// to the other roles, so a CTA that drew short items takes more of them.
+// Every mbarrier wait is bounded (error word in the workspace, CTA
+// aborted), as in the decode kernels.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -77,11 +80,14 @@ constexpr int B_FULL_K = 0, B_FULL_V = B_FULL_K + NSTK, B_EMPTY_K = B_FULL_V + N
               B_EMPTY_V = B_EMPTY_K + NSTK, B_Q_FULL = B_EMPTY_V + NSTV,
               B_Q_EMPTY = B_Q_FULL + 1, B_S_FULL = B_Q_EMPTY + 1, B_S_EMPTY = B_S_FULL + 2,
               B_P_FULL = B_S_EMPTY + 2, B_P_EMPTY = B_P_FULL + 1, B_O_FULL = B_P_EMPTY + 1,
-              B_O_EMPTY = B_O_FULL + 2, NBARS = B_O_EMPTY + 1;
+              B_O_EMPTY = B_O_FULL + 2, B_ITEM_FULL = B_O_EMPTY + 1,
+              B_ITEM_EMPTY = B_ITEM_FULL + 4, NBARS = B_ITEM_EMPTY + 4;
+constexpr int NRING = 4;  // work items published ahead by the K producer
 constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 4;
 // tile prefix per request, [R+1]; 16 bits suffice: at most 65535 new tokens
-constexpr int OFF_TP = OFF_ABORT + 4;
+constexpr int OFF_RING = OFF_ABORT + 4;  // [NRING] item indices
+constexpr int OFF_TP = OFF_RING + NRING * 4;
 constexpr int OFF_XCH = (OFF_TP + (kMaxReqs + 1) * 2 + 15) / 16 * 16;  // [256] floats
 constexpr int SMEM_BYTES = OFF_XCH + 256 * 4 + 1024;                  // + alignment slack
 constexpr int NSOFT = 256;  // softmax threads: two per q tile row
@@ -99,6 +105,7 @@ struct Params {
   const int32_t* seq_lens;      // [R]
   const int32_t* qsl;           // [R + 1]
   int* err;                     // workspace word 0
+  unsigned* next_item;          // workspace word 1: items handed out (zeroed before launch)
   int num_seqs, num_tokens, num_heads, num_kv_heads, max_blocks, num_blocks, block_size, log2_bs;
   int box_tok, log2_box;
   float scale_log2;
@@ -174,6 +181,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       uint32_t cnt = 1;
       if ((i >= B_S_EMPTY && i < B_S_EMPTY + 2) || i == B_P_FULL || i == B_O_EMPTY)
         cnt = NSOFT;
+      // an item slot is read by the V producer, the MMA thread and the 8
+      // softmax warps (one arrival each)
+      if (i >= B_ITEM_EMPTY && i < B_ITEM_EMPTY + NRING) cnt = 2 + NSOFT / 32;
       ptx::mbar_init(sm.bar(i), cnt);
     }
     *sm.abort_flag() = 0;
@@ -211,6 +221,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm.base + OFF_TMEM);
   const long long total = (long long)tp[R] * p.num_kv_heads;  // work items
+  // Items are handed out dynamically (a counter in the workspace): the K
+  // producer takes the next index and publishes it in a ring slot; the
+  // other roles read the slots in order.  An index >= total ends the CTA.
+  volatile int* ring_s = reinterpret_cast<volatile int*>(sm.base + OFF_RING);
+  auto read_item = [&](int k, bool arrive_lane0) -> long long {
+    const int slot = k & (NRING - 1);
+    if (!wait_bar(sm, sm.bar(B_ITEM_FULL + slot), (uint32_t)(k / NRING) & 1, p.err, 30))
+      return total;
+    const long long i = ring_s[slot];
+    __syncwarp();
+    if (arrive_lane0) ptx::mbar_arrive(sm.bar(B_ITEM_EMPTY + slot));
+    return i;
+  };
 
   if (warp == PROD_WARP || warp == VPROD_WARP) {
     // ================= producers (K and the q tiles: warp 8; V: warp 10) ====
@@ -221,7 +244,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int b_full = isk ? B_FULL_K : B_FULL_V, b_empty = isk ? B_EMPTY_K : B_EMPTY_V;
     int qk = 0;        // items with chunks so far (q tile loads)
     long long ck = 0;  // chunks so far
-    for (long long i = blockIdx.x; i < total; i += gridDim.x) {
+    for (int k = 0;; ++k) {
+      long long i;
+      if (isk) {
+        // publish the next item (after every reader has taken the slot's last one)
+        const int slot = k & (NRING - 1);
+        if (!wait_bar(sm, sm.bar(B_ITEM_EMPTY + slot), ((uint32_t)(k / NRING) & 1) ^ 1, p.err,
+                      29))
+          break;
+        long long got = 0;
+        if (lane == 0) {
+          got = atomicAdd(p.next_item, 1u);
+          ring_s[slot] = (int)(got < total ? got : total);
+          ptx::mbar_arrive(sm.bar(B_ITEM_FULL + slot));
+        }
+        i = __shfl_sync(0xffffffffu, got, 0);
+      } else {
+        i = read_item(k, lane == 0);
+      }
+      if (i >= total) break;
       const Item it = item_of<G>(i, tp, R, p);
       if (it.nch == 0) continue;
       if (isk) {
@@ -285,36 +326,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32_ab(128, CHK, false, false);
       constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32_ab(128, D, false, true);
       const uint32_t qbase = sm.base_u32 + OFF_Q;
-      // QK cursor
-      long long qi = blockIdx.x;  // item
+      // QK cursor: pulls items from the ring; the PV cursor follows through a
+      // short local queue (it lags by at most the chunks in flight)
+      constexpr int NQUEUE = 8;
+      Item queue[NQUEUE];
+      int kr = 0;          // ring slots read
+      bool ring_done = false, have_q = false;
       Item qit{};
       int qj = 0, qk = 0;  // chunk in item, items with chunks so far
       bool q_ready = false;
-      auto next_q_item = [&]() {
-        while (qi < total) {
-          qit = item_of<G>(qi, tp, R, p);
-          if (qit.nch > 0) return;
-          qi += gridDim.x;
-        }
-      };
-      next_q_item();
-      // PV cursor
-      long long pi = blockIdx.x;
       Item pit{};
       int pj = 0, pk = 0;
-      auto next_p_item = [&]() {
-        while (pi < total) {
-          pit = item_of<G>(pi, tp, R, p);
-          if (pit.nch > 0) return;
-          pi += gridDim.x;
-        }
-      };
-      next_p_item();
       long long nq = 0, npv = 0;
       long long t_idle = clock64();
       while (true) {
         bool progress = false;
-        if (qi < total) {
+        if (!have_q && !ring_done) {
+          const int slot = kr & (NRING - 1);
+          if (ptx::mbar_test_wait(sm.bar(B_ITEM_FULL + slot), (uint32_t)(kr / NRING) & 1)) {
+            const long long i = ring_s[slot];
+            ptx::mbar_arrive(sm.bar(B_ITEM_EMPTY + slot));
+            ++kr;
+            if (i >= total) {
+              ring_done = true;
+            } else {
+              const Item it = item_of<G>(i, tp, R, p);
+              if (it.nch > 0) {
+                qit = it;
+                queue[qk % NQUEUE] = it;
+                have_q = true;
+                qj = 0;
+                q_ready = false;
+              }
+            }
+            progress = true;
+          }
+        }
+        if (have_q) {
           if (qj == 0 && !q_ready && ptx::mbar_test_wait(sm.bar(B_Q_FULL), qk & 1)) {
             q_ready = true;
             progress = true;
@@ -341,13 +389,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               qj = 0;
               ++qk;
               q_ready = false;
-              qi += gridDim.x;
-              next_q_item();
+              have_q = false;
             }
             progress = true;
           }
         }
         if (npv < nq) {
+          pit = queue[pk % NQUEUE];
           const int s = (int)(npv % NSTV);
           const int b = (int)(npv & 1);
           const uint32_t bph = (uint32_t)(npv >> 1) & 1;
@@ -373,12 +421,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (++pj == pit.nch) {
               pj = 0;
               ++pk;
-              pi += gridDim.x;
-              next_p_item();
             }
             progress = true;
           }
-        } else if (qi >= total) {
+        } else if (ring_done && !have_q) {
           break;
         }
         if (progress) {
@@ -426,7 +472,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       return xch[tid ^ 128];
     };
     long long ck = 0;
-    for (long long i = blockIdx.x; i < total; i += gridDim.x) {
+    for (int k = 0;; ++k) {
+      const long long i = read_item(k, lane == 0);
+      if (i >= total) break;
       const Item it = item_of<G>(i, tp, R, p);
       const int rt = it.qt * MQ + tok;  // the row's token within the request
       const bool row_ok = tok < it.ntok;
@@ -665,6 +713,10 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream) {
   prm.seq_lens = a.seq_lens;
   prm.qsl = a.query_start_loc;
   prm.err = static_cast<int*>(a.workspace);
+  prm.next_item = reinterpret_cast<unsigned*>(static_cast<char*>(a.workspace) + 4);
+  // the item counter starts at zero for every launch (a memset node when captured)
+  cudaError_t ez = cudaMemsetAsync(prm.next_item, 0, sizeof(unsigned), stream);
+  if (ez != cudaSuccess) return ez;
   prm.num_seqs = a.num_seqs;
   prm.num_tokens = a.num_tokens;
   prm.num_heads = a.num_heads;
