@@ -328,7 +328,9 @@ pa_status pa_varlen_attention(void* out, const void* q, const void* k_cache, con
  *            block_size >= 8, at most 256 requests and scale > 0, else
  *            PA_ERR_UNSUPPORTED.  Sets workspace word 0 (int32) to a nonzero
  *            code if a bounded internal wait expired or a block id was out of
- *            range; the library never clears it.
+ *            range; the library never clears it.  Workspace word 1 is the
+ *            tiles' work counter, zeroed on `stream` before each launch (an
+ *            asynchronous memset, captured with the kernel in a graph).
  *  method 0: method 2 where it applies and the step adds at least 16 new
  *            tokens per request on average, else method 1.
  *  Other arguments as pa_varlen_attention.
