@@ -32,9 +32,10 @@
 // of the CTA that computed it -- slot 0 for the unit its range ends in, slot
 // 1 for the unit it starts in -- and the last piece to arrive merges.  The
 // merge warp merges pieces finished while the CTA still has work; a CTA's
-// final piece is merged by its softmax warps, straight from registers when
-// every other piece has already arrived (the usual case: neighbours take
-// their shared units first).
+// final piece is merged by its softmax warps, without counting when every
+// other piece has already arrived (the usual case: neighbours take their
+// shared units first).  Both read all pieces from the slots in CTA order
+// with the same roundings, so the output does not depend on who merges.
 //
 // Warp roles (256 threads):
 //   warps 0-3  softmax + epilogue: thread t owns TMEM lane t (row t of the
