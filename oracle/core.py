@@ -11,6 +11,9 @@ marshals numpy arrays, and checks return codes.  Definitions followed:
 * decode       -- "Paged KV cache", ``PagedKVCache.gather`` + ``paged_attention``
   restricted to one query token per sequence: gather through the block table,
   then softmax(scale * q K^T) V with the GQA map h -> h // G.
+* varlen       -- ``orc_varlen``, wrapped by ``oracle/varlen.py``: "Paged KV
+  cache", section "Paged attention" (several new tokens per request, each
+  seeing the context up to its own position).
 * E4M3         -- the OCP 8-bit floating point specification (E4M3, bias 7,
   max 448, NaN S.1111.111), round-to-nearest-even, saturating.
 """
@@ -75,6 +78,9 @@ def _load():
                                        i32, P, i32, i32, f64, f64, f64, P, i32,
                                        i32]
             lib.orc_decode.restype = ctypes.c_int
+            lib.orc_varlen.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P,
+                                       i32, P, P, i32, i32, f64, f64, f64, i32]
+            lib.orc_varlen.restype = ctypes.c_int
             _lib = lib
     return _lib
 

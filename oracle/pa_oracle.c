@@ -33,8 +33,18 @@
  *    llm-stack-book §4.6, section "The PagedAttention Kernel" (the math is
  *    unchanged; the block table is only an indirection).  n == 0 gives a
  *    zero output row (a reading: the pages are silent).
+ *  - Varlen causal attention (several new tokens per request: multi-token
+ *    decode, chunked and full prefill).  "Paged KV cache", section "Paged
+ *    attention": request r's new tokens are queries qsl[r]..qsl[r+1]-1 and
+ *    are the last num_new of its seq_len context tokens, so new token j sits
+ *    at position seq_len - num_new + j and attends to positions 0 through
+ *    that one.  Per (request, KV head): gather the request's rows through its
+ *    block table, then for each new token and each query head of the group
+ *    a textbook softmax over the visible positions.  A request whose
+ *    num_new exceeds seq_len has no valid position for its first tokens; its
+ *    rows are defined as zero (a reading: the pages are silent).
  *
- * No online softmax, no partitions, no blocking: the decode is the plain
+ * No online softmax, no partitions, no blocking: each result is the plain
  * definition, written so it can be read against the pages.
  */
 #include <math.h>
@@ -317,5 +327,158 @@ int orc_decode(double* out, const uint16_t* q, const void* k_cache,
     free(th); free(ws);
   }
   free(all);
+  return status;
+}
+
+/* ---- varlen causal attention --------------------------------------------- */
+
+typedef struct {
+  double* out;                 /* [N, H_q, d] fp64, N = qsl[num_reqs] */
+  const uint16_t* q;           /* [N, H_q, d] bf16 */
+  const void* k_cache;         /* [num_blocks, B, H_kv, d] */
+  const void* v_cache;
+  int32_t num_blocks, block_size, num_kv_heads, head_dim, kv_dtype;
+  const int32_t* block_tables; /* [num_reqs, max_blocks] */
+  int32_t max_blocks;
+  const int32_t* seq_lens;     /* [num_reqs] context tokens after the step */
+  const int32_t* qsl;          /* [num_reqs + 1] query start locations */
+  int32_t num_reqs, num_heads;
+  double scale, k_scale, v_scale;
+} orc_varlen_args;
+
+static double varlen_elem(const orc_varlen_args* a, const void* cache,
+                          int64_t idx, double kv_scale) {
+  if (a->kv_dtype == ORC_KV_BF16)
+    return orc_bf16_to_double(((const uint16_t*)cache)[idx]);
+  return orc_e4m3_to_double(((const uint8_t*)cache)[idx]) * kv_scale;
+}
+
+/* One (request, KV head g) unit.  Returns 0, -1 on a bad id / length, -2 on
+ * host OOM. */
+static int varlen_unit(const orc_varlen_args* a, int32_t r, int32_t g) {
+  const int32_t H = a->num_heads, Hkv = a->num_kv_heads, d = a->head_dim;
+  const int32_t B = a->block_size, G = H / Hkv;
+  const int32_t first = a->qsl[r], num_new = a->qsl[r + 1] - a->qsl[r];
+  const int32_t seq_len = a->seq_lens[r];
+  if (num_new < 0 || seq_len < 0) return -1;
+  if (num_new == 0) return 0;
+  if (num_new > seq_len) { /* no valid position for the first tokens */
+    for (int32_t j = 0; j < num_new; ++j)
+      for (int32_t i = 0; i < G; ++i)
+        memset(a->out + (((int64_t)first + j) * H + (int64_t)g * G + i) * d, 0,
+               sizeof(double) * (size_t)d);
+    return 0;
+  }
+  if ((int64_t)seq_len > (int64_t)a->max_blocks * B) return -1;
+
+  /* gather the context rows of KV head g, widening only what is read */
+  double* K = (double*)malloc(sizeof(double) * (size_t)seq_len * d);
+  double* V = (double*)malloc(sizeof(double) * (size_t)seq_len * d);
+  double* w = (double*)malloc(sizeof(double) * (size_t)seq_len);
+  if (!K || !V || !w) {
+    free(K); free(V); free(w);
+    return -2;
+  }
+  const int32_t* table = a->block_tables + (int64_t)r * a->max_blocks;
+  for (int32_t t = 0; t < seq_len; ++t) {
+    int32_t phys = table[t / B];
+    if (phys < 0 || phys >= a->num_blocks) {
+      free(K); free(V); free(w);
+      return -1;
+    }
+    int64_t base = (((int64_t)phys * B + (t % B)) * Hkv + g) * d;
+    for (int32_t e = 0; e < d; ++e) {
+      K[(int64_t)t * d + e] = varlen_elem(a, a->k_cache, base + e, a->k_scale);
+      V[(int64_t)t * d + e] = varlen_elem(a, a->v_cache, base + e, a->v_scale);
+    }
+  }
+
+  for (int32_t j = 0; j < num_new; ++j) {
+    const int32_t last = seq_len - num_new + j; /* its own position */
+    for (int32_t i = 0; i < G; ++i) {
+      const int32_t h = g * G + i;
+      const uint16_t* qh = a->q + (((int64_t)first + j) * H + h) * d;
+      double top = -INFINITY;
+      for (int32_t t = 0; t <= last; ++t) {
+        double dot = 0.0;
+        for (int32_t e = 0; e < d; ++e)
+          dot += orc_bf16_to_double(qh[e]) * K[(int64_t)t * d + e];
+        w[t] = a->scale * dot;
+        if (w[t] > top) top = w[t];
+      }
+      double sum = 0.0;
+      for (int32_t t = 0; t <= last; ++t) {
+        w[t] = exp(w[t] - top);
+        sum += w[t];
+      }
+      double* o = a->out + (((int64_t)first + j) * H + h) * d;
+      for (int32_t e = 0; e < d; ++e) {
+        double acc = 0.0;
+        for (int32_t t = 0; t <= last; ++t) acc += w[t] * V[(int64_t)t * d + e];
+        o[e] = acc / sum;
+      }
+    }
+  }
+  free(K); free(V); free(w);
+  return 0;
+}
+
+typedef struct {
+  const orc_varlen_args* a;
+  int32_t n_units, stride, first;
+  int status;
+} orc_varlen_worker;
+
+static void* varlen_worker_main(void* p) {
+  orc_varlen_worker* w = (orc_varlen_worker*)p;
+  const int32_t Hkv = w->a->num_kv_heads;
+  for (int32_t u = w->first; u < w->n_units; u += w->stride) {
+    int st = varlen_unit(w->a, u / Hkv, u % Hkv);
+    if (st != 0) w->status = st;
+  }
+  return NULL;
+}
+
+/* Every (request, KV head) unit; nthreads > 1 spreads the same per-unit
+ * function over POSIX threads (results do not depend on it).  Returns 0, -1
+ * on a bad id, length or head count, -2 on host OOM. */
+int orc_varlen(double* out, const uint16_t* q, const void* k_cache,
+               const void* v_cache, int32_t num_blocks, int32_t block_size,
+               int32_t num_kv_heads, int32_t head_dim, int32_t kv_dtype,
+               const int32_t* block_tables, int32_t max_blocks,
+               const int32_t* seq_lens, const int32_t* qsl, int32_t num_reqs,
+               int32_t num_heads, double scale, double k_scale,
+               double v_scale, int32_t nthreads) {
+  if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || num_reqs < 0)
+    return -1;
+  orc_varlen_args a = {out, q, k_cache, v_cache, num_blocks, block_size,
+                       num_kv_heads, head_dim, kv_dtype, block_tables,
+                       max_blocks, seq_lens, qsl, num_reqs, num_heads,
+                       scale, k_scale, v_scale};
+  const int32_t n_units = num_reqs * num_kv_heads;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > n_units) nthreads = n_units > 0 ? n_units : 1;
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  orc_varlen_worker* ws =
+      (orc_varlen_worker*)malloc(sizeof(orc_varlen_worker) * (size_t)nthreads);
+  if (!th || !ws) {
+    free(th); free(ws);
+    return -2;
+  }
+  int status = 0;
+  for (int32_t t = 0; t < nthreads; ++t) {
+    ws[t].a = &a; ws[t].n_units = n_units; ws[t].stride = nthreads;
+    ws[t].first = t; ws[t].status = 0;
+  }
+  if (nthreads == 1) {
+    varlen_worker_main(&ws[0]);
+  } else {
+    for (int32_t t = 0; t < nthreads; ++t)
+      pthread_create(&th[t], NULL, varlen_worker_main, &ws[t]);
+    for (int32_t t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+  }
+  for (int32_t t = 0; t < nthreads; ++t)
+    if (ws[t].status != 0) status = ws[t].status;
+  free(th); free(ws);
   return status;
 }

@@ -1,39 +1,47 @@
 """Pure-Python model of the block pool and block tables -- TEST INFRASTRUCTURE.
 
-Followed definitions:
+Only tests, the smoke check and the benchmark's CPU legs use this module.
 
-* Free queue and ref counts: "Paged KV cache" (ai-infra-handbooks), class
-  ``BlockPool`` -- a FIFO queue of free ids initialised 0..n-1, allocation
-  takes from the head and is all-or-nothing (returns None when short), a free
-  decrements each ref count and appends blocks that reach zero to the tail.
-* Per-sequence tables, growth and slots: "4.6 PagedAttention & KV-Cache
-  Memory Management" (llm-stack-book), class ``BlockManager`` -- allocate
-  ceil(n/B) blocks for a prompt, grow by one block exactly when the position
-  about to be written is a multiple of B, slot = table[p // B] * B + p % B.
-* Fork and copy-on-write: same page, section "Copy-on-write for shared
-  prefixes" -- fork copies the table and increments every ref count; before a
-  write into a block with ref count > 1 a fresh block is taken, the old ref
-  count is decremented, the table entry is remapped, and (src, dst) is
-  reported for a device copy; with ref count 1 the write goes in place.
+The rules it states, and where the pages give them:
 
+* Pool ("Paged KV cache" (ai-infra-handbooks), section "Implementation",
+  the block pool; its doctest under "Block tables and slot mapping"):
+  R1  every block id starts free; the free ids wait in one queue, in the
+      order 0..n-1 unless a start order is given;
+  R2  a request for n blocks is granted only whole: with fewer than n free it
+      is refused and nothing changes; otherwise the n ids at the front of the
+      queue leave it, in queue order, each with exactly one holder;
+  R3  a release takes one holder from each listed block; a block left with no
+      holder joins the back of the queue.
+* Tables and growth ("4.6 PagedAttention & KV-Cache Memory Management"
+  (llm-stack-book), section "Block Tables, the Allocator & Copy-on-Write"):
+  a prompt of n tokens takes ceil(n / B) blocks; a sequence takes one more
+  block exactly when the position about to be written is a multiple of B;
+  position p lives at slot table[p // B] * B + p % B.
+* Fork and copy-on-write (same page, section "Copy-on-write for shared
+  prefixes"): a fork shares every block (one more holder each); a write
+  into a block that has other holders first moves the writer to a fresh
+  block (R2 with n = 1), drops the writer's hold on the old one, and reports
+  (old, new) so the device copies the contents; a block with one holder is
+  written where it is.
 * Prefix caching across requests (``PrefixCachePoolModel``): "Paged KV
-  cache" (ai-infra-handbooks), copy-on-write exercise -- vLLM V1 shares only
-  full blocks and every answer starts writing in its own block; "4.6
-  PagedAttention & KV-Cache Memory Management", section "Copy-on-write for
-  shared prefixes" -- the same machinery generalises to reuse across
-  requests.  The pages do not say how a block is recognised; the reading
-  taken: a full block is the content (parent block, parent generation, its
-  B tokens), a generation advances whenever a block is handed out fresh (its
-  entry dies with it), freed cached blocks wait in the free queue and leave it
-  when matched.  Kept as plain dictionaries keyed by that tuple.
+  cache", Exercises (the copy-on-write answer: vLLM V1 shares only full
+  blocks, so every request writes in a block of its own); "4.6 ...",
+  section "Copy-on-write for shared prefixes" (the same sharing serves
+  requests that repeat a prompt).  The pages do not say how a full block is
+  recognised.  Reading taken: a full block's identity is (its parent block,
+  the parent's generation, its B token ids), with parent -1 for a prompt's
+  first block; a block's generation grows each time it is handed out fresh,
+  which also forgets its identity; a cached block whose holders are all gone
+  stays in the free queue, keeps its identity, and leaves the queue from
+  wherever it sits when a later prompt matches it.
 
-Readings where the pages differ: FIFO (the handbook's deque and its printed
-``[5, 6, 7, 0]`` example) rather than the llm-stack-book's ``pop()`` from the
-end; all-or-nothing allocation instead of raising after a partial pop.
+Readings where the pages disagree: the queue is first-in first-out (the
+handbook's printed ``[5, 6, 7, 0]``), not the llm-stack-book's take from the
+end; a short pool refuses the whole request instead of raising after a
+partial hand-out.
 """
 from __future__ import annotations
-
-from collections import deque
 
 
 class PoolExhausted(Exception):
@@ -41,45 +49,57 @@ class PoolExhausted(Exception):
 
 
 class BlockPoolModel:
+    """Rules R1-R3 plus fork (``incref``) and copy-on-write (``cow``)."""
+
     def __init__(self, num_blocks: int, free_order=None):
         self.num_blocks = num_blocks
-        self.ref_cnt = [0] * num_blocks
-        order = range(num_blocks) if free_order is None else free_order
-        self.free_queue = deque(order)
+        start = list(range(num_blocks)) if free_order is None else [int(b) for b in free_order]
+        if sorted(start) != list(range(num_blocks)):
+            raise ValueError("the start order must list every block once")
+        self._waiting = start                   # R1: front of the queue first
+        self._holders = [0] * num_blocks
 
+    # -- queries
     def num_free(self) -> int:
-        return len(self.free_queue)
+        return len(self._waiting)
 
     def refcount(self, blk: int) -> int:
-        return self.ref_cnt[blk]
+        return self._holders[blk]
+
+    def free_order(self):
+        return list(self._waiting)
+
+    # -- R2
+    def _take_front(self, n: int):
+        granted, self._waiting = self._waiting[:n], self._waiting[n:]
+        for b in granted:
+            self._holders[b] = 1
+        return granted
 
     def allocate(self, n: int):
-        if n > len(self.free_queue):
-            return None
-        blocks = [self.free_queue.popleft() for _ in range(n)]
+        """n blocks from the front of the queue, or None (and no change)."""
+        return self._take_front(n) if n <= len(self._waiting) else None
+
+    # -- R3 and fork
+    def free(self, blocks) -> None:
         for b in blocks:
-            self.ref_cnt[b] = 1
-        return blocks
+            self._holders[b] -= 1
+            if not self._holders[b]:
+                self._waiting.append(b)
 
     def incref(self, blocks) -> None:
         for b in blocks:
-            self.ref_cnt[b] += 1
-
-    def free(self, blocks) -> None:
-        for b in blocks:
-            self.ref_cnt[b] -= 1
-            if self.ref_cnt[b] == 0:
-                self.free_queue.append(b)
+            self._holders[b] += 1
 
     def cow(self, blk: int):
-        """(src, dst) for a write into ``blk``; dst == src when private."""
-        if self.ref_cnt[blk] == 1:
+        """(src, dst) for a write into ``blk``; dst == src when unshared."""
+        if self._holders[blk] == 1:
             return blk, blk
-        new = self.allocate(1)
-        if new is None:
+        fresh = self.allocate(1)
+        if fresh is None:
             raise PoolExhausted("no free block for copy-on-write")
-        self.ref_cnt[blk] -= 1
-        return blk, new[0]
+        self._holders[blk] -= 1
+        return blk, fresh[0]
 
 
 def slot_of(table, pos: int, block_size: int) -> int:
@@ -88,7 +108,7 @@ def slot_of(table, pos: int, block_size: int) -> int:
 
 
 class SequenceTablesModel:
-    """Sequence-level bookkeeping on top of ``BlockPoolModel``."""
+    """Per-sequence block tables kept on top of a ``BlockPoolModel``."""
 
     def __init__(self, pool: BlockPoolModel, block_size: int):
         self.pool = pool
@@ -96,29 +116,30 @@ class SequenceTablesModel:
         self.tables = {}
 
     def allocate(self, seq, num_tokens: int) -> None:
-        n = -(-num_tokens // self.block_size)
-        blocks = self.pool.allocate(n)
-        if blocks is None:
-            raise PoolExhausted(f"need {n} blocks, {self.pool.num_free()} free")
-        self.tables[seq] = blocks
+        need = -(-num_tokens // self.block_size)
+        got = self.pool.allocate(need)
+        if got is None:
+            raise PoolExhausted(f"need {need} blocks, {self.pool.num_free()} free")
+        self.tables[seq] = got
 
     def append_token(self, seq, cur_len: int) -> None:
-        """Grow before writing position ``cur_len`` if it opens a new block."""
-        if cur_len % self.block_size == 0:
-            blocks = self.pool.allocate(1)
-            if blocks is None:
-                raise PoolExhausted("no free block to grow the sequence")
-            self.tables[seq].append(blocks[0])
+        """Before position ``cur_len`` is written: a new block if it opens one."""
+        if cur_len % self.block_size:
+            return
+        got = self.pool.allocate(1)
+        if got is None:
+            raise PoolExhausted("no free block to grow the sequence")
+        self.tables[seq] += got
 
     def fork(self, parent, child) -> None:
-        self.tables[child] = list(self.tables[parent])
-        self.pool.incref(self.tables[parent])
+        self.tables[child] = self.tables[parent][:]
+        self.pool.incref(self.tables[child])
 
     def cow_for_write(self, seq, pos: int):
-        """Make the block holding ``pos`` private; return (src, dst)."""
-        lb = pos // self.block_size
-        src, dst = self.pool.cow(self.tables[seq][lb])
-        self.tables[seq][lb] = dst
+        """Make the block holding ``pos`` the writer's own; return (src, dst)."""
+        table = self.tables[seq]
+        src, dst = self.pool.cow(table[pos // self.block_size])
+        table[pos // self.block_size] = dst
         return src, dst
 
     def slot_index(self, seq, pos: int) -> int:
@@ -129,79 +150,71 @@ class SequenceTablesModel:
 
 
 class PrefixCachePoolModel(BlockPoolModel):
-    """``BlockPoolModel`` plus full-block prefix caching (see module notes)."""
+    """``BlockPoolModel`` with full-block prefix caching (module notes)."""
 
     def __init__(self, num_blocks: int, block_size: int, free_order=None):
         super().__init__(num_blocks, free_order)
         self.block_size = block_size
-        self.gen = [0] * num_blocks
-        self.entry_of = {}   # (parent, parent_gen, tokens) -> block
-        self.key_of = {}     # block -> its key
+        self._generation = [0] * num_blocks
+        self._by_identity = {}   # identity -> the block holding it
+        self._identity = {}      # block -> its identity, while it has one
 
     def num_cached(self) -> int:
-        return len(self.key_of)
+        return len(self._identity)
 
-    def _drop_entry(self, b: int) -> None:
-        key = self.key_of.pop(b, None)
-        if key is not None and self.entry_of.get(key) == b:
-            del self.entry_of[key]
+    def _forget(self, b: int) -> None:
+        ident = self._identity.pop(b, None)
+        if ident is not None and self._by_identity.get(ident) == b:
+            del self._by_identity[ident]
 
-    def _fresh(self) -> int:
-        b = self.free_queue.popleft()
-        self._drop_entry(b)
-        self.gen[b] += 1
-        self.ref_cnt[b] = 1
-        return b
+    def _take_front(self, n: int):
+        granted = super()._take_front(n)
+        for b in granted:                     # handed out fresh: a new generation
+            self._forget(b)
+            self._generation[b] += 1
+        return granted
 
-    def allocate(self, n: int):
-        if n > len(self.free_queue):
-            return None
-        return [self._fresh() for _ in range(n)]
+    def _identity_of(self, parent: int, tokens) -> tuple:
+        gen = self._generation[parent] if parent >= 0 else 0
+        return parent, gen, tuple(int(t) for t in tokens)
 
-    def cow(self, blk: int):
-        if self.ref_cnt[blk] == 1:
-            return blk, blk
-        if not self.free_queue:
-            raise PoolExhausted("no free block for copy-on-write")
-        self.ref_cnt[blk] -= 1
-        return blk, self._fresh()
-
-    def _key(self, parent: int, tokens) -> tuple:
-        return (parent, self.gen[parent] if parent >= 0 else 0, tuple(int(t) for t in tokens))
-
-    def register(self, b: int, parent: int, tokens) -> None:
-        self._drop_entry(b)
-        key = self._key(parent, tokens)
-        if key in self.entry_of:
-            return
-        self.entry_of[key] = b
-        self.key_of[b] = key
+    def register_block(self, b: int, parent: int, tokens) -> None:
+        """Give block ``b`` the identity (parent, parent's generation, tokens);
+        the first block registered under an identity keeps it."""
+        if len(tokens) != self.block_size:
+            raise ValueError("a registered block holds exactly block_size tokens")
+        self._forget(b)
+        ident = self._identity_of(parent, tokens)
+        if ident not in self._by_identity:
+            self._by_identity[ident] = b
+            self._identity[b] = ident
 
     def allocate_prefix(self, tokens):
-        """(blocks, cached_tokens) for a new sequence, or None when short."""
+        """(blocks, cached_tokens) for a new sequence with prompt ``tokens``,
+        or None (and no change) when the pool is short."""
         B = self.block_size
-        n = len(tokens)
-        nblk, nfull = -(-n // B), n // B
-        hits, parent = [], -1
-        for k in range(nfull):
-            b = self.entry_of.get(self._key(parent, tokens[k * B:(k + 1) * B]))
+        tokens = list(tokens)
+        full, total = len(tokens) // B, -(-len(tokens) // B)
+        # 1. the longest chain of full blocks already cached for this prompt
+        matched, parent = [], -1
+        while len(matched) < full:
+            k = len(matched)
+            b = self._by_identity.get(self._identity_of(parent, tokens[k * B:(k + 1) * B]))
             if b is None:
                 break
-            hits.append(b)
+            matched.append(b)
             parent = b
-        free_hits = sum(1 for b in hits if self.ref_cnt[b] == 0)
-        if nblk - len(hits) > len(self.free_queue) - free_hits:
+        # 2. all or nothing: matched blocks that sit in the queue are not
+        #    available to serve the fresh part
+        idle = [b for b in matched if self._holders[b] == 0]
+        if total - len(matched) > len(self._waiting) - len(idle):
             return None
-        for b in hits:
-            if self.ref_cnt[b] == 0:
-                self.free_queue.remove(b)
-            self.ref_cnt[b] += 1
-        blocks = list(hits)
-        parent = hits[-1] if hits else -1
-        for k in range(len(hits), nblk):
-            b = self._fresh()
-            blocks.append(b)
-            if k < nfull:
-                self.register(b, parent, tokens[k * B:(k + 1) * B])
-            parent = b
-        return blocks, len(hits) * B
+        for b in idle:
+            self._waiting.remove(b)
+        self.incref(matched)
+        # 3. fresh blocks for the rest; each new full block gets its identity
+        blocks = matched + self._take_front(total - len(matched))
+        for k in range(len(matched), full):
+            self.register_block(blocks[k], blocks[k - 1] if k else -1,
+                                tokens[k * B:(k + 1) * B])
+        return blocks, len(matched) * B

@@ -219,4 +219,4 @@ def test_native_matches_model_on_random_ops():
                 assert {k: list(v) for k, v in ma.tables.items()} == \
                        {k: list(v) for k, v in mb.tables.items()}
                 assert ma.pool.num_free() == mb.pool.num_free()
-        assert list(ma.pool.free_queue) == list(mb.pool.free_order())
+        assert ma.pool.free_order() == list(mb.pool.free_order())

@@ -3,8 +3,9 @@
 Pins from the pages: a shared prompt's full blocks are stored once and
 reused by later requests (their K/V need not be recomputed), a partly filled
 last block is never shared (each request writes into its own block), blocks
-are released to the free queue and reused in freeing order.  Then the native
-pool is checked against the Python model on random request traces."""
+are released to the free queue and reused in freeing order.  Every hand
+trace runs on the oracle's model and on the native pool, each on its own;
+then the two are compared on random request traces."""
 import random
 
 import pytest
@@ -15,14 +16,23 @@ from paged_kv_cache_108_gb300 import pool
 B = 16
 
 
-def _pool(n, order=None):
+def _native(n, order=None):
     p = pool.BlockPool(n, free_order=order)
     p.enable_prefix_cache(B)
     return p
 
 
-def test_full_prompt_blocks_are_shared_and_the_partial_block_is_not():
-    p = _pool(20)
+def _model(n, order=None):
+    return PrefixCachePoolModel(n, B, free_order=order)
+
+
+@pytest.fixture(params=["model", "native"])
+def make_pool(request):
+    return _model if request.param == "model" else _native
+
+
+def test_full_prompt_blocks_are_shared_and_the_partial_block_is_not(make_pool):
+    p = make_pool(20)
     prompt = list(range(100, 140))                 # 40 tokens: 2 full blocks + 8 tokens
     a, ca = p.allocate_prefix(prompt)
     b, cb = p.allocate_prefix(prompt)
@@ -32,8 +42,8 @@ def test_full_prompt_blocks_are_shared_and_the_partial_block_is_not():
     assert p.num_free() == 20 - 4
 
 
-def test_system_prompt_is_stored_once_for_many_requests():
-    p = _pool(64)
+def test_system_prompt_is_stored_once_for_many_requests(make_pool):
+    p = make_pool(64)
     system = list(range(64))                       # 4 full blocks
     tables = [p.allocate_prefix(system + [1000 + r] * (r + 1)) for r in range(10)]
     shared = tables[0][0][:4]
@@ -42,8 +52,8 @@ def test_system_prompt_is_stored_once_for_many_requests():
     assert [p.refcount(x) for x in shared] == [10] * 4
 
 
-def test_freed_cached_blocks_are_reused_until_evicted_in_freeing_order():
-    p = _pool(6, order=[0, 1, 2, 3, 4, 5])
+def test_freed_cached_blocks_are_reused_until_evicted_in_freeing_order(make_pool):
+    p = make_pool(6, order=[0, 1, 2, 3, 4, 5])
     prompt = list(range(32))                       # 2 full blocks
     blocks, _ = p.allocate_prefix(prompt)          # blocks 0, 1
     p.free(blocks)                                 # free queue: 2 3 4 5 0 1
@@ -61,23 +71,23 @@ def test_freed_cached_blocks_are_reused_until_evicted_in_freeing_order():
     assert third == [1, 2] and p.num_cached() == 2  # fresh from the head, registered anew
 
 
-def test_prompts_diverging_after_one_block_share_one_block():
-    p = _pool(10)
+def test_prompts_diverging_after_one_block_share_one_block(make_pool):
+    p = make_pool(10)
     a, _ = p.allocate_prefix(list(range(32)))
     b, cb = p.allocate_prefix(list(range(16)) + list(range(50, 66)))
     assert cb == 16 and b[0] == a[0] and b[1] != a[1]
 
 
-def test_out_of_blocks_leaves_the_pool_unchanged():
-    p = _pool(4)
+def test_out_of_blocks_leaves_the_pool_unchanged(make_pool):
+    p = make_pool(4)
     p.allocate_prefix(list(range(32)))
     before = (p.free_order(), [p.refcount(i) for i in range(4)], p.num_cached())
     assert p.allocate_prefix(list(range(32)) + list(range(200, 260))) is None
     assert (p.free_order(), [p.refcount(i) for i in range(4)], p.num_cached()) == before
 
 
-def test_registering_a_block_filled_by_decode():
-    p = _pool(8)
+def test_registering_a_block_filled_by_decode(make_pool):
+    p = make_pool(8)
     a, _ = p.allocate_prefix(list(range(20)))      # block 1 holds tokens 16..19 so far
     tail = list(range(16, 32))                     # decode filled it
     p.register_block(a[1], a[0], tail)
@@ -93,8 +103,8 @@ def test_native_pool_matches_the_model_on_random_traces(seed):
     n = rng.choice([24, 40, 80])
     order = list(range(n))
     rng.shuffle(order)
-    nat = _pool(n, order)
-    mod = PrefixCachePoolModel(n, B, free_order=order)
+    nat = _native(n, order)
+    mod = _model(n, order)
     templates = [[rng.randrange(50) for _ in range(rng.choice([16, 32, 48, 70]))] for _ in range(4)]
     live = []
     for step in range(250):
@@ -124,6 +134,6 @@ def test_native_pool_matches_the_model_on_random_traces(seed):
                 got = nat.cow(bk)
                 assert got == mod.cow(bk)
                 blocks[i] = got[1]
-        assert nat.free_order() == list(mod.free_queue)
-        assert [nat.refcount(i) for i in range(n)] == mod.ref_cnt
+        assert nat.free_order() == mod.free_order()
+        assert [nat.refcount(i) for i in range(n)] == [mod.refcount(i) for i in range(n)]
         assert nat.num_cached() == mod.num_cached()

@@ -4,8 +4,10 @@ Checked against what the pages and the mathematics fix, not against the
 oracle itself: the pages' printed three-request block tables, a scalar
 brute-force attention loop on tiny inputs, closed forms (q = 0 averages the
 visible V rows; the first prefill token sees only itself), equality with the
-(separately pinned) decode oracle when each request has one new token, and
-invariance under any permutation of physical blocks."""
+(separately pinned) decode oracle when each request has one new token,
+invariance under any permutation of physical blocks, an E4M3 cache against a
+scalar loop over torch's own E4M3 decoding, and the zero-row reading for a
+request with more new tokens than context."""
 import json
 import math
 import os
@@ -133,3 +135,48 @@ def test_any_block_permutation_gives_the_same_output():
     o2 = varlen.varlen_attention(moved["q"], moved["kc"], moved["vc"], moved["tables"],
                                  moved["seq_lens"], moved["qsl"], 0.125)
     assert np.array_equal(o1, o2)
+
+
+def test_e4m3_cache_matches_brute_force_over_torch_decoding():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(13)
+    B, Hkv, H, d, nb = 4, 2, 4, 16, 12
+    kc = rng.integers(0, 256, size=(nb, B, Hkv, d), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=(nb, B, Hkv, d), dtype=np.uint8)
+    kc[(kc & 0x7F) == 0x7F] = 0x11   # keep NaN codes out of the context
+    vc[(vc & 0x7F) == 0x7F] = 0x22
+    tables = np.array([[3, 7, 1], [10, 0, 5]], dtype=np.int32)
+    seq_lens, qlens = [11, 6], [3, 2]
+    qsl = np.array([0, 3, 5])
+    q = _bf16(rng.standard_normal((5, H, d)))
+    ks, vs = 0.03125, 0.75
+    out = varlen.varlen_attention(q, kc, vc, tables, seq_lens, qsl, 0.2, ks, vs)
+
+    def deq(codes, s):
+        return torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).double().numpy() * s
+
+    for r in range(2):
+        for j in range(qlens[r]):
+            last = seq_lens[r] - qlens[r] + j
+            for h in range(H):
+                g = h // (H // Hkv)
+                rows = [(tables[r][t // B], t % B) for t in range(last + 1)]
+                kk = np.array([deq(kc[b, o, g], ks) for b, o in rows])
+                vv = np.array([deq(vc[b, o, g], vs) for b, o in rows])
+                qv = _f(q[qsl[r] + j, h])
+                lg = [0.2 * float(np.dot(qv, kk[t])) for t in range(last + 1)]
+                mx = max(lg)
+                w = np.array([math.exp(x - mx) for x in lg])
+                want = (w[:, None] * vv).sum(axis=0) / w.sum()
+                np.testing.assert_allclose(out[qsl[r] + j, h], want, rtol=0, atol=1e-12)
+
+
+def test_more_new_tokens_than_context_gives_zero_rows():
+    c = _case([12, 9], [3, 4], 4, 2, 8, 4, 16, seed=17)
+    seq_lens = np.array([12, 2])          # request 1: 4 new tokens, 2 in its context
+    out = varlen.varlen_attention(c["q"], c["kc"], c["vc"], c["tables"], seq_lens, c["qsl"],
+                                  scale=0.3)
+    assert not out[3:].any()
+    alone = varlen.varlen_attention(c["q"][:3], c["kc"], c["vc"], c["tables"][:1],
+                                    seq_lens[:1], c["qsl"][:2], scale=0.3)
+    assert np.array_equal(out[:3], alone)
