@@ -141,6 +141,51 @@ def causal_pairs(context_lens, new_tokens) -> int:
     return sum(int(n - T) * T + T * (T + 1) // 2 for n in context_lens)
 
 
+def decode_bytes_of(w, kv_bytes, new_tokens, tokens) -> int:
+    """Algorithmic bytes of one decode call (what the method must move): the
+    K/V rows of ``tokens`` stored tokens once per KV head (rows stored once
+    are read once, so shared prefix blocks count once), q and out, the
+    block-table entries and the lengths."""
+    kv = tokens * w.num_kv_heads * w.head_dim * kv_bytes * 2
+    qo = 2 * w.num_seqs * new_tokens * w.num_heads * w.head_dim * 2
+    table = int(sum(math.ceil(n / w.block_size) for n in w.context_lens)) * 4
+    return kv + qo + table + w.num_seqs * 4
+
+
+def write_bytes_of(w, kv_bytes, new_tokens) -> int:
+    """Algorithmic bytes of the step's cache write: the new tokens' bf16 K
+    and V read, their cache rows written, and their slots."""
+    n = w.num_seqs * new_tokens
+    return 2 * n * w.num_kv_heads * w.head_dim * (2 + kv_bytes) + n * 4
+
+
+def step_config(args, w, unique_tokens, fp8, new_tokens, group, sbytes, dbytes, world):
+    """The ``config`` object of the JSON line (both arms print the same one)."""
+    cfg = {"workload": f"{WORKLOADS[args.workload]}, "
+                       + (f"{new_tokens} new tokens per sequence "
+                          + ("(chunked prefill, pa_varlen_attention tiles), "
+                             if new_tokens >= PREFILL_TOKENS else
+                             "(pa_decode_multi), ") if new_tokens > 1 else "")
+                       + (f"shared-prefix groups of {group} "
+                          "(pa_decode_shared_prefix), " if group else "")
+                       + f"{'e4m3 (per-tensor scale)' if fp8 else 'bf16'} KV, "
+                       f"block {w.block_size}, sum ctx {int(np.sum(w.context_lens))}",
+           "num_seqs": w.num_seqs,
+           "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads,
+           "head_dim": w.head_dim, "block_size": w.block_size,
+           "num_blocks": w.num_blocks, "sum_context": int(np.sum(w.context_lens)),
+           "partition_tokens": args.partition or "auto", "kernel": args.kernel or "auto",
+           "bytes_per_step": sbytes, "decode_bytes_per_step": dbytes}
+    if unique_tokens != int(np.sum(w.context_lens)):
+        cfg["decode_bytes_logical"] = decode_bytes_of(w, 1 if fp8 else 2, new_tokens,
+                                                      int(np.sum(w.context_lens)))
+        cfg["unique_context_tokens"] = unique_tokens
+    cfg["l2"] = (f"flushed between steps by reading a {L2_FLUSH_BYTES >> 20} MB buffer "
+                 "(untimed)")
+    cfg["parallelism"] = "replicas" if world > 1 else "single GPU"
+    return cfg
+
+
 class Step:
     """Device-resident state of one decode step of a workload."""
 
@@ -209,7 +254,8 @@ class Step:
         # unless the SIMT kernel is forced; SIMT adds a combine launch
         simt = kernel == 1
         G = H // hkv
-        tc = kernel == 2 or (kernel == 0 and d == 128 and B >= 8 and S <= 1024 and G in (1, 2, 4, 8))
+        tc = kernel == 2 or (kernel == 0 and d == 128 and S <= 1024 and G in (1, 2, 4, 8)
+                                   and (B >= 8 or T > 1))
         splits = int(np.max(w.context_lens)) > (partition or 256)
         self.launches_per_step = 2 + (1 if not tc and splits else 0)
         if shared_prefix_group:
@@ -218,15 +264,9 @@ class Step:
         if T >= PREFILL_TOKENS:
             self.launches_per_step = 2  # cache write, prefill tiles
 
-    # algorithmic bytes of one step (what the method must move): K/V rows
-    # stored once are read once (shared prefix blocks count once)
     def decode_bytes(self, logical=False) -> int:
-        w = self.w
-        tokens = int(np.sum(w.context_lens)) if logical else self.unique_tokens
-        kv = tokens * w.num_kv_heads * w.head_dim * self.kv_bytes * 2
-        qo = 2 * w.num_seqs * self.new_tokens * w.num_heads * w.head_dim * 2
-        table = int(sum(math.ceil(n / w.block_size) for n in w.context_lens)) * 4
-        return kv + qo + table + w.num_seqs * 4
+        tokens = int(np.sum(self.w.context_lens)) if logical else self.unique_tokens
+        return decode_bytes_of(self.w, self.kv_bytes, self.new_tokens, tokens)
 
     # causal attention flops of one step: per query head, 4 d per visible
     # (new token, key) pair -- the tensor-core prefill tiles' algorithmic work
@@ -235,10 +275,7 @@ class Step:
         return 4.0 * w.head_dim * w.num_heads * causal_pairs(w.context_lens, self.new_tokens)
 
     def write_bytes(self) -> int:
-        w = self.w
-        # K and V: bf16 tokens read, cache rows written
-        n = w.num_seqs * self.new_tokens
-        return 2 * n * w.num_kv_heads * w.head_dim * (2 + self.kv_bytes) + n * 4
+        return write_bytes_of(self.w, self.kv_bytes, self.new_tokens)
 
     def run_write(self, slots=None, k=None, v=None):
         self.ops.reshape_and_cache(self.k_new if k is None else k, self.v_new if v is None else v,
@@ -458,17 +495,34 @@ def run_ours(args, rank, world, local_rank):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    def host_ahead():
+        # a few ms of GPU sleep ahead of a timed loop: the host enqueues the
+        # first iterations while the GPU waits, so host-side latency (the
+        # clock sampler starting, a first call through a code path) never
+        # shows between a start event and its kernels
+        torch.cuda._sleep(int(4e6))
+
     with ClockSampler(local_rank) as clk:
+        time.sleep(0.3)  # the sampler's own start-up (NVML) is over before timing
+        host_ahead()
+        # after an idle GPU the first call runs with cold clocks (measured
+        # 160-280 us against 87 us for the batch-64 step): a few untimed
+        # steps, queued back to back with the timed ones, wake it first
+        for _ in range(3):
+            flush_l2()
+            one_step()
         for k in range(K):
             flush_l2()
             ev[k][0].record(stream)
             one_step()
             ev[k][1].record(stream)
+        host_ahead()
         for k in range(K):
             flush_l2()
             ev[k][2].record(stream)
             step.run_decode()
             ev[k][3].record(stream)
+        host_ahead()
         for k in range(K):
             flush_l2()
             ev[k][4].record(stream)
@@ -529,30 +583,13 @@ def run_ours(args, rank, world, local_rank):
         "data": ("synthetic (seeded N(0,1) K/V quantised to e4m3 with scale amax/448, bf16 q; "
                  "lengths from the pages' seeded request mix)" if step.fp8 else
                  "synthetic (seeded N(0,1) bf16 K/V/q; lengths from the pages' seeded request mix)"),
-        "config": {"workload": f"{WORKLOADS[args.workload]}, "
-                               + (f"{step.new_tokens} new tokens per sequence "
-                                  + ("(chunked prefill, pa_varlen_attention tiles), "
-                                     if step.new_tokens >= PREFILL_TOKENS else
-                                     "(pa_decode_multi), ") if step.new_tokens > 1 else "")
-                               + (f"shared-prefix groups of {step.group} "
-                                  "(pa_decode_shared_prefix), " if step.group else "")
-                               + f"{'e4m3 (per-tensor scale)' if step.fp8 else 'bf16'} KV, "
-                               f"block {w.block_size}, sum ctx {int(np.sum(w.context_lens))}",
-                   "num_seqs": w.num_seqs,
-                   "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads,
-                   "head_dim": w.head_dim, "block_size": w.block_size,
-                   "num_blocks": w.num_blocks, "sum_context": int(np.sum(w.context_lens)),
-                   "partition_tokens": args.partition or "auto", "kernel": args.kernel or "auto",
-                   "bytes_per_step": sbytes, "decode_bytes_per_step": dbytes,
-                   **({"decode_bytes_logical": step.decode_bytes(logical=True),
-                       "unique_context_tokens": step.unique_tokens}
-                      if step.unique_tokens != int(np.sum(w.context_lens)) else {}),
-                   "l2": f"flushed between steps by reading a {L2_FLUSH_BYTES >> 20} MB buffer "
-                         "(untimed)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": step_config(args, w, step.unique_tokens, step.fp8, step.new_tokens,
+                              step.group, sbytes, dbytes, world),
         "us_per_step": round(mean_step * 1e3, 2),
         "us_per_step_p50": round(statistics.median(step_ms) * 1e3, 2),
         "us_per_step_p90": round(float(np.percentile(step_ms, 90)) * 1e3, 2),
+        "us_per_step_max": round(max(step_ms) * 1e3, 2),
+        "us_decode_p50": round(statistics.median(dec_ms) * 1e3, 2),
         "us_decode": round(mean_dec * 1e3, 2),
         "us_write": round(sum(wr_ms) / K * 1e3, 2),
         "tokens_per_s": round(world * w.num_seqs * step.new_tokens / (mean_step * 1e-3), 1),
@@ -656,42 +693,72 @@ def run_e2e(step, args, device, dist):
 
 
 def run_reference(args, rank, world):
-    """The oracle as the reference arm: each step is a bounded sample of the
-    headline workload (a fixed set of (sequence, kv-head) units) decoded by
-    the fp64 CPU oracle on the host cores."""
+    """The oracle as the reference arm: every step is the whole step of the
+    same workload -- the cache write of the new tokens, then the decode of
+    every (sequence, KV head) unit -- by the fp64 CPU oracle on all host
+    cores, on a seeded N(0,1) pool of the same shape."""
     if rank != 0:
         return
     from oracle import core as ocore
-    from paged_kv_cache_108_gb300 import synth
-    w = synth.llama8b(with_data=False)
+    from paged_kv_cache_108_gb300 import pool, synth
+    if args.new_tokens != 1 or args.shared_prefix_group:
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times single-token "
+                          "decode steps through pa_decode only"}), flush=True)
+        return
+    w, unique = build_workload(args.workload, args.block_size, args.kv_dtype)
+    fp8 = args.kv_dtype == "fp8"
     rng = np.random.default_rng(w.seed)
     shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
-    kc = synth.normal_bf16(rng, shape)
-    vc = synth.normal_bf16(rng, shape)
+    ks = vs = 1.0
+    if fp8:
+        caches = []
+        for _ in range(2):
+            x = synth.normal_bf16(rng, shape)
+            sc = synth.per_tensor_scale(x)
+            codes = np.zeros(shape, dtype=np.uint8)
+            ocore.reshape_and_cache(x.reshape(-1, w.num_kv_heads, w.head_dim), x.reshape(
+                -1, w.num_kv_heads, w.head_dim), codes, codes.copy(),
+                np.arange(w.num_blocks * w.block_size, dtype=np.int32), sc, sc)
+            caches.append((codes, sc))
+            del x
+        (kc, ks), (vc, vs) = caches
+    else:
+        kc = synth.normal_bf16(rng, shape)
+        vc = synth.normal_bf16(rng, shape)
     q = synth.normal_bf16(rng, (w.num_seqs, w.num_heads, w.head_dim))
+    k_new = synth.normal_bf16(rng, (w.num_seqs, w.num_kv_heads, w.head_dim))
+    v_new = synth.normal_bf16(rng, (w.num_seqs, w.num_kv_heads, w.head_dim))
+    seqs = np.arange(w.num_seqs, dtype=np.int32)
     threads = os.cpu_count() or 1
-    # each step decodes sequences 0..7 (64 of the 512 (sequence, kv-head) units)
-    n_seq = 8
-    units = [(i, g) for i in range(n_seq) for g in range(w.num_kv_heads)]
-    ub = sum(int(w.context_lens[i]) * w.head_dim * 2 * 2 for i, _ in units)
-    qo = n_seq * w.num_heads * w.head_dim * 2 * 2
+    kv_bytes = 1 if fp8 else 2
+    dbytes = decode_bytes_of(w, kv_bytes, 1, unique)
+    sbytes = dbytes + write_bytes_of(w, kv_bytes, 1)
+
+    def one_step():
+        slots = pool.slot_mapping(w.block_tables, w.block_size, w.context_lens - 1, seqs)
+        ocore.reshape_and_cache(k_new, v_new, kc, vc, slots, ks, vs)
+        ocore.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, ks, vs,
+                     nthreads=threads)
+
     for _ in range(max(args.warmup, 3)):
-        ocore.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, units=units, nthreads=threads)
+        one_step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        ocore.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale, units=units, nthreads=threads)
+        one_step()
     dt = (time.perf_counter() - t0) / args.steps
-    value = (ub + qo) / dt / 1e9
+    value = sbytes / dt / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
             "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "llama8b-layer decode sample: sequences 0-7 x 8 kv heads "
-                                   "of the batch-64 step (32q/8kv, d=128, block 16)"},
+            "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) pool of the same shape)",
+            "config": step_config(args, w, unique, fp8, 1, 0, sbytes, dbytes, world),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                              "kind": "oracle",
-                             "sample": "64 (sequence, kv-head) units (sequences 0-7) of the "
-                                       "llama8b step per step"},
+                             "sample": f"the whole {args.workload} step per step: host slot "
+                                       f"mapping and cache write of {w.num_seqs} tokens, then "
+                                       f"all {w.num_seqs * w.num_kv_heads} (sequence, kv-head) "
+                                       f"decode units, fp64, {threads} threads"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

@@ -109,11 +109,11 @@ size_t pa_decode_workspace_size_ex(int32_t num_seqs, int32_t num_heads,
  *  kernel 1: SIMT kernel (CUDA cores, cp.async ring, fixed split-K
  *            partitions of partition_tokens, separate combine kernel); serves
  *            every supported shape.
- *  kernel 2: tensor-core kernel (tcgen05 MMA, TMA loads, persistent CTAs that
- *            each stream an equal share of 128-token (bf16) or 256-token
- *            (e4m3) chunks, in-kernel merge of split units); needs head_dim
- *            128, block_size >= 8 and at most 1024 sequences, else
- *            PA_ERR_UNSUPPORTED.  For an e4m3 cache the MMAs take the cache
+ *  kernel 2: tensor-core kernel (tcgen05 MMA, TMA loads -- 16-byte cp.async
+ *            gathers for block_size below 8 --, persistent CTAs that each
+ *            stream an equal share of 128-token (bf16) or 256-token (e4m3)
+ *            chunks, in-kernel merge of split units); needs head_dim 128 and
+ *            at most 1024 sequences, else PA_ERR_UNSUPPORTED.  For an e4m3 cache the MMAs take the cache
  *            bytes as they are (kind::f8f6f4); q and the softmax weights are
  *            split into e4m3 parts (three for q, two for the weights) whose
  *            sum keeps them to about 2^-12 and 2^-8 relative.
@@ -131,7 +131,9 @@ size_t pa_decode_workspace_size_ex(int32_t num_seqs, int32_t num_heads,
  *  kernel 0: kernel 3 where it applies and the batch has many units (per
  *            unit: a sequence and its 8 or 16 KV heads; at least twice the SM
  *            count, or half of it for GQA group 1), else kernel 2 where it
- *            applies, else kernel 1. */
+ *            applies (below 8 tokens per block only for several tokens per
+ *            sequence: the gathered loads stream slower than the SIMT
+ *            kernel), else kernel 1. */
 typedef struct {
   int32_t partition_tokens; /* split-K partition length: power of two >= 64 */
   int32_t kernel;           /* 0 auto, 1 SIMT, 2 tensor-core, 3 head-packed tensor-core */
@@ -225,11 +227,19 @@ pa_status pa_write_and_decode(const void* key, const void* value,
  * that loads the library holds it until the process exits).  It allocates
  * nothing and calls no allocating routine.
  *
- *  - Output and numerics are those of pa_decode; the split-K partition
- *    length is the shortest power of two from 256 tokens whose partials fit.
+ *  - Output and numerics are those of pa_decode with the automatic kernel
+ *    choice.  When that choice is the SIMT kernel (head_dim other than 128,
+ *    block_size below 8, ...), its split-K partition length is the shortest
+ *    power of two from 256 tokens whose partials fit; the tensor-core
+ *    kernels ignore partition lengths and use their fixed per-CTA slots.
  *  - PA_ERR_UNSUPPORTED, with nothing launched, when the sizes need more
  *    scratch than the array holds even with 65536-token partitions; use
  *    pa_decode with a workspace then.
+ *  - Device-side faults the tensor-core kernels detect (an expired bounded
+ *    wait, an out-of-range block id, which they replace by block 0) set a
+ *    status word kept in the array.  Decode calls never clear it; read and
+ *    clear it with pa_decode_noalloc_error.  The SIMT kernel reports
+ *    nothing there.
  *  - The first call on each device looks up the array's device address
  *    (with that device current) and caches it; make that first call before
  *    any stream capture begins.
@@ -247,6 +257,18 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache,
                             int32_t num_heads, float scale,
                             const float* k_scale, const float* v_scale,
                             pa_stream_t stream);
+
+/* pa_decode_noalloc_error -- enqueue on `stream` a copy of the current
+ * device's pa_decode_noalloc status word into *code, then clear the word.
+ * 0 means no pa_decode_noalloc call on this device reported a device-side
+ * fault since the word was last read; a nonzero value is the code of such a
+ * fault: 3 for a block id outside the pool, any other value for a bounded
+ * wait that expired (the value names the wait).
+ * `code` may be device memory or host memory (page-locked for the copy to
+ * stay asynchronous); its value is valid once the stream has reached the
+ * copy.  Like pa_decode_noalloc, it allocates nothing.  PA_ERR_INVALID for
+ * a NULL code, PA_ERR_CUDA if the copy or the clear cannot be enqueued. */
+pa_status pa_decode_noalloc_error(int32_t* code, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * pa_copy_blocks -- device side of copy-on-write: for each (src, dst) pair,
@@ -331,8 +353,12 @@ pa_status pa_varlen_attention(void* out, const void* q, const void* k_cache, con
  *            range; the library never clears it.  Workspace word 1 is the
  *            tiles' work counter, zeroed on `stream` before each launch (an
  *            asynchronous memset, captured with the kernel in a graph).
- *  method 0: method 2 where it applies and the step adds at least 16 new
- *            tokens per request on average, else method 1.
+ *  method 0: where method 2 applies: method 2 for every request when the
+ *            step adds at least 16 new tokens per request on average;
+ *            otherwise, when it adds 16 or more in all, method 2 for the
+ *            requests adding 16 or more and method 1 for the others (two
+ *            launches on `stream`; word 0 is then the tiles' error word,
+ *            zeroed by the call before the tiles run); else method 1.
  *  Other arguments as pa_varlen_attention.
  * ---------------------------------------------------------------------- */
 pa_status pa_varlen_attention_ex(void* out, const void* q, const void* k_cache,

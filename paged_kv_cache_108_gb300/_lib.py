@@ -14,6 +14,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpa.so")
 
 PA_OK, PA_ERR_INVALID, PA_ERR_OOM, PA_ERR_CUDA, PA_ERR_UNSUPPORTED = range(5)
+PA_DECODE_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024  # include/pa.h
 PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
 
 
@@ -58,6 +59,7 @@ SIGNATURES = {
                            P, SIZE, ctypes.POINTER(DecodeOpts), P]),
     "pa_decode_noalloc": (I32, [P, P, P, P, CacheDesc, P, I32, P, I32, I32, ctypes.c_float, P,
                                 P, P]),
+    "pa_decode_noalloc_error": (I32, [P, P]),
     "pa_write_and_decode": (I32, [P, P, P, I32, P, P, P, P, CacheDesc, P, I32, P, I32, I32,
                                   ctypes.c_float, P, P, P, SIZE, P]),
     "pa_copy_blocks": (I32, [P, P, CacheDesc, P, I32, P]),

@@ -18,6 +18,9 @@ thread_local std::string g_last_error;
 constexpr int kAutoPartition = 512;     // default split-K partition (tokens)
 constexpr int kAutoPartitionMin = 256;  // smallest automatic choice
 constexpr int kMaxPartition = 65536;
+// pa_varlen_attention method 0: requests adding this many new tokens or more
+// take the tensor-core prefill tiles
+constexpr int kTileMinTokens = 16;
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -200,6 +203,37 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t hea
 
 }  // extern "C"
 
+// The automatic kernel choice (pa_decode_opts.kernel 0) for a call of this
+// shape: 3 head-packed, 2 per-head tensor-core, 1 SIMT.  The head-packed
+// kernel streams faster (bigger copies) but its units (sequence x 8 or 16 KV
+// heads) are long, and a unit split over several CTAs ends in a merge at the
+// CTA's tail.  Measured on GB300 (GQA 4): 64 units (batch 64, ~1900 tokens)
+// 94.5 vs 86.8 us; 256 units about equal; 512 units 2.5 % faster; 1000 short
+// units 24 % faster.  For MHA the per-head kernel computes 16 columns for one
+// head, so the head-packed one wins earlier (128 units: 3 % faster).
+int pa_decode_auto_kernel(const pa_cache_desc& cache, int32_t num_heads, int32_t num_seqs,
+                          int32_t tokens_per_seq) {
+  if (cache.num_kv_heads <= 0 || num_heads % cache.num_kv_heads != 0) return 1;
+  const int group = num_heads / cache.num_kv_heads;
+  const bool fp8 = cache.dtype == PA_KV_FP8_E4M3;
+  if (pa::hp_supported(cache.head_dim, group, fp8, num_seqs, cache.num_kv_heads,
+                       cache.block_size, tokens_per_seq)) {
+    const int64_t hp_units = (int64_t)num_seqs * (cache.num_kv_heads / (group >= 2 ? 8 : 16));
+    if (group == 1 ? 2 * hp_units >= num_sms() : hp_units >= 2 * num_sms()) return 3;
+  }
+  // Below 8 tokens per block the tensor-core kernel gathers rows with cp.async
+  // and publishes a stage only once its own copies have landed; measured on
+  // GB300 at block size 1 (batch-64 layer): 220.8 us (2.28 TB/s) against the
+  // SIMT kernel's 136.4 us (3.7 TB/s), both reading the algorithmic bytes.  A
+  // single token per sequence therefore takes the SIMT kernel there; several
+  // tokens per sequence take the tensor-core kernel, which reads the context
+  // once instead of once per token.
+  if (pa::tc_supported(cache.head_dim, group, fp8, num_seqs, cache.block_size, tokens_per_seq) &&
+      (cache.block_size >= 8 || tokens_per_seq > 1))
+    return 2;
+  return 1;
+}
+
 // pa_decode_ex's body.  prev_writes_cache_only: the kernel launched just
 // before on `stream` is this library's cache write, so the tensor-core
 // kernel may read its metadata (lengths, tables, q) while that write is still
@@ -245,20 +279,11 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
   }
 
   const bool fp8 = cache.dtype == PA_KV_FP8_E4M3;
-  const bool hp_fits = (kernel == 0 || kernel == 3) &&
-                       pa::hp_supported(cache.head_dim, group, fp8, num_seqs,
-                                        cache.num_kv_heads, cache.block_size, tokens_per_seq);
-  // Automatic choice: the head-packed kernel streams faster (bigger copies)
-  // but its units (sequence x 8 or 16 KV heads) are long, and a unit split
-  // over several CTAs ends in a merge at the CTA's tail.  Measured on GB300
-  // (GQA 4): 64 units (batch 64, ~1900 tokens) 94.5 vs 86.8 us; 256 units
-  // about equal; 512 units 2.5 % faster; 1000 short units 24 % faster.  For
-  // MHA the per-head kernel computes 16 columns for one head, so the
-  // head-packed one wins earlier (128 units: 3 % faster).
-  const int64_t hp_units =
-      hp_fits ? (int64_t)num_seqs * (cache.num_kv_heads / (group >= 2 ? 8 : 16)) : 0;
-  const bool hp_ok = hp_fits && (kernel == 3 || (group == 1 ? 2 * hp_units >= num_sms()
-                                                             : hp_units >= 2 * num_sms()));
+  const int chosen =
+      kernel != 0 ? kernel : pa_decode_auto_kernel(cache, num_heads, num_seqs, tokens_per_seq);
+  const bool hp_ok = chosen == 3 &&
+                     pa::hp_supported(cache.head_dim, group, fp8, num_seqs, cache.num_kv_heads,
+                                      cache.block_size, tokens_per_seq);
   if (kernel == 3 && !hp_ok)
     return pa_fail(PA_ERR_UNSUPPORTED,
                    "pa_decode: head-packed kernel needs a bf16 cache, head_dim 128, GQA group "
@@ -293,16 +318,16 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
     a.early_meta = prev_writes_cache_only;
     return cuda_status(pa::launch_decode_hp(a, reinterpret_cast<cudaStream_t>(stream)), fn);
   }
-  const bool tc_ok = kernel != 1 && pa::tc_supported(cache.head_dim, group, fp8, num_seqs,
+  const bool tc_ok = chosen == 2 && pa::tc_supported(cache.head_dim, group, fp8, num_seqs,
                                                       cache.block_size, tokens_per_seq);
   if (tokens_per_seq > 1 && !tc_ok)  // the SIMT kernel serves one token per sequence
     return pa_fail(PA_ERR_UNSUPPORTED, "pa_decode: several tokens per sequence need the "
                                        "tensor-core kernel");
-  if (kernel == 2 || (kernel == 0 && tc_ok)) {
+  if (chosen == 2) {
     if (!tc_ok)
       return pa_fail(PA_ERR_UNSUPPORTED,
-                     "pa_decode: tensor-core kernel needs head_dim 128, "
-                     "block_size >= 8 and at most 1024 sequences");
+                     "pa_decode: tensor-core kernel needs head_dim 128 "
+                     "and at most 1024 sequences");
     const int nsm = num_sms();
     const size_t need = pa::tc_workspace_bytes(num_seqs, num_heads, max_ctx, nsm, tokens_per_seq);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) {
@@ -461,6 +486,36 @@ size_t pa_varlen_workspace_size(int32_t num_tokens, int32_t num_heads, int32_t h
                                          block_size);
 }
 
+}  // extern "C"
+
+// Method 1 of pa_varlen_attention: one virtual decode sequence per new token
+// (its request's table, its causal length).  Tokens of requests with
+// tile_min or more new tokens (tile_min > 0) get empty virtual sequences.
+static pa_status varlen_per_token(void* out, const void* q, const void* k_cache,
+                                  const void* v_cache, pa_cache_desc cache,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* seq_lens, const int32_t* query_start_loc,
+                                  int32_t num_seqs, int32_t num_tokens, int32_t num_heads,
+                                  float scale, const float* k_scale, const float* v_scale,
+                                  void* workspace, size_t workspace_bytes, pa_stream_t stream,
+                                  int tile_min) {
+  char* ws = static_cast<char*>(workspace);
+  int32_t* vtables = reinterpret_cast<int32_t*>(ws);
+  const size_t tb = align256((size_t)num_tokens * max_blocks_per_seq * 4);
+  int32_t* vlens = reinterpret_cast<int32_t*>(ws + tb);
+  const size_t meta = tb + align256((size_t)num_tokens * 4);
+  cudaError_t e = pa::launch_varlen_meta(block_tables, max_blocks_per_seq, cache.block_size,
+                                         seq_lens, query_start_loc, 0, num_seqs, num_tokens,
+                                         vtables, vlens, reinterpret_cast<cudaStream_t>(stream),
+                                         tile_min);
+  if (e != cudaSuccess) return cuda_status(e, "pa_varlen_attention");
+  return decode_impl(out, q, k_cache, v_cache, cache, vtables, max_blocks_per_seq, vlens,
+                     num_tokens, num_heads, scale, k_scale, v_scale, ws + meta,
+                     workspace_bytes - meta, nullptr, stream, false);
+}
+
+extern "C" {
+
 pa_status pa_varlen_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
                               pa_cache_desc cache, const int32_t* block_tables,
                               int32_t max_blocks_per_seq, const int32_t* seq_lens,
@@ -499,6 +554,7 @@ pa_status pa_varlen_attention_ex(void* out, const void* q, const void* k_cache,
     return pa_fail(PA_ERR_INVALID, "pa_varlen_attention: misaligned pointer");
   pa_status st = check_cache(cache, fn);
   if (st != PA_OK) return st;
+  if ((st = check_scales(cache, k_scale, v_scale, fn)) != PA_OK) return st;
   const size_t need = pa_varlen_workspace_size(num_tokens, num_heads, cache.head_dim,
                                                max_blocks_per_seq, cache.block_size);
   if (need == 0 || workspace_bytes < need) {
@@ -515,7 +571,15 @@ pa_status pa_varlen_attention_ex(void* out, const void* q, const void* k_cache,
     return pa_fail(PA_ERR_UNSUPPORTED,
                    "pa_varlen_attention: prefill tiles need a bf16 cache, head_dim 128, GQA "
                    "group 1, 2, 4 or 8, block_size >= 8, at most 256 requests and scale > 0");
-  if (method == 2 || (method == 0 && tiles_fit && num_tokens >= 16 * num_seqs)) {
+  // Method 0 with tiles available: when the step adds 16 or more tokens per
+  // request on average, the tiles serve every request; otherwise requests
+  // adding 16 or more tokens go to the tiles and the others to one decode per
+  // new token (the long requests' tokens are empty virtual sequences there,
+  // zero rows the tiles then overwrite), so one long prefill among many
+  // single-token decodes no longer runs token by token.
+  const bool tiles_all = method == 2 || (method == 0 && tiles_fit && num_tokens >= 16 * num_seqs);
+  const bool tiles_mixed = !tiles_all && method == 0 && tiles_fit && num_tokens >= kTileMinTokens;
+  if (tiles_all || tiles_mixed) {
     if (!out || !q || !k_cache || !v_cache)
       return pa_fail(PA_ERR_INVALID, "pa_varlen_attention: NULL pointer");
     if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
@@ -539,21 +603,21 @@ pa_status pa_varlen_attention_ex(void* out, const void* q, const void* k_cache,
     a.block_size = cache.block_size;
     a.num_ctas = num_sms();
     a.scale = scale;
+    a.min_tokens = tiles_all ? 0 : kTileMinTokens;
+    if (tiles_all) return cuda_status(pa::launch_prefill_tc(a, s), fn);
+    // the short requests first (below), then the tiles on the same stream;
+    // word 0 is the tiles' error word once the decode has used the metadata
+    st = varlen_per_token(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                          seq_lens, query_start_loc, num_seqs, num_tokens, num_heads, scale,
+                          k_scale, v_scale, workspace, workspace_bytes, stream, kTileMinTokens);
+    if (st != PA_OK) return st;
+    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) return cuda_status(e, fn);
     return cuda_status(pa::launch_prefill_tc(a, s), fn);
   }
-  char* ws = static_cast<char*>(workspace);
-  int32_t* vtables = reinterpret_cast<int32_t*>(ws);
-  const size_t tb = align256((size_t)num_tokens * max_blocks_per_seq * 4);
-  int32_t* vlens = reinterpret_cast<int32_t*>(ws + tb);
-  const size_t meta = tb + align256((size_t)num_tokens * 4);
-  cudaError_t e = pa::launch_varlen_meta(block_tables, max_blocks_per_seq, cache.block_size,
-                                         seq_lens, query_start_loc, 0, num_seqs, num_tokens,
-                                         vtables, vlens, s);
-  if (e != cudaSuccess) return cuda_status(e, fn);
-  // one virtual sequence per new token: its request's table, its causal length
-  return decode_impl(out, q, k_cache, v_cache, cache, vtables, max_blocks_per_seq, vlens,
-                     num_tokens, num_heads, scale, k_scale, v_scale, ws + meta,
-                     workspace_bytes - meta, nullptr, stream, false);
+  return varlen_per_token(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
+                          seq_lens, query_start_loc, num_seqs, num_tokens, num_heads, scale,
+                          k_scale, v_scale, workspace, workspace_bytes, stream, 0);
 }
 
 size_t pa_decode_multi_workspace_size(int32_t num_seqs, int32_t tokens_per_seq,

@@ -168,7 +168,7 @@ __global__ void step_prepare_kernel(int32_t* __restrict__ block_tables, int max_
 __global__ void varlen_meta_kernel(const int32_t* __restrict__ block_tables, int max_blocks,
                                    int block_size, const int32_t* __restrict__ seq_lens,
                                    const int32_t* __restrict__ qsl, int uniform_tokens,
-                                   int num_seqs, int32_t* __restrict__ vtables,
+                                   int num_seqs, int tile_min, int32_t* __restrict__ vtables,
                                    int32_t* __restrict__ vlens) {
   const int t = blockIdx.x;
   __shared__ int s_req, s_ctx;
@@ -191,6 +191,8 @@ __global__ void varlen_meta_kernel(const int32_t* __restrict__ block_tables, int
     const int n = seq_lens[a];
     int ctx = n - num_new + (t - start) + 1;
     if (num_new > n || t >= start + num_new || ctx < 1) ctx = 0;
+    // tokens of requests the prefill tiles serve: an empty virtual sequence
+    if (tile_min > 0 && num_new >= tile_min) ctx = 0;
     if ((int64_t)ctx > (int64_t)max_blocks * block_size) ctx = 0;
     s_req = a;
     s_ctx = ctx;
@@ -293,10 +295,10 @@ cudaError_t launch_lse_merge(const void* o1, const float* l1, const void* o2, co
 cudaError_t launch_varlen_meta(const int32_t* block_tables, int max_blocks, int block_size,
                                const int32_t* seq_lens, const int32_t* query_start_loc,
                                int uniform_tokens, int num_seqs, int num_tokens, int32_t* vtables,
-                               int32_t* vlens, cudaStream_t stream) {
+                               int32_t* vlens, cudaStream_t stream, int tile_min) {
   varlen_meta_kernel<<<num_tokens, 128, 0, stream>>>(block_tables, max_blocks, block_size,
                                                      seq_lens, query_start_loc, uniform_tokens,
-                                                     num_seqs, vtables, vlens);
+                                                     num_seqs, tile_min, vtables, vlens);
   return cudaGetLastError();
 }
 

@@ -13,6 +13,16 @@
 // It reuses pa_decode_ex unchanged: it only picks a split-K partition length
 // whose scratch fits in the array (the smallest power of two from 256 tokens
 // up), then passes the array as the workspace.
+//
+// Status word.  The tensor-core kernels report an expired bounded wait or an
+// out-of-range block id by writing a nonzero code into word 0 of their
+// workspace; they never clear it.  Here word 0 of the array is that word for
+// every call that runs a tensor-core kernel (the array's start is their
+// workspace), and the SIMT kernel, which reports nothing, gets the array from
+// byte 256 on so its partials never land on the word.  The word therefore
+// keeps the first call's zero (a __device__ array starts zeroed) until a
+// kernel reports a fault, and stays set until pa_decode_noalloc_error reads
+// and clears it.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -23,6 +33,9 @@
 #include "pa_host.h"
 
 namespace {
+
+// Bytes at the array's start kept clear of SIMT partials (word 0 = status).
+constexpr size_t kStatusBytes = 256;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_DECODE_NOALLOC_SCRATCH_BYTES];
 
@@ -72,12 +85,17 @@ extern "C" pa_status pa_decode_noalloc(void* out, const void* q, const void* k_c
                         context_lens, num_seqs, num_heads, scale, k_scale, v_scale, nullptr, 0,
                         nullptr, stream);
   }
+  // the tensor-core kernels take the whole array (word 0 is their error word);
+  // the SIMT kernel takes it from kStatusBytes on
+  const int kernel = pa_decode_auto_kernel(cache, num_heads, num_seqs, 1);
+  const size_t offset = kernel == 1 ? kStatusBytes : 0;
+  const size_t room = (size_t)PA_DECODE_NOALLOC_SCRATCH_BYTES - offset;
   // the smallest partition length (fewest idle SMs) whose partials fit
   int32_t partition = 0;
   for (int32_t ps = 256; ps <= 65536; ps *= 2) {
     const size_t need = pa_decode_workspace_size_ex(num_seqs, num_heads, cache.head_dim,
                                                     max_blocks_per_seq, cache.block_size, ps);
-    if (need <= (size_t)PA_DECODE_NOALLOC_SCRATCH_BYTES) {
+    if (need <= room) {
       partition = ps;
       break;
     }
@@ -85,19 +103,35 @@ extern "C" pa_status pa_decode_noalloc(void* out, const void* q, const void* k_c
   if (partition == 0) {
     char buf[240];
     snprintf(buf, sizeof buf,
-             "pa_decode_noalloc: %d sequences x %d heads x %d tokens need more than the %u-byte "
-             "built-in scratch; use pa_decode with a caller workspace",
-             num_seqs, num_heads, max_blocks_per_seq * cache.block_size,
+             "pa_decode_noalloc: %d sequences x %d heads x %lld tokens need more than the "
+             "%u-byte built-in scratch; use pa_decode with a caller workspace",
+             num_seqs, num_heads, (long long)max_blocks_per_seq * cache.block_size,
              (unsigned)PA_DECODE_NOALLOC_SCRATCH_BYTES);
     return pa_fail(PA_ERR_UNSUPPORTED, buf);
   }
   void* scratch = nullptr;
   pa_status st = scratch_for_current_device(&scratch);
   if (st != PA_OK) return st;
-  // no part of the scratch has to start at zero: every split-K partial is
-  // written by the decode kernel before the combine kernel reads it
-  pa_decode_opts opts{partition, 0};
+  // no part of the workspace has to start at zero: every split-K partial is
+  // written before it is read, and the merge counters carry a per-call tag
+  pa_decode_opts opts{partition, kernel};
   return pa_decode_ex(out, q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq,
-                      context_lens, num_seqs, num_heads, scale, k_scale, v_scale, scratch,
-                      (size_t)PA_DECODE_NOALLOC_SCRATCH_BYTES, &opts, stream);
+                      context_lens, num_seqs, num_heads, scale, k_scale, v_scale,
+                      static_cast<unsigned char*>(scratch) + offset, room, &opts, stream);
+}
+
+extern "C" pa_status pa_decode_noalloc_error(int32_t* code, pa_stream_t stream) {
+  if (!code) return pa_fail(PA_ERR_INVALID, "pa_decode_noalloc_error: NULL code");
+  void* scratch = nullptr;
+  pa_status st = scratch_for_current_device(&scratch);
+  if (st != PA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(code, scratch, sizeof(int32_t), cudaMemcpyDefault, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(scratch, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) {
+    char buf[200];
+    snprintf(buf, sizeof buf, "pa_decode_noalloc_error: %s", cudaGetErrorString(e));
+    return pa_fail(PA_ERR_CUDA, buf);
+  }
+  return PA_OK;
 }

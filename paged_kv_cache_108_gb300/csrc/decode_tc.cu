@@ -28,7 +28,10 @@
 //   warp 4     producer: per chunk, TMA tensor loads of each physical block's
 //              K rows (and, for an e4m3 cache, V rows; 4-D tensor map
 //              [blocks, block_size, H_kv, d], 128-byte swizzle, 128-byte-wide
-//              boxes) into a 3-stage ring and, for bf16, each segment's q rows;
+//              boxes) into a 3-stage ring and, for bf16, each segment's q rows.
+//              Blocks of fewer than 8 tokens cannot fill a 1024-byte swizzle
+//              atom with one box: their rows are gathered instead, 16 bytes
+//              per lane and cp.async, into the same swizzled layout;
 //   warp 5     TMEM allocation and the single MMA-issuing thread;
 //   warp 6     merge warp: counts finished pieces of split units and merges
 //              a unit's pieces when its last piece is done;
@@ -70,7 +73,9 @@ constexpr int D = 128;
 constexpr int NQ = 16;                 // MMA N of PV: query heads (bf16), hi/lo rows of P (fp8)
 constexpr int kMaxSeqs = 1024;
 constexpr int kMaxCols = 16;           // columns of a unit (the MMA N of PV)
-constexpr int TAB_SLOTS = 4, TAB_AHEAD = 3, TAB_W = 32;  // block-id ring: 4 chunks x 32 boxes
+// block-id ring: 4 chunks x up to 256 ids (a 256-token e4m3 chunk of 1-token
+// blocks)
+constexpr int TAB_SLOTS = 4, TAB_AHEAD = 3, TAB_W = 256;
 
 // Shared-memory layout and roles for a bf16 or an fp8-e4m3 cache.
 template <bool FP8>
@@ -150,6 +155,12 @@ struct Params {
   const float* v_scale;
   unsigned long long epoch;  // 48-bit tag of this call
   int early_meta;            // previous kernel wrote only the cache
+  // block_size < 8: K/V rows are gathered with 16-byte cp.async copies
+  // instead of TMA boxes (a box of fewer than 8 rows cannot fill a whole
+  // 1024-byte swizzle atom); kc / vc are the caches' base addresses
+  int gather;
+  const unsigned char* kc;
+  const unsigned char* vc;
 };
 
 template <int G, bool FP8>
@@ -207,6 +218,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
       if ((i >= B_S_EMPTY && i < B_S_EMPTY + 2) || (i >= B_P_FULL && i < B_P_FULL + 2) ||
           (i >= B_O_EMPTY && i < B_O_EMPTY + 2) || (i >= B_EPI && i < B_EPI + 2))
         cnt = 128;
+      if (p.gather && i < B_EMPTY) cnt = 32;  // gathered rows: every producer lane arrives
       if (FP8 && i >= B_Q_FULL && i < B_Q_FULL + 2) cnt = 32;        // the q warp's lanes
       if (FP8 && i >= B_Q_EMPTY && i < B_Q_EMPTY + 2) cnt = 1 + 128;  // MMA + softmax threads
       ptx::mbar_init(sm.bar(i), cnt);
@@ -308,9 +320,10 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
   if (warp == 4 || warp == Cf::VPROD) {
     // ================= producers (K: warp 4, V: warp VPROD) =================
     // Block ids travel through a shared-memory ring filled by 4-byte cp.async
-    // copies TAB_AHEAD chunks ahead (lane b copies and later uses box b's id;
-    // block_size >= 8 keeps a chunk within 32 boxes), so table reads overlap
-    // instead of following one another.
+    // copies TAB_AHEAD chunks ahead (TMA boxes: lane b copies and later uses
+    // box b's id, block_size >= 8 keeping a chunk within 32 boxes; gathered
+    // rows: up to 256 ids a chunk, read by the lanes that copy their rows),
+    // so table reads overlap instead of following one another.
     const bool isk = warp == 4;                      // loads K (and q)
     const bool isv = !Cf::TWO_PROD || warp != 4;     // loads V
     const int tab_off = OFF_TAB + (isk ? 0 : TAB_SLOTS * TAB_W * 4);
@@ -318,10 +331,9 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
     const int* tab_s = reinterpret_cast<const int*>(sm.base + tab_off);
     auto fetch_ids = [&](const Walk& w, int slot) {
       const int nb = (w.valid() + p.box_tok - 1) >> p.log2_box;
-      if (lane < nb)
-        cp_async_4(tab + (slot * TAB_W + lane) * 4,
-                   p.block_tables + (int64_t)w.seq * p.max_blocks +
-                       ((w.j * CH + lane * p.box_tok) >> p.log2_bs));
+      const int32_t* row = p.block_tables + (int64_t)w.seq * p.max_blocks;
+      for (int e = lane; e < nb; e += 32)
+        cp_async_4(tab + (slot * TAB_W + e) * 4, row + ((w.j * CH + e * p.box_tok) >> p.log2_bs));
     };
     walk.init(lo, hi, seq_lo, seq_hi);
     Walk ahead = walk;
@@ -333,6 +345,17 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
       }
       cp_async_commit();
     }
+    // Gathered rows (block_size < 8): the lanes copy 16-byte pieces and each
+    // lane arrives on the chunk's FULL barrier once its own pieces have
+    // landed and been made visible to the tensor cores (fence.proxy.async).
+    // Commit groups per chunk i: rows(i), then ids(i + TAB_AHEAD); after
+    // them, waiting until three groups remain pending completes rows(i - 1)
+    // and ids(i + 1), so chunk i - 1 is published one chunk late.
+    auto publish = [&](int l) {
+      ptx::fence_proxy_async_smem();
+      if (isk) ptx::mbar_arrive(sm.bar(B_FULL_K + l % NST));
+      if (isv) ptx::mbar_arrive(sm.bar(B_FULL_V + l % NST));
+    };
     int local = 0, seg = 0;
     for (; !walk.done(); walk.next(), ++local) {
       const int s = local % NST;
@@ -340,7 +363,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
       const int cs = walk.j * CH;
       const int valid = walk.valid();
       const int nbox = (valid + p.box_tok - 1) >> p.log2_box;
-      cp_async_wait<TAB_AHEAD - 1>();  // this chunk's ids have landed
+      if (!p.gather || local == 0) cp_async_wait<TAB_AHEAD - 1>();  // this chunk's ids have landed
       const int phys_in = lane < nbox ? tab_s[(local % TAB_SLOTS) * TAB_W + lane] : 0;
       if (!wait_bar(sm, sm.bar(B_EMPTY + s), ph ^ 1, p.err, 1)) break;
       if (!FP8 && isk && walk.first_of_segment()) {
@@ -359,36 +382,73 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
         }
         ++seg;
       }
-      const uint32_t bytes = (uint32_t)nbox * p.box_tok * (uint32_t)(D * Cf::ELT);
       if (p.early_meta && local == 0) ptx::grid_dependency_wait();
       const uint32_t kdst = sm.base_u32 + OFF_K + s * TILE_B;
       const uint32_t vdst = sm.base_u32 + OFF_V + s * TILE_B;
-      const uint32_t row = (uint32_t)(lane * p.box_tok) * 128u;
-      const int off = (cs + lane * p.box_tok) & (p.block_size - 1);
-      int phys = phys_in;
-      if (lane < nbox && (unsigned)phys >= (unsigned)p.num_blocks) {
-        atomicExch(p.err, 3);  // bad block id: load block 0 instead of faulting
-        phys = 0;
-      }
-      if (lane == 0) {
-        if (isk) ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_K + s), bytes);
-        if (isv) ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_V + s), bytes);
-      }
-      __syncwarp();
-      if (lane < nbox) {
-        // a token row of one head is 128 bytes in fp8 (one box) and 256 bytes
-        // in bf16 (two 64-column boxes, one per 128-byte column block)
-        if (isk) {
-          ptx::tma_load_4d(kdst + row, &tm_k, sm.bar(B_FULL_K + s), 0, walk.g, off, phys);
-          if (!FP8)
-            ptx::tma_load_4d(kdst + HALF_B + row, &tm_k, sm.bar(B_FULL_K + s), 64, walk.g, off,
-                             phys);
+      if (p.gather) {
+        // Eight lanes per row, four rows per step: lane l copies 16-byte
+        // piece l % 8 of row 4 * step + l / 8 (bf16: of both 128-byte column
+        // blocks), so one instruction moves four whole 128-byte row pieces.
+        // smem as the TMA boxes would leave it (128-byte rows, 16-byte pieces
+        // XOR-swizzled by row & 7; bf16 column blocks HALF_B apart).
+        const int* ids = tab_s + (local % TAB_SLOTS) * TAB_W;
+        const int64_t row_bytes = (int64_t)Hkv * D * Cf::ELT;
+        const int pc = lane & 7;
+        const unsigned char* kg = p.kc + (int64_t)walk.g * D * Cf::ELT + pc * 16;
+        const unsigned char* vg = p.vc + (int64_t)walk.g * D * Cf::ELT + pc * 16;
+        const int steps = (valid + 3) >> 2;
+#pragma unroll 4
+        for (int st = 0; st < steps; ++st) {
+          const int r = st * 4 + (lane >> 3);
+          if (r < valid) {
+            int phys = ids[r >> p.log2_bs];
+            if ((unsigned)phys >= (unsigned)p.num_blocks) {
+              atomicExch(p.err, 3);  // bad block id: load block 0 instead of faulting
+              phys = 0;
+            }
+            const int64_t src =
+                ((int64_t)phys * p.block_size + ((cs + r) & (p.block_size - 1))) * row_bytes;
+            const uint32_t so = (uint32_t)(r * 128 + ((pc ^ (r & 7)) << 4));
+            if (isk) {
+              cp_async_16(kdst + so, kg + src, 16);
+              if (!FP8) cp_async_16(kdst + HALF_B + so, kg + src + 128, 16);
+            }
+            if (isv) {
+              cp_async_16(vdst + so, vg + src, 16);
+              if (!FP8) cp_async_16(vdst + HALF_B + so, vg + src + 128, 16);
+            }
+          }
         }
-        if (isv) {
-          ptx::tma_load_4d(vdst + row, &tm_v, sm.bar(B_FULL_V + s), 0, walk.g, off, phys);
-          if (!FP8)
-            ptx::tma_load_4d(vdst + HALF_B + row, &tm_v, sm.bar(B_FULL_V + s), 64, walk.g, off,
-                             phys);
+        cp_async_commit();
+      } else {
+        const uint32_t bytes = (uint32_t)nbox * p.box_tok * (uint32_t)(D * Cf::ELT);
+        const uint32_t row = (uint32_t)(lane * p.box_tok) * 128u;
+        const int off = (cs + lane * p.box_tok) & (p.block_size - 1);
+        int phys = phys_in;
+        if (lane < nbox && (unsigned)phys >= (unsigned)p.num_blocks) {
+          atomicExch(p.err, 3);  // bad block id: load block 0 instead of faulting
+          phys = 0;
+        }
+        if (lane == 0) {
+          if (isk) ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_K + s), bytes);
+          if (isv) ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_V + s), bytes);
+        }
+        __syncwarp();
+        if (lane < nbox) {
+          // a token row of one head is 128 bytes in fp8 (one box) and 256 bytes
+          // in bf16 (two 64-column boxes, one per 128-byte column block)
+          if (isk) {
+            ptx::tma_load_4d(kdst + row, &tm_k, sm.bar(B_FULL_K + s), 0, walk.g, off, phys);
+            if (!FP8)
+              ptx::tma_load_4d(kdst + HALF_B + row, &tm_k, sm.bar(B_FULL_K + s), 64, walk.g,
+                               off, phys);
+          }
+          if (isv) {
+            ptx::tma_load_4d(vdst + row, &tm_v, sm.bar(B_FULL_V + s), 0, walk.g, off, phys);
+            if (!FP8)
+              ptx::tma_load_4d(vdst + HALF_B + row, &tm_v, sm.bar(B_FULL_V + s), 64, walk.g,
+                               off, phys);
+          }
         }
       }
       if (!ahead.done()) {
@@ -396,15 +456,22 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
         ahead.next();
       }
       cp_async_commit();
+      if (p.gather && local > 0) {
+        cp_async_wait<3>();  // rows(local - 1) and ids(local + 1) have landed
+        publish(local - 1);
+      }
     }
     cp_async_wait<0>();
+    if (p.gather && local > 0) publish(local - 1);
     // drain: the last loads issued must land before the CTA can exit
+    // (gathered rows have landed already: every copy group is complete)
     __syncwarp();
     if (lane == 0) {
-      for (int l = max(0, local - NST); l < local; ++l) {
-        if (isk) drain_bar(sm.bar(B_FULL_K + l % NST), (l / NST) & 1);
-        if (isv) drain_bar(sm.bar(B_FULL_V + l % NST), (l / NST) & 1);
-      }
+      if (!p.gather)
+        for (int l = max(0, local - NST); l < local; ++l) {
+          if (isk) drain_bar(sm.bar(B_FULL_K + l % NST), (l / NST) & 1);
+          if (isv) drain_bar(sm.bar(B_FULL_V + l % NST), (l / NST) & 1);
+        }
       if (!FP8 && isk)
         for (int sg = max(0, seg - 2); sg < seg; ++sg)
           drain_bar(sm.bar(B_Q_FULL + (sg & 1)), (sg >> 1) & 1);
@@ -1016,14 +1083,16 @@ size_t tc_workspace_bytes(int64_t num_seqs, int64_t num_heads, int64_t /*max_ctx
 
 bool tc_supported(int head_dim, int group, bool fp8, int num_seqs, int block_size,
                   int tokens_per_seq) {
-  // block_size >= 8 keeps every TMA destination 1024-byte aligned (whole
-  // 128-byte-swizzle atoms).  A unit's columns (group x tokens) fill the MMA
-  // N: up to 16 for bf16, 8 for e4m3 (its q takes three rows per column).
+  // Every power-of-two block size: from 8 tokens up the K/V rows arrive as
+  // TMA boxes (whole 1024-byte swizzle atoms), below 8 as gathered 16-byte
+  // copies.  A unit's columns (group x tokens) fill the MMA N: up to 16 for
+  // bf16, 8 for e4m3 (its q takes three rows per column).
   const int t = tokens_per_seq > 0 ? tokens_per_seq : 1;
   const int cols = group * t;
   const bool pow2 = group > 0 && (group & (group - 1)) == 0 && (cols & (cols - 1)) == 0;
   return head_dim == tc::D && pow2 && group <= 8 && cols <= (fp8 ? 8 : 16) &&
-         num_seqs <= tc::kMaxSeqs && block_size >= 8 && tc::encode_fn() != nullptr;
+         num_seqs <= tc::kMaxSeqs && block_size >= 1 &&
+         (block_size & (block_size - 1)) == 0 && tc::encode_fn() != nullptr;
 }
 
 cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream) {
@@ -1115,6 +1184,9 @@ cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream) {
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   prm.early_meta = a.early_meta ? 1 : 0;
   prm.epoch = next_call_epoch();
+  prm.gather = a.block_size < 8 ? 1 : 0;
+  prm.kc = static_cast<const unsigned char*>(a.k_cache);
+  prm.vc = static_cast<const unsigned char*>(a.v_cache);
   const int G = gq * ntok;  // columns of a unit
   if (a.fp8) {
     switch (G) {

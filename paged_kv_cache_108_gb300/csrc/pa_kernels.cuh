@@ -88,6 +88,7 @@ struct PrefillLaunch {
   void* workspace;
   int num_seqs, num_tokens, num_heads, num_kv_heads, max_blocks, num_blocks, block_size;
   int num_ctas;
+  int min_tokens;  // requests with fewer new tokens get no tiles (0: every request)
   float scale;
 };
 bool prefill_supported(int head_dim, int group, bool fp8, int num_seqs, int block_size);
@@ -117,7 +118,7 @@ cudaError_t launch_lse_merge(const void* o1, const float* l1, const void* o2, co
 cudaError_t launch_varlen_meta(const int32_t* block_tables, int max_blocks, int block_size,
                                const int32_t* seq_lens, const int32_t* query_start_loc,
                                int uniform_tokens, int num_seqs, int num_tokens, int32_t* vtables,
-                               int32_t* vlens, cudaStream_t stream);
+                               int32_t* vlens, cudaStream_t stream, int tile_min = 0);
 
 cudaError_t launch_step_prepare(int32_t* block_tables, int max_blocks, int block_size,
                                 int32_t* context_lens, int num_seqs, const int32_t* updates,

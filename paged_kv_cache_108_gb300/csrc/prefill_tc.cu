@@ -108,6 +108,7 @@ struct Params {
   unsigned* next_item;          // workspace word 1: items handed out (zeroed before launch)
   int num_seqs, num_tokens, num_heads, num_kv_heads, max_blocks, num_blocks, block_size, log2_bs;
   int box_tok, log2_box;
+  int min_tokens;  // requests with fewer new tokens get no tiles
   float scale_log2;
 };
 
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // tiles per request, then an exclusive prefix (warp 0)
   for (int r = tid; r < R; r += NTHREADS) {
     const int T = __ldg(&p.qsl[r + 1]) - __ldg(&p.qsl[r]);
-    tp[r] = (uint16_t)(T > 0 ? (T + MQ - 1) / MQ : 0);
+    tp[r] = (uint16_t)(T > 0 && T >= p.min_tokens ? (T + MQ - 1) / MQ : 0);
   }
   __syncthreads();
   if (warp == 0) {
@@ -717,6 +718,7 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream) {
   // the item counter starts at zero for every launch (a memset node when captured)
   cudaError_t ez = cudaMemsetAsync(prm.next_item, 0, sizeof(unsigned), stream);
   if (ez != cudaSuccess) return ez;
+  prm.min_tokens = a.min_tokens;
   prm.num_seqs = a.num_seqs;
   prm.num_tokens = a.num_tokens;
   prm.num_heads = a.num_heads;

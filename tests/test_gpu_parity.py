@@ -61,6 +61,14 @@ def test_block_size_and_precision_sweep(block_size, kv_dtype):
 
 
 @requires_gpu
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_simt_kernel_on_one_token_blocks(kv_dtype):
+    # the tensor-core kernel serves block size 1 by default; the SIMT kernel
+    # stays a supported choice for it
+    _check_step(synth.sweep(1, kv_dtype), kernel=1)
+
+
+@requires_gpu
 @pytest.mark.parametrize("hq,hkv,d", [(8, 8, 64), (16, 8, 128), (32, 4, 128), (16, 2, 64)])
 def test_head_configurations(hq, hkv, d):
     lens = [1, 2, 15, 16, 17, 63, 64, 65, 200, 1000]

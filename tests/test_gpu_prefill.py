@@ -6,8 +6,10 @@ put request lengths on both sides of tile and 128-key chunk boundaries, mix
 chunked prefill (a context before the new tokens), full prefill (none) and
 single-token requests, and cover every GQA group the tiles serve, several
 block sizes, long prefills, many small requests, requests without new
-tokens, requests whose count exceeds their context (zero rows), and the
-kernel's error word."""
+tokens, requests whose count exceeds their context (zero rows), the
+kernel's error word, e4m3 caches (the e4m3 tolerance, against the oracle on
+the dequantised cache), and the automatic choice on a step that mixes one
+prefill with single-token decodes."""
 import numpy as np
 import pytest
 import torch
@@ -47,7 +49,7 @@ def _check(c, scale, method=TILES):
     ref = varlen.varlen_attention(c["q"], harness.bits_from_dev(c["kc"]),
                                   harness.bits_from_dev(c["vc"]), c["tables"], c["seq_lens"],
                                   c["qsl"], scale, c["kscale"], c["vscale"])
-    harness.assert_close(got, ref, False)
+    harness.assert_close(got, ref, c["kv"] == "fp8")
     assert np.isfinite(got).all()
     return got
 
@@ -131,3 +133,18 @@ def test_tiles_refuse_shapes_they_do_not_serve(what):
         c = _setup([40, 20], [10, 20], 64, 4, 128, 16, seed=117)
     with pytest.raises(PaError, match="prefill tiles"):
         _run(c, 0.1)
+
+
+@requires_gpu
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (16, 16)])
+def test_automatic_choice_on_a_step_mixing_one_prefill_with_decodes(hq, hkv):
+    # one 700-token chunked prefill among 40 single-token decodes (average
+    # under 16 new tokens per request): the prefill goes to the tiles, the
+    # decodes to the decode kernels, in one call
+    rng = np.random.default_rng(120)
+    seq = [1500] + [int(x) for x in rng.integers(1, 4000, size=40)]
+    new = [700] + [1] * 40
+    c = _setup(seq, new, hq, hkv, 128, 16, seed=121)
+    got = _check(c, 128 ** -0.5, method=0)
+    per_token = _run(c, 128 ** -0.5, method=1)
+    harness.assert_close(got, per_token, False)

@@ -45,9 +45,38 @@ def test_tc_long_context():
 
 
 @requires_gpu
-@pytest.mark.parametrize("block_size", [8, 16, 64, 256])
+@pytest.mark.parametrize("block_size", [1, 2, 4, 8, 16, 64, 256])
 def test_tc_block_sizes(block_size):
+    # below 8 tokens per block the rows are gathered by cp.async, not TMA
     _check(synth.sweep(block_size, "bf16"))
+
+
+@requires_gpu
+@pytest.mark.parametrize("block_size", [1, 2, 4])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_tc_gathered_rows_at_chunk_edges(block_size, kv_dtype):
+    # lengths on both sides of the 128-token (bf16) and 256-token (e4m3)
+    # chunk ends, single tokens, and long units split over CTAs
+    lens = [1, 2, 3, 127, 128, 129, 255, 256, 257, 511, 513, 5000, 20000]
+    w = synth.make(f"tc-gather-{block_size}-{kv_dtype}", lens, 32, 8, 128, block_size,
+                   kv_dtype=kv_dtype, seed=53 + block_size)
+    _check(w)
+
+
+@requires_gpu
+def test_tc_gathered_rows_permutation_invariant_and_agree_with_simt():
+    lens = [int(x) for x in np.random.default_rng(61).integers(1, 1500, size=20)]
+    a = synth.make("tc-gather-perm-a", lens, 32, 8, 128, 1, seed=62)
+    b = synth.make("tc-gather-perm-b", lens, 32, 8, 128, 1, seed=62)
+    # same data, blocks placed by another permutation
+    perm = np.random.default_rng(63).permutation(a.num_blocks).astype(np.int32)
+    b.block_tables = np.where(a.block_tables >= 0, perm[a.block_tables], a.block_tables)
+    ga = harness.product_step(a, kernel=TC)
+    gb = harness.product_step(b, kernel=TC)
+    assert ga["err"] == 0 and gb["err"] == 0
+    assert np.array_equal(ga["out"], gb["out"])
+    simt = harness.product_step(a, kernel=1)["out"]
+    harness.assert_close(ga["out"], simt, False)
 
 
 @requires_gpu
@@ -145,7 +174,7 @@ def test_write_and_decode_matches_separate_calls():
 # ---- e4m3 cache: kind::f8f6f4 MMAs with q and P split into e4m3 parts ----
 
 @requires_gpu
-@pytest.mark.parametrize("block_size", [8, 16, 64, 256])
+@pytest.mark.parametrize("block_size", [1, 2, 4, 8, 16, 64, 256])
 def test_tc_fp8_block_sizes(block_size):
     _check(synth.sweep(block_size, "fp8"))
 

@@ -157,3 +157,13 @@ def test_multi_token_split_units_with_masked_columns():
     c = _setup(lens, [4] * 4, 32, 8, 128, 16, seed=21)
     got = _check_multi(c, 4, 0.09)
     assert np.isfinite(got).all()
+
+
+@requires_gpu
+@pytest.mark.parametrize("block_size,kv", [(1, "bf16"), (2, "fp8"), (4, "bf16")])
+def test_multi_token_decode_on_gathered_rows(block_size, kv):
+    # blocks below 8 tokens: the one-pass kernel gathers its rows by cp.async
+    rng = np.random.default_rng(30 + block_size)
+    lens = [int(x) for x in rng.integers(4, 1800, size=12)] + [4, 5, 260]
+    c = _setup(lens, [4] * len(lens), 32, 8, 128, block_size, kv, seed=31 + block_size)
+    _check_multi(c, 4, 128 ** -0.5)
