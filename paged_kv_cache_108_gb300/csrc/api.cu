@@ -569,7 +569,7 @@ pa_status pa_varlen_attention_ex(void* out, const void* q, const void* k_cache,
                                                cache.block_size);
   if (method == 2 && !tiles_fit)
     return pa_fail(PA_ERR_UNSUPPORTED,
-                   "pa_varlen_attention: prefill tiles need a bf16 cache, head_dim 128, GQA "
+                   "pa_varlen_attention: prefill tiles need head_dim 128, GQA "
                    "group 1, 2, 4 or 8, block_size >= 8, at most 256 requests and scale > 0");
   // Method 0 with tiles available: when the step adds 16 or more tokens per
   // request on average, the tiles serve every request; otherwise requests
@@ -604,6 +604,9 @@ pa_status pa_varlen_attention_ex(void* out, const void* q, const void* k_cache,
     a.num_ctas = num_sms();
     a.scale = scale;
     a.min_tokens = tiles_all ? 0 : kTileMinTokens;
+    a.fp8 = fp8;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     if (tiles_all) return cuda_status(pa::launch_prefill_tc(a, s), fn);
     // the short requests first (below), then the tiles on the same stream;
     // word 0 is the tiles' error word once the decode has used the metadata

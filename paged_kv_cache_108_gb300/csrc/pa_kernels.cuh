@@ -90,6 +90,9 @@ struct PrefillLaunch {
   int num_ctas;
   int min_tokens;  // requests with fewer new tokens get no tiles (0: every request)
   float scale;
+  bool fp8;                // e4m3 cache: k_scale / v_scale are device scalars
+  const float* k_scale;
+  const float* v_scale;
 };
 bool prefill_supported(int head_dim, int group, bool fp8, int num_seqs, int block_size);
 cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream);

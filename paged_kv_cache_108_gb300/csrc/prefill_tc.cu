@@ -67,37 +67,58 @@ constexpr int CHK = 128;                  // keys per chunk
 // only after its PV MMA, so K runs one stage further ahead
 constexpr int NSTK = 3, NSTV = 2;
 constexpr int kMaxReqs = 256;
-constexpr int TILE_B = CHK * D * 2;       // one K or V chunk: 32 KiB
-constexpr int HALF_B = 128 * 128;         // one 64-column half of a 128-row tile
-constexpr int QTILE_B = 128 * D * 2;      // the q tile: 128 rows
-constexpr int PTILE_B = 128 * CHK * 2;    // P: 128 rows x 128 keys bf16
-constexpr int OFF_K = 0;
-constexpr int OFF_V = OFF_K + NSTK * TILE_B;
-constexpr int OFF_Q = OFF_V + NSTV * TILE_B;
-constexpr int OFF_P = OFF_Q + QTILE_B;
-constexpr int OFF_BAR = OFF_P + PTILE_B;  // one P buffer (the softmax rarely waits for it)
-constexpr int B_FULL_K = 0, B_FULL_V = B_FULL_K + NSTK, B_EMPTY_K = B_FULL_V + NSTV,
-              B_EMPTY_V = B_EMPTY_K + NSTK, B_Q_FULL = B_EMPTY_V + NSTV,
-              B_Q_EMPTY = B_Q_FULL + 1, B_S_FULL = B_Q_EMPTY + 1, B_S_EMPTY = B_S_FULL + 2,
-              B_P_FULL = B_S_EMPTY + 2, B_P_EMPTY = B_P_FULL + 1, B_O_FULL = B_P_EMPTY + 1,
-              B_O_EMPTY = B_O_FULL + 2, B_ITEM_FULL = B_O_EMPTY + 1,
-              B_ITEM_EMPTY = B_ITEM_FULL + 4, NBARS = B_ITEM_EMPTY + 4;
+constexpr int HALF_B = 128 * 128;         // one 128-byte-wide column block of 128 rows
+constexpr int QTILE_B = 128 * D * 2;      // the bf16 q tile: 128 rows
 constexpr int NRING = 4;  // work items published ahead by the K producer
-constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
-constexpr int OFF_ABORT = OFF_TMEM + 4;
-// tile prefix per request, [R+1]; 16 bits suffice: at most 65535 new tokens
-constexpr int OFF_RING = OFF_ABORT + 4;  // [NRING] item indices
-constexpr int OFF_TP = OFF_RING + NRING * 4;
-constexpr int OFF_XCH = (OFF_TP + (kMaxReqs + 1) * 2 + 15) / 16 * 16;  // [256] floats
-constexpr int SMEM_BYTES = OFF_XCH + 256 * 4 + 1024;                  // + alignment slack
 constexpr int NSOFT = 256;  // softmax threads: two per q tile row
 constexpr int NTHREADS = NSOFT + 96;
 constexpr int PROD_WARP = NSOFT / 32, MMA_WARP = PROD_WARP + 1, VPROD_WARP = MMA_WARP + 1;
 constexpr int TMEM_COLS = 512;  // S[2] at 0 and 128, O at 256
 constexpr int S_COL = 0, O_COL = 256;
-constexpr float kRescaleLog2 = 8.f;
-static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
-static_assert(OFF_BAR % 1024 == 0, "tiles stay 1024-byte aligned");
+constexpr int B_FULL_K = 0, B_FULL_V = B_FULL_K + NSTK, B_EMPTY_K = B_FULL_V + NSTV,
+              B_EMPTY_V = B_EMPTY_K + NSTK, B_Q_FULL = B_EMPTY_V + NSTV,
+              B_Q_EMPTY = B_Q_FULL + 1, B_S_FULL = B_Q_EMPTY + 1, B_S_EMPTY = B_S_FULL + 2,
+              B_P_FULL = B_S_EMPTY + 2, B_P_EMPTY = B_P_FULL + 1, B_O_FULL = B_P_EMPTY + 1,
+              B_O_EMPTY = B_O_FULL + 2, B_ITEM_FULL = B_O_EMPTY + 1,
+              B_ITEM_EMPTY = B_ITEM_FULL + 4, B_QP_FULL = B_ITEM_EMPTY + 4,
+              B_QP_EMPTY = B_QP_FULL + 1, NBARS = B_QP_EMPTY + 1;
+
+// Shared-memory layout for a bf16 or an e4m3 cache.  e4m3: K and V chunks are
+// 128 bytes a row; the bf16 q tile is staged, then split by the softmax
+// threads into three e4m3 parts (rows scaled by a power of two each); P is
+// two e4m3 parts.
+template <bool FP8>
+struct PCfg {
+  static constexpr int ELT = FP8 ? 1 : 2;
+  static constexpr int TILE_B = CHK * D * ELT;   // one K or V chunk
+  static constexpr int NQPART = FP8 ? 3 : 0;
+  static constexpr int QPART_B = 128 * D;        // one e4m3 part of the q tile
+  static constexpr int NPPART = FP8 ? 2 : 1;
+  static constexpr int PPART_B = 128 * CHK * ELT;  // P (bf16) or one e4m3 part of it
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + NSTK * TILE_B;
+  static constexpr int OFF_Q = OFF_V + NSTV * TILE_B;
+  static constexpr int OFF_QP = OFF_Q + QTILE_B;
+  static constexpr int OFF_P = OFF_QP + NQPART * QPART_B;
+  static constexpr int OFF_BAR = OFF_P + NPPART * PPART_B;  // one P buffer
+  static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
+  static constexpr int OFF_ABORT = OFF_TMEM + 4;
+  static constexpr int OFF_RING = OFF_ABORT + 4;  // [NRING] item indices
+  // tile prefix per request, [R+1]; 16 bits suffice: at most 65535 new tokens
+  static constexpr int OFF_TP = OFF_RING + NRING * 4;
+  static constexpr int OFF_XCH = (OFF_TP + (kMaxReqs + 1) * 2 + 15) / 16 * 16;  // [256] floats
+  // e4m3: per-row rescale factors [2][128] (by chunk parity) and final sums [128]
+  static constexpr int OFF_ALPHA = OFF_XCH + 256 * 4;
+  static constexpr int OFF_LSUM = OFF_ALPHA + (FP8 ? 2 * 128 * 4 : 0);
+  static constexpr int SMEM_BYTES = OFF_LSUM + (FP8 ? 128 * 4 : 0) + 1024;  // + alignment slack
+  // O is rescaled when a row's max grows by more than 2^R: p <= 2^R.  e4m3
+  // P holds p * 2^(8 - R) <= 256 (inside e4m3's 448), so a smaller R keeps
+  // small weights above e4m3's 2^-9 floor
+  static constexpr float kRescaleLog2 = FP8 ? 3.f : 8.f;
+  static constexpr float kPScale = FP8 ? 32.f : 1.f;  // 2^(8 - R)
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+  static_assert(OFF_BAR % 1024 == 0, "tiles stay 1024-byte aligned");
+};
 
 struct Params {
   void* out;                    // [num_tokens, H, D] bf16
@@ -110,6 +131,8 @@ struct Params {
   int box_tok, log2_box;
   int min_tokens;  // requests with fewer new tokens get no tiles
   float scale_log2;
+  const float* k_scale;  // e4m3: per-tensor dequantisation scales (device scalars)
+  const float* v_scale;
 };
 
 // One work item: request r, query tile qt (tokens qt*MQ ..), KV head g.
@@ -149,11 +172,18 @@ __device__ __forceinline__ Item item_of(long long i, const uint16_t* tp, int R,
   return it;
 }
 
-template <int G>
+template <int G, bool FP8>
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_q, const Params p) {
+  using C = PCfg<FP8>;
+  constexpr int TILE_B = C::TILE_B, QPART_B = C::QPART_B, PPART_B = C::PPART_B;
+  constexpr int OFF_K = C::OFF_K, OFF_V = C::OFF_V, OFF_Q = C::OFF_Q, OFF_QP = C::OFF_QP,
+                OFF_P = C::OFF_P, OFF_BAR = C::OFF_BAR, OFF_TMEM = C::OFF_TMEM,
+                OFF_ABORT = C::OFF_ABORT, OFF_RING = C::OFF_RING, OFF_TP = C::OFF_TP,
+                OFF_XCH = C::OFF_XCH;
+  constexpr float kRescaleLog2 = C::kRescaleLog2;
   constexpr int MQ = 128 / G;  // new tokens per tile
   extern __shared__ unsigned char smem_raw[];
   Smem sm;
@@ -180,8 +210,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (tid == 0) {
     for (int i = 0; i < NBARS; ++i) {
       uint32_t cnt = 1;
-      if ((i >= B_S_EMPTY && i < B_S_EMPTY + 2) || i == B_P_FULL || i == B_O_EMPTY)
+      if ((i >= B_S_EMPTY && i < B_S_EMPTY + 2) || i == B_P_FULL || i == B_O_EMPTY ||
+          i == B_QP_FULL)
         cnt = NSOFT;
+      // e4m3: the softmax threads read the staged q tile (and free it)
+      if (FP8 && i == B_Q_EMPTY) cnt = NSOFT;
       // an item slot is read by the V producer, the MMA thread and the 8
       // softmax warps (one arrival each)
       if (i >= B_ITEM_EMPTY && i < B_ITEM_EMPTY + NRING) cnt = 2 + NSOFT / 32;
@@ -299,13 +332,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (lane == 0)
           ptx::mbar_arrive_expect_tx(sm.bar(b_full + s),
-                                     (uint32_t)nbox * p.box_tok * (uint32_t)(D * 2));
+                                     (uint32_t)nbox * p.box_tok * (uint32_t)(D * C::ELT));
         __syncwarp();
         if (lane < nbox) {
+          // a row is one 128-byte box column (e4m3: all of d; bf16: two
+          // 64-column halves HALF_B apart)
           const uint32_t dst = ring + s * TILE_B + (uint32_t)(lane * p.box_tok) * 128u;
           const int off = (j * CHK + lane * p.box_tok) & (p.block_size - 1);
           ptx::tma_load_4d(dst, tm, sm.bar(b_full + s), 0, it.g, off, phys);
-          ptx::tma_load_4d(dst + HALF_B, tm, sm.bar(b_full + s), 64, it.g, off, phys);
+          if (!FP8) ptx::tma_load_4d(dst + HALF_B, tm, sm.bar(b_full + s), 64, it.g, off, phys);
         }
       }
       if (!ok) break;
@@ -324,9 +359,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // q tile) and the PV MMA of chunk npv < nq (needs P, the V chunk and, at
     // an item's first chunk, O read out by the previous item's epilogue).
     if (lane == 0) {
-      constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32_ab(128, CHK, false, false);
-      constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32_ab(128, D, false, true);
-      const uint32_t qbase = sm.base_u32 + OFF_Q;
+      // e4m3 uses the operand forms of the e4m3 decode kernel: both K-major
+      // for the logits; for P V the transposed product O^T = V^T P^T, V the
+      // MN-major A operand and P's rows the K-major B operand
+      constexpr uint32_t IDESC_QK = FP8 ? ptx::idesc_e4m3_f32(128, CHK, false)
+                                        : ptx::idesc_bf16_f32_ab(128, CHK, false, false);
+      constexpr uint32_t IDESC_PV = FP8 ? ptx::idesc_e4m3_f32(D, 128, true)
+                                        : ptx::idesc_bf16_f32_ab(128, D, false, true);
+      // the MMA's q operand: the bf16 tile, or (e4m3) its three parts
+      const uint32_t qbase = sm.base_u32 + (FP8 ? OFF_QP : OFF_Q);
+      const int b_qfull = FP8 ? B_QP_FULL : B_Q_FULL, b_qempty = FP8 ? B_QP_EMPTY : B_Q_EMPTY;
       // QK cursor: pulls items from the ring; the PV cursor follows through a
       // short local queue (it lags by at most the chunks in flight)
       constexpr int NQUEUE = 8;
@@ -364,7 +406,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
         if (have_q) {
-          if (qj == 0 && !q_ready && ptx::mbar_test_wait(sm.bar(B_Q_FULL), qk & 1)) {
+          if (qj == 0 && !q_ready && ptx::mbar_test_wait(sm.bar(b_qfull), qk & 1)) {
             q_ready = true;
             progress = true;
           }
@@ -374,19 +416,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               ptx::mbar_test_wait(sm.bar(B_S_EMPTY + b), ((uint32_t)(nq >> 1) & 1) ^ 1)) {
             ptx::tc_fence_after();
             const uint32_t kbase = sm.base_u32 + OFF_K + s * TILE_B;
+            if constexpr (FP8) {
+              // S = sum over the three q parts of part K^T: rows and keys are
+              // 128-byte rows (all of d), 32 bytes of d per MMA
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t da =
-                  ptx::smem_desc_sw128(qbase + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
-              const uint64_t db =
-                  ptx::smem_desc_sw128(kbase + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
-              ptx::tc_mma_f16(tmem + S_COL + CHK * b, da, db, IDESC_QK, kk > 0);
+              for (int part = 0; part < 3; ++part)
+#pragma unroll
+                for (int kk = 0; kk < D / 32; ++kk) {
+                  const uint64_t da =
+                      ptx::smem_desc_sw128(qbase + part * QPART_B + kk * 32, 16, 1024);
+                  const uint64_t db = ptx::smem_desc_sw128(kbase + kk * 32, 16, 1024);
+                  ptx::tc_mma_f8(tmem + S_COL + CHK * b, da, db, IDESC_QK, part > 0 || kk > 0);
+                }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t da =
+                    ptx::smem_desc_sw128(qbase + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
+                const uint64_t db =
+                    ptx::smem_desc_sw128(kbase + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
+                ptx::tc_mma_f16(tmem + S_COL + CHK * b, da, db, IDESC_QK, kk > 0);
+              }
             }
             ptx::tc_commit(sm.bar(B_S_FULL + b));
             ptx::tc_commit(sm.bar(B_EMPTY_K + s));  // the K chunk may be reloaded
             ++nq;
             if (++qj == qit.nch) {
-              ptx::tc_commit(sm.bar(B_Q_EMPTY));  // the q tile may be reloaded
+              ptx::tc_commit(sm.bar(b_qempty));  // the q tile (parts) may be rewritten
               qj = 0;
               ++qk;
               q_ready = false;
@@ -406,14 +462,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ptx::tc_fence_after();
             const uint32_t vbase = sm.base_u32 + OFF_V + s * TILE_B;
             const uint32_t pbase = sm.base_u32 + OFF_P;
-            // A = P, K-major (64 keys per 128-byte swizzled half); B = V read
-            // MN-major (16 keys per MMA, d halves HALF_B apart)
+            if constexpr (FP8) {
+              // O^T (tensor-memory lane = d, column = q row) += V^T P^T: A = the
+              // V chunk read MN-major (a 128-byte row is all of d; 32 keys per
+              // MMA), B = the two e4m3 parts of P, K-major (a q row's 128 keys
+              // in one 128-byte row)
 #pragma unroll
-            for (int kk = 0; kk < CHK / 16; ++kk) {
-              const uint64_t da =
-                  ptx::smem_desc_sw128(pbase + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
-              const uint64_t db = ptx::smem_desc_sw128(vbase + kk * 2048, HALF_B, 1024);
-              ptx::tc_mma_f16(tmem + O_COL, da, db, IDESC_PV, pj > 0 || kk > 0);
+              for (int part = 0; part < 2; ++part)
+#pragma unroll
+                for (int kk = 0; kk < CHK / 32; ++kk) {
+                  const uint64_t da = ptx::smem_desc_sw128(vbase + kk * 4096, TILE_B, 1024);
+                  const uint64_t db =
+                      ptx::smem_desc_sw128(pbase + part * PPART_B + kk * 32, 16, 1024);
+                  ptx::tc_mma_f8(tmem + O_COL, da, db, IDESC_PV, pj > 0 || part > 0 || kk > 0);
+                }
+            } else {
+              // A = P, K-major (64 keys per 128-byte swizzled half); B = V read
+              // MN-major (16 keys per MMA, d halves HALF_B apart)
+#pragma unroll
+              for (int kk = 0; kk < CHK / 16; ++kk) {
+                const uint64_t da =
+                    ptx::smem_desc_sw128(pbase + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
+                const uint64_t db = ptx::smem_desc_sw128(vbase + kk * 2048, HALF_B, 1024);
+                ptx::tc_mma_f16(tmem + O_COL, da, db, IDESC_PV, pj > 0 || kk > 0);
+              }
             }
             ptx::tc_commit(sm.bar(B_O_FULL + b));
             ptx::tc_commit(sm.bar(B_P_EMPTY));
@@ -444,7 +516,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         drain_bar(sm.bar(B_S_FULL + (int)((nq - 1) & 1)), (uint32_t)((nq - 1) >> 1) & 1);
         drain_bar(sm.bar(B_EMPTY_K + (int)((nq - 1) % NSTK)), (uint32_t)((nq - 1) / NSTK) & 1);
       }
-      if (qk > 0) drain_bar(sm.bar(B_Q_EMPTY), (qk - 1) & 1);
+      if (qk > 0) drain_bar(sm.bar(b_qempty), (qk - 1) & 1);
       if (npv > 0) {
         const long long L = npv - 1;
         drain_bar(sm.bar(B_EMPTY_V + (int)(L % NSTV)), (uint32_t)(L / NSTV) & 1);
@@ -473,6 +545,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       return xch[tid ^ 128];
     };
     long long ck = 0;
+    int qk_s = 0;  // items with chunks so far (e4m3: q tiles converted)
+    const float ksc = FP8 ? __ldg(p.k_scale) : 1.f;
+    const float vsc = FP8 ? __ldg(p.v_scale) : 1.f;
     for (int k = 0;; ++k) {
       const long long i = read_item(k, lane == 0);
       if (i >= total) break;
@@ -491,6 +566,65 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int lim = row_ok ? it.ctx + rt + 1 : 0;  // keys < lim are visible to the row
       float m_ref = -INFINITY, l = 0.f;
       bool good = true;
+      float rs = p.scale_log2;  // logit scale of this row, log2 units
+      if constexpr (FP8) {
+        // ---- the q tile's three e4m3 parts (the MMA's A operand) ----
+        // Row r of the staged bf16 tile, scaled by the power of two 2^e that
+        // puts its max |q| in [128, 256), is hi + mid + lo, each part the
+        // e4m3 rounding of what the previous ones leave (exact residuals):
+        // about 2^-12 relative.  2^-e and k_scale fold into the row's scale.
+        good = wait_bar(sm, sm.bar(B_Q_FULL), qk_s & 1, p.err, 31);
+        const unsigned char* qrow = sm.base + OFF_Q + half * HALF_B + row * 128;
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(qrow + ((c ^ (row & 7)) << 4));
+          w[4 * c] = v.x;
+          w[4 * c + 1] = v.y;
+          w[4 * c + 2] = v.z;
+          w[4 * c + 3] = v.w;
+        }
+        ptx::mbar_arrive(sm.bar(B_Q_EMPTY));  // the staged tile may be reloaded
+        float amax = 0.f;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[c])), fabsf(bf16_hi(w[c]))));
+        amax = fmaxf(amax, partner(amax));
+        const int eb = (int)(__float_as_uint(amax) >> 23);  // 0 for zero / subnormal
+        const int e = max(-126, min(126, eb == 0 ? 0 : 134 - eb));
+        const float mul = __int_as_float((127 + e) << 23);
+        rs = p.scale_log2 * ksc * __int_as_float((127 - e) << 23);
+        if (qk_s > 0) good = wait_bar(sm, sm.bar(B_QP_EMPTY), (qk_s - 1) & 1, p.err, 32) && good;
+        unsigned char* qp = sm.base + OFF_QP + row * 128;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {  // 16 values of d: one 16-byte piece per part
+          uint32_t pw[3][4];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const uint32_t w0 = w[c4 * 8 + 2 * q4], w1 = w[c4 * 8 + 2 * q4 + 1];
+            float a0 = bf16_lo(w0) * mul, a1 = bf16_hi(w0) * mul;
+            float a2 = bf16_lo(w1) * mul, a3 = bf16_hi(w1) * mul;
+#pragma unroll
+            for (int part = 0; part < 3; ++part) {
+              const uint16_t c01 = pack_e4m3x2_rn(a0, a1), c23 = pack_e4m3x2_rn(a2, a3);
+              const float2 f01 = e4m3x2_to_float2(c01), f23 = e4m3x2_to_float2(c23);
+              a0 -= f01.x;
+              a1 -= f01.y;
+              a2 -= f23.x;
+              a3 -= f23.y;
+              pw[part][q4] = (uint32_t)c01 | ((uint32_t)c23 << 16);
+            }
+          }
+          const int o = (((half * 4 + c4) ^ (row & 7)) << 4);
+#pragma unroll
+          for (int part = 0; part < 3; ++part)
+            *reinterpret_cast<uint4*>(qp + part * QPART_B + o) =
+                make_uint4(pw[part][0], pw[part][1], pw[part][2], pw[part][3]);
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(sm.bar(B_QP_FULL));
+        ++qk_s;
+      }
       for (int j = 0; j < it.nch; ++j, ++ck) {
         const int b = (int)(ck & 1);
         const uint32_t bph = (uint32_t)(ck >> 1) & 1;
@@ -529,8 +663,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         const float hm = fmaxf(fmaxf(hm4[0], hm4[1]), fmaxf(hm4[2], hm4[3]));
         // the row's chunk max in log2 units, the same in both threads
-        const float cm = fmaxf(hm, partner(hm)) * p.scale_log2;
-        if (cm > m_ref + kRescaleLog2) {
+        const float cm = fmaxf(hm, partner(hm)) * rs;
+        if constexpr (FP8) {
+          // O^T: row r of O is column r of the tensor-memory tile, spread over
+          // all 128 lanes (d).  Each row publishes its factor (1 when it keeps
+          // its reference max); if any row rescales, every thread rescales its
+          // 64 columns once the previous chunk's PV has landed.  The factors
+          // alternate between two buffers by chunk, and the reduction barrier
+          // below is passed by every thread once per chunk, so a buffer is
+          // rewritten only after every thread has used it.
+          float alpha = 1.f;
+          if (cm > m_ref + kRescaleLog2) {
+            if (m_ref != -INFINITY) alpha = fast_exp2(m_ref - cm);
+            m_ref = cm;
+          }
+          float* al = reinterpret_cast<float*>(sm.base + C::OFF_ALPHA) + (int)(ck & 1) * 128;
+          if (half == 0) al[row] = alpha;
+          if (ptx::bar_red_or(9, NSOFT, alpha != 1.f)) {
+            const long long L = ck - 1;
+            wait_bar(sm, sm.bar(B_O_FULL + (int)(L & 1)), (uint32_t)(L >> 1) & 1, p.err, 24);
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+              float o[32];
+              const uint32_t ta = tmem + lane_base + O_COL + half * 64 + 32 * q2;
+              ptx::tmem_ld_x32(ta, o);
+              ptx::tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] *= al[half * 64 + 32 * q2 + e];
+              ptx::tmem_st_x32(ta, o);
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+          }
+          l *= alpha;
+        } else if (cm > m_ref + kRescaleLog2) {
           if (m_ref != -INFINITY) {
             // rescale this half of the row of O (earlier chunks): after their PV
             const float alpha = fast_exp2(m_ref - cm);
@@ -561,41 +728,109 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (kc < CHK) {
             wait_bar(sm, sm.bar(B_FULL_V + s), ph, p.err, 26);
             if (row >= kc) {
-              // this thread's 64 columns of V row `row`
-              unsigned char* vrow = sm.base + OFF_V + s * TILE_B + half * HALF_B + row * 128;
+              // this thread's 64 columns of V row `row` (e4m3: bytes half * 64
+              // .. of the 128-byte row; bf16: the row's 64-column half)
+              if constexpr (FP8) {
+                unsigned char* vrow = sm.base + OFF_V + s * TILE_B + row * 128;
 #pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                const int cc = (c + row) & 7;
-                *reinterpret_cast<uint4*>(vrow + cc * 16) = make_uint4(0, 0, 0, 0);
+                for (int c = 0; c < 4; ++c)
+                  *reinterpret_cast<uint4*>(vrow + (((half * 4 + c) ^ (row & 7)) << 4)) =
+                      make_uint4(0, 0, 0, 0);
+              } else {
+                unsigned char* vrow = sm.base + OFF_V + s * TILE_B + half * HALF_B + row * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                  const int cc = (c + row) & 7;
+                  *reinterpret_cast<uint4*>(vrow + cc * 16) = make_uint4(0, 0, 0, 0);
+                }
               }
             }
           }
         }
-        // keys half * 64 ..: the row's 128-byte half `half` of the P tile
-        unsigned char* prow = sm.base + OFF_P + half * HALF_B + row * 128;
         float l4[4] = {0.f, 0.f, 0.f, 0.f};  // this chunk's sum, four chains
+        if constexpr (FP8) {
+          // 2^(8 - R) p (at most 256) as hi + lo e4m3 parts: bytes half * 64 ..
+          // of the row's 128-byte row in each part; the sum adds the parts, so
+          // the factor and the rounding cancel in O / l
+          unsigned char* prow = sm.base + OFF_P + row * 128;
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          uint32_t w[4];
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t hw[4], lw[4];
 #pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const int e = (c8 & 3) * 8 + 2 * e2;
-            // p = 2^(s * scale - m): one FMA per logit (masked logits are -inf)
-            const float p0 = fast_exp2(fmaf(sv[c8 >> 2][e], p.scale_log2, -msafe));
-            const float p1 = fast_exp2(fmaf(sv[c8 >> 2][e + 1], p.scale_log2, -msafe));
-            l4[e2] += p0 + p1;  // before the bf16 rounding the MMA sees: within its error
-            const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-            w[e2] = *reinterpret_cast<const uint32_t*>(&pb);
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int e = c4 * 16 + q4 * 4;  // key among this thread's 64
+              float x[4];
+#pragma unroll
+              for (int t4 = 0; t4 < 4; ++t4)
+                x[t4] = fast_exp2(fmaf(sv[(e + t4) >> 5][(e + t4) & 31], rs, -msafe)) * C::kPScale;
+              const uint16_t h01 = pack_e4m3x2_rn(x[0], x[1]), h23 = pack_e4m3x2_rn(x[2], x[3]);
+              const float2 f01 = e4m3x2_to_float2(h01), f23 = e4m3x2_to_float2(h23);
+              const uint16_t g01 = pack_e4m3x2_rn(x[0] - f01.x, x[1] - f01.y);
+              const uint16_t g23 = pack_e4m3x2_rn(x[2] - f23.x, x[3] - f23.y);
+              const float2 r01 = e4m3x2_to_float2(g01), r23 = e4m3x2_to_float2(g23);
+              l4[q4] += ((f01.x + r01.x) + (f01.y + r01.y)) + ((f23.x + r23.x) + (f23.y + r23.y));
+              hw[q4] = (uint32_t)h01 | ((uint32_t)h23 << 16);
+              lw[q4] = (uint32_t)g01 | ((uint32_t)g23 << 16);
+            }
+            const int o = (((half * 4 + c4) ^ (row & 7)) << 4);
+            *reinterpret_cast<uint4*>(prow + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(prow + PPART_B + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
-          *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+          // keys half * 64 ..: the row's 128-byte half `half` of the P tile
+          unsigned char* prow = sm.base + OFF_P + half * HALF_B + row * 128;
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const int e = (c8 & 3) * 8 + 2 * e2;
+              // p = 2^(s * scale - m): one FMA per logit (masked logits are -inf)
+              const float p0 = fast_exp2(fmaf(sv[c8 >> 2][e], rs, -msafe));
+              const float p1 = fast_exp2(fmaf(sv[c8 >> 2][e + 1], rs, -msafe));
+              l4[e2] += p0 + p1;  // before the bf16 rounding the MMA sees: within its error
+              const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+              w[e2] = *reinterpret_cast<const uint32_t*>(&pb);
+            }
+            *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
         }
         l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(sm.bar(B_P_FULL));
       }
       // ---- epilogue: this half of the row of O after the item's last PV ----
-      {
+      if constexpr (FP8) {
+        // O^T: this thread holds element d = its lane of the 64 q rows of its
+        // half (columns).  Every row's sum is published first (0 for rows past
+        // the tile's tokens, which are not stored).
+        const long long L = ck - 1;
+        wait_bar(sm, sm.bar(B_O_FULL + (int)(L & 1)), (uint32_t)(L >> 1) & 1, p.err, 27);
+        ptx::tc_fence_after();
+        const float lsum = l + partner(l);
+        float* ls = reinterpret_cast<float*>(sm.base + C::OFF_LSUM);
+        if (half == 0) ls[row] = row_ok ? lsum : 0.f;
+        ptx::bar_sync_named(10, NSOFT);
+        __nv_bfloat16* ocol = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                              ((int64_t)(it.q0 + it.qt * MQ) * p.num_heads + it.g * G) * D + row;
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          float o[32];
+          ptx::tmem_ld_x32(tmem + lane_base + O_COL + half * 64 + 32 * q2, o);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int r = half * 64 + 32 * q2 + e;  // q row of the tile: token r / G, head r % G
+            const float lr = ls[r];
+            if (lr > 0.f)
+              ocol[((int64_t)(r / G) * p.num_heads + (r % G)) * D] =
+                  __float2bfloat16_rn((o[e] * vsc) / lr);
+          }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(sm.bar(B_O_EMPTY));
+      } else {
         const long long L = ck - 1;
         wait_bar(sm, sm.bar(B_O_FULL + (int)(L & 1)), (uint32_t)(L >> 1) & 1, p.err, 27);
         ptx::tc_fence_after();
@@ -637,27 +872,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 // ---------------- host side ----------------
 
-template <int G>
+template <int G, bool FP8>
 cudaError_t launch_g(const Params& prm, const CUtensorMap& mk, const CUtensorMap& mv,
                      const CUtensorMap& mq, int num_ctas, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<G, FP8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         PCfg<FP8>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_ctas);
   cfg.blockDim = dim3(NTHREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = PCfg<FP8>::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<G>, mk, mv, mq, prm);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<G, FP8>, mk, mv, mq, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -667,7 +903,7 @@ cudaError_t launch_g(const Params& prm, const CUtensorMap& mk, const CUtensorMap
 bool prefill_supported(int head_dim, int group, bool fp8, int num_seqs, int block_size) {
   // block_size >= 8 keeps every K/V box 1024-byte aligned in smem (whole
   // 128-byte-swizzle atoms), as in the decode kernels
-  return !fp8 && head_dim == pf::D && (group == 1 || group == 2 || group == 4 || group == 8) &&
+  return head_dim == pf::D && (group == 1 || group == 2 || group == 4 || group == 8) &&
          num_seqs <= pf::kMaxReqs && block_size >= 8 && tc::encode_fn() != nullptr;
 }
 
@@ -680,20 +916,28 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream) {
   CUtensorMap mk, mv, mq;
   {
     // [blocks, block_size, H_kv, d] as in the decode kernels: a box is one
-    // 64-column half of box_tok tokens of one KV head
+    // 128-byte column block (64 bf16 or all 128 e4m3 of d) of box_tok tokens
+    // of one KV head
+    const cuuint64_t elt = a.fp8 ? 1 : 2;
+    const CUtensorMapDataType dt =
+        a.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    // L2 fills of a row's own size (a 256-byte fill of a 128-byte e4m3 row
+    // would also pull the next KV head's row)
+    const CUtensorMapL2promotion promo =
+        a.fp8 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)a.num_kv_heads, (cuuint64_t)a.block_size,
                           (cuuint64_t)a.num_blocks};
-    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)a.num_kv_heads * D * 2,
-                             (cuuint64_t)a.block_size * a.num_kv_heads * D * 2};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)box_tok, 1};
+    cuuint64_t strides[3] = {(cuuint64_t)D * elt, (cuuint64_t)a.num_kv_heads * D * elt,
+                             (cuuint64_t)a.block_size * a.num_kv_heads * D * elt};
+    cuuint32_t box[4] = {(cuuint32_t)(128 / elt), 1, (cuuint32_t)box_tok, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
-    if (enc(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.k_cache), dims, strides,
-            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (enc(&mk, dt, 4, const_cast<void*>(a.k_cache), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-    if (enc(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.v_cache), dims, strides,
-            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (enc(&mv, dt, 4, const_cast<void*>(a.v_cache), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
   {
@@ -734,11 +978,22 @@ cudaError_t launch_prefill_tc(const PrefillLaunch& a, cudaStream_t stream) {
   while ((1 << lx) < box_tok) ++lx;
   prm.log2_box = lx;
   prm.scale_log2 = a.scale * 1.4426950408889634f;
+  prm.k_scale = a.k_scale;
+  prm.v_scale = a.v_scale;
+  if (a.fp8) {
+    switch (group) {
+      case 1: return launch_g<1, true>(prm, mk, mv, mq, a.num_ctas, stream);
+      case 2: return launch_g<2, true>(prm, mk, mv, mq, a.num_ctas, stream);
+      case 4: return launch_g<4, true>(prm, mk, mv, mq, a.num_ctas, stream);
+      case 8: return launch_g<8, true>(prm, mk, mv, mq, a.num_ctas, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (group) {
-    case 1: return launch_g<1>(prm, mk, mv, mq, a.num_ctas, stream);
-    case 2: return launch_g<2>(prm, mk, mv, mq, a.num_ctas, stream);
-    case 4: return launch_g<4>(prm, mk, mv, mq, a.num_ctas, stream);
-    case 8: return launch_g<8>(prm, mk, mv, mq, a.num_ctas, stream);
+    case 1: return launch_g<1, false>(prm, mk, mv, mq, a.num_ctas, stream);
+    case 2: return launch_g<2, false>(prm, mk, mv, mq, a.num_ctas, stream);
+    case 4: return launch_g<4, false>(prm, mk, mv, mq, a.num_ctas, stream);
+    case 8: return launch_g<8, false>(prm, mk, mv, mq, a.num_ctas, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -121,12 +121,10 @@ def test_tiles_repeatable_bit_for_bit():
 
 
 @requires_gpu
-@pytest.mark.parametrize("what", ["head_dim", "fp8", "block4", "group16"])
+@pytest.mark.parametrize("what", ["head_dim", "block4", "group16"])
 def test_tiles_refuse_shapes_they_do_not_serve(what):
     if what == "head_dim":
         c = _setup([40, 20], [10, 20], 8, 2, 64, 16, seed=117)
-    elif what == "fp8":
-        c = _setup([40, 20], [10, 20], 32, 8, 128, 16, "fp8", seed=117)
     elif what == "block4":
         c = _setup([40, 20], [10, 20], 32, 8, 128, 4, seed=117)
     else:
@@ -148,3 +146,55 @@ def test_automatic_choice_on_a_step_mixing_one_prefill_with_decodes(hq, hkv):
     got = _check(c, 128 ** -0.5, method=0)
     per_token = _run(c, 128 ** -0.5, method=1)
     harness.assert_close(got, per_token, False)
+
+
+# ---- e4m3 cache: kind::f8f6f4 tiles, q and P split into e4m3 parts ----
+
+@requires_gpu
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (16, 16), (16, 8), (64, 8)])
+def test_tiles_fp8_mixed_step(hq, hkv):
+    g = hq // hkv
+    mq = 128 // g
+    seq = [700, 300, 1500, 129, mq + 5, 2 * mq, 40]
+    new = [200, 300, 1, 129, mq + 1, mq - 1, 40]
+    c = _setup(seq, new, hq, hkv, 128, 16, "fp8", seed=130 + g)
+    _check(c, 128 ** -0.5)
+
+
+@requires_gpu
+@pytest.mark.parametrize("block_size", [8, 64, 256])
+def test_tiles_fp8_block_sizes_and_long_chunks(block_size):
+    c = _setup([2048, 3512, 257], [2048, 512, 257], 32, 8, 128, block_size, "fp8",
+               seed=140 + block_size)
+    _check(c, 128 ** -0.5)
+
+
+@requires_gpu
+def test_tiles_fp8_query_magnitudes_and_per_token_agreement():
+    # rows of very different size: each row gets its own power-of-two scale
+    c = _setup([900, 450, 77], [300, 450, 20], 32, 8, 128, 16, "fp8", seed=150)
+    q = c["q"].astype(np.uint32) << 16
+    f = q.view(np.float32)
+    f[::3] *= np.float32(40.0)
+    f[1::3] *= np.float32(1e-3)
+    c["q"] = (f.view(np.uint32) >> 16).astype(np.uint16)
+    tiles = _check(c, 0.08)
+    per_token = _run(c, 0.08, method=1)
+    harness.assert_close(tiles, per_token, True)
+
+
+@requires_gpu
+def test_tiles_fp8_repeatable_bit_for_bit():
+    c = _setup([1200, 640], [600, 640], 32, 8, 128, 16, "fp8", seed=151)
+    a = _run(c, 0.09)
+    b = _run(c, 0.09)
+    assert np.array_equal(a, b)
+
+
+@requires_gpu
+def test_automatic_choice_fp8_mixed_step():
+    rng = np.random.default_rng(160)
+    seq = [1500] + [int(x) for x in rng.integers(1, 4000, size=30)]
+    new = [600] + [1] * 30
+    c = _setup(seq, new, 32, 8, 128, 16, "fp8", seed=161)
+    _check(c, 128 ** -0.5, method=0)
