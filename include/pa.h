@@ -346,9 +346,12 @@ pa_status pa_varlen_attention(void* out, const void* q, const void* k_cache, con
  *            (token, query head) rows on the MMA's M side against 128-key
  *            chunks of the paged context, online softmax with one thread per
  *            row and O kept in tensor memory; the context is read once per
- *            tile.  Needs a bf16 cache, head_dim 128, G in {1, 2, 4, 8},
- *            block_size >= 8, at most 256 requests and scale > 0, else
- *            PA_ERR_UNSUPPORTED.  Sets workspace word 0 (int32) to a nonzero
+ *            tile.  For an e4m3 cache the MMAs take the cache bytes as they
+ *            are (kind::f8f6f4): each q row is split into three e4m3 parts
+ *            under its own power-of-two scale and the weights into two, and
+ *            P V is computed as its transpose.  Needs head_dim 128, G in
+ *            {1, 2, 4, 8}, block_size >= 8, at most 256 requests and
+ *            scale > 0, else PA_ERR_UNSUPPORTED.  Sets workspace word 0 (int32) to a nonzero
  *            code if a bounded internal wait expired or a block id was out of
  *            range; the library never clears it.  Workspace word 1 is the
  *            tiles' work counter, zeroed on `stream` before each launch (an
