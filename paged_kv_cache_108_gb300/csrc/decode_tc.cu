@@ -73,13 +73,16 @@ constexpr int D = 128;
 constexpr int NQ = 16;                 // MMA N of PV: query heads (bf16), hi/lo rows of P (fp8)
 constexpr int kMaxSeqs = 1024;
 constexpr int kMaxCols = 16;           // columns of a unit (the MMA N of PV)
-// block-id ring: 4 chunks x up to 256 ids (a 256-token e4m3 chunk of 1-token
-// blocks)
-constexpr int TAB_SLOTS = 4, TAB_AHEAD = 3, TAB_W = 256;
+constexpr int TAB_SLOTS = 4, TAB_AHEAD = 3;  // block-id ring: 4 chunks, fetched 3 ahead
 
-// Shared-memory layout and roles for a bf16 or an fp8-e4m3 cache.
-template <bool FP8>
+// Shared-memory layout and roles for a bf16 or an fp8-e4m3 cache, with K/V
+// rows arriving as TMA boxes or (GATHER, block_size < 8) gathered by cp.async.
+template <bool FP8, bool GATHER>
 struct Cfg {
+  // block ids per chunk in the ring: one per TMA box (block_size >= 8 keeps a
+  // chunk within 32 boxes), or one per block of a gathered chunk (up to a
+  // 256-token e4m3 chunk of 1-token blocks)
+  static constexpr int TAB_W = GATHER ? 256 : 32;
   // tokens per chunk: 128 bf16 or 256 e4m3 rows, 32 KiB of K and 32 of V
   static constexpr int CH = FP8 ? 256 : 128;
   static constexpr int NHALF = CH / 128;        // 128-token halves (one logits MMA each)
@@ -155,20 +158,19 @@ struct Params {
   const float* v_scale;
   unsigned long long epoch;  // 48-bit tag of this call
   int early_meta;            // previous kernel wrote only the cache
-  // block_size < 8: K/V rows are gathered with 16-byte cp.async copies
-  // instead of TMA boxes (a box of fewer than 8 rows cannot fill a whole
-  // 1024-byte swizzle atom); kc / vc are the caches' base addresses
-  int gather;
+  // the caches' base addresses, for the gathered copies (block_size < 8: a
+  // TMA box of fewer than 8 rows cannot fill a whole 1024-byte swizzle atom)
   const unsigned char* kc;
   const unsigned char* vc;
 };
 
-template <int G, bool FP8>
-__global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
+template <int G, bool FP8, bool GATHER>
+__global__ void __launch_bounds__(Cfg<FP8, GATHER>::NTHREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_q, const Params p) {
-  using Cf = Cfg<FP8>;
+  using Cf = Cfg<FP8, GATHER>;
+  constexpr int TAB_W = Cf::TAB_W;
   constexpr int CH = Cf::CH, NHALF = Cf::NHALF, NQ_S = Cf::NQ_S, S_W = Cf::S_W,
                 O_COL = Cf::O_COL, TMEM_COLS = Cf::TMEM_COLS;
   using Walk = ChunkWalk<CH>;
@@ -218,7 +220,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
       if ((i >= B_S_EMPTY && i < B_S_EMPTY + 2) || (i >= B_P_FULL && i < B_P_FULL + 2) ||
           (i >= B_O_EMPTY && i < B_O_EMPTY + 2) || (i >= B_EPI && i < B_EPI + 2))
         cnt = 128;
-      if (p.gather && i < B_EMPTY) cnt = 32;  // gathered rows: every producer lane arrives
+      if (GATHER && i < B_EMPTY) cnt = 32;  // gathered rows: every producer lane arrives
       if (FP8 && i >= B_Q_FULL && i < B_Q_FULL + 2) cnt = 32;        // the q warp's lanes
       if (FP8 && i >= B_Q_EMPTY && i < B_Q_EMPTY + 2) cnt = 1 + 128;  // MMA + softmax threads
       ptx::mbar_init(sm.bar(i), cnt);
@@ -332,8 +334,13 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
     auto fetch_ids = [&](const Walk& w, int slot) {
       const int nb = (w.valid() + p.box_tok - 1) >> p.log2_box;
       const int32_t* row = p.block_tables + (int64_t)w.seq * p.max_blocks;
-      for (int e = lane; e < nb; e += 32)
-        cp_async_4(tab + (slot * TAB_W + e) * 4, row + ((w.j * CH + e * p.box_tok) >> p.log2_bs));
+      if constexpr (GATHER) {
+        for (int e = lane; e < nb; e += 32)
+          cp_async_4(tab + (slot * TAB_W + e) * 4, row + ((w.j * CH + e * p.box_tok) >> p.log2_bs));
+      } else if (lane < nb) {
+        cp_async_4(tab + (slot * TAB_W + lane) * 4,
+                   row + ((w.j * CH + lane * p.box_tok) >> p.log2_bs));
+      }
     };
     walk.init(lo, hi, seq_lo, seq_hi);
     Walk ahead = walk;
@@ -363,7 +370,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
       const int cs = walk.j * CH;
       const int valid = walk.valid();
       const int nbox = (valid + p.box_tok - 1) >> p.log2_box;
-      if (!p.gather || local == 0) cp_async_wait<TAB_AHEAD - 1>();  // this chunk's ids have landed
+      if (!GATHER || local == 0) cp_async_wait<TAB_AHEAD - 1>();  // this chunk's ids have landed
       const int phys_in = lane < nbox ? tab_s[(local % TAB_SLOTS) * TAB_W + lane] : 0;
       if (!wait_bar(sm, sm.bar(B_EMPTY + s), ph ^ 1, p.err, 1)) break;
       if (!FP8 && isk && walk.first_of_segment()) {
@@ -385,7 +392,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
       if (p.early_meta && local == 0) ptx::grid_dependency_wait();
       const uint32_t kdst = sm.base_u32 + OFF_K + s * TILE_B;
       const uint32_t vdst = sm.base_u32 + OFF_V + s * TILE_B;
-      if (p.gather) {
+      if constexpr (GATHER) {
         // Eight lanes per row, four rows per step: lane l copies 16-byte
         // piece l % 8 of row 4 * step + l / 8 (bf16: of both 128-byte column
         // blocks), so one instruction moves four whole 128-byte row pieces.
@@ -456,18 +463,18 @@ __global__ void __launch_bounds__(Cfg<FP8>::NTHREADS, 1)
         ahead.next();
       }
       cp_async_commit();
-      if (p.gather && local > 0) {
+      if (GATHER && local > 0) {
         cp_async_wait<3>();  // rows(local - 1) and ids(local + 1) have landed
         publish(local - 1);
       }
     }
     cp_async_wait<0>();
-    if (p.gather && local > 0) publish(local - 1);
+    if (GATHER && local > 0) publish(local - 1);
     // drain: the last loads issued must land before the CTA can exit
     // (gathered rows have landed already: every copy group is complete)
     __syncwarp();
     if (lane == 0) {
-      if (!p.gather)
+      if (!GATHER)
         for (int l = max(0, local - NST); l < local; ++l) {
           if (isk) drain_bar(sm.bar(B_FULL_K + l % NST), (l / NST) & 1);
           if (isv) drain_bar(sm.bar(B_FULL_V + l % NST), (l / NST) & 1);
@@ -1038,21 +1045,22 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-template <int G, bool FP8>
-cudaError_t launch_g(const TcLaunch& a, const Params& prm, const CUtensorMap& mk,
-                     const CUtensorMap& mv, const CUtensorMap& mq, cudaStream_t stream) {
+template <int G, bool FP8, bool GATHER>
+cudaError_t launch_g3(const Params& prm, const CUtensorMap& mk, const CUtensorMap& mv,
+                      const CUtensorMap& mq, cudaStream_t stream) {
+  using Cf = Cfg<FP8, GATHER>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<G, FP8>,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<G, FP8, GATHER>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<FP8>::SMEM_BYTES);
+                                         Cf::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(prm.num_ctas);
-  cfg.blockDim = dim3(Cfg<FP8>::NTHREADS);
-  cfg.dynamicSmemBytes = Cfg<FP8>::SMEM_BYTES;
+  cfg.blockDim = dim3(Cf::NTHREADS);
+  cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   // programmatic dependent launch: the prologue may overlap the previous
@@ -1061,9 +1069,17 @@ cudaError_t launch_g(const TcLaunch& a, const Params& prm, const CUtensorMap& mk
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<G, FP8>, mk, mv, mq, prm);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<G, FP8, GATHER>, mk, mv, mq, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// block_size < 8: the instantiation that gathers rows by cp.async
+template <int G, bool FP8>
+cudaError_t launch_g(const TcLaunch& a, const Params& prm, const CUtensorMap& mk,
+                     const CUtensorMap& mv, const CUtensorMap& mq, cudaStream_t stream) {
+  return a.block_size < 8 ? launch_g3<G, FP8, true>(prm, mk, mv, mq, stream)
+                          : launch_g3<G, FP8, false>(prm, mk, mv, mq, stream);
 }
 
 }  // namespace tc
@@ -1184,7 +1200,6 @@ cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream) {
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   prm.early_meta = a.early_meta ? 1 : 0;
   prm.epoch = next_call_epoch();
-  prm.gather = a.block_size < 8 ? 1 : 0;
   prm.kc = static_cast<const unsigned char*>(a.k_cache);
   prm.vc = static_cast<const unsigned char*>(a.v_cache);
   const int G = gq * ntok;  // columns of a unit
