@@ -218,6 +218,10 @@ int pa_decode_auto_kernel(const pa_cache_desc& cache, int32_t num_heads, int32_t
   const bool fp8 = cache.dtype == PA_KV_FP8_E4M3;
   if (pa::hp_supported(cache.head_dim, group, fp8, num_seqs, cache.num_kv_heads,
                        cache.block_size, tokens_per_seq)) {
+    // Below 8 tokens per block a per-head tile would be gathered row by row
+    // (256 bytes each); the head-packed kernel copies a block's rows of 8
+    // or 16 heads (2 or 4 KiB per token) with one TMA box.
+    if (cache.block_size < 8) return 3;
     const int64_t hp_units = (int64_t)num_seqs * (cache.num_kv_heads / (group >= 2 ? 8 : 16));
     if (group == 1 ? 2 * hp_units >= num_sms() : hp_units >= 2 * num_sms()) return 3;
   }
@@ -287,8 +291,8 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
   if (kernel == 3 && !hp_ok)
     return pa_fail(PA_ERR_UNSUPPORTED,
                    "pa_decode: head-packed kernel needs a bf16 cache, head_dim 128, GQA group "
-                   "1, 2 or 4, num_kv_heads a multiple of 16 (group 1) or 8, block_size >= "
-                   "8 (group 1) or 16, at most 1024 sequences and one token per sequence");
+                   "1, 2 or 4, num_kv_heads a multiple of 16 (group 1) or 8, at most 1024 "
+                   "sequences and one token per sequence");
   if (hp_ok) {
     const int nsm = num_sms();
     const size_t need = pa::hp_workspace_bytes(num_seqs, num_heads, nsm);

@@ -80,8 +80,9 @@ constexpr int D = 128;
 constexpr int kMaxSeqs = 1024;
 constexpr int TAB_SLOTS = 4, TAB_AHEAD = 3;  // block-id ring: one id per chunk
 
-// G query heads per KV head (1, 2 or 4).
-template <int G>
+// G query heads per KV head (1, 2 or 4).  TM: token-major tiles, for blocks
+// of fewer than TT tokens (see the tile note above the kernel).
+template <int G, bool TM>
 struct Cfg {
   static constexpr int HB = G >= 2 ? 8 : 16;  // KV heads per tile
   static constexpr int TT = 128 / HB;         // tokens per chunk
@@ -90,6 +91,10 @@ struct Cfg {
   static constexpr int NST = 3;               // K/V ring stages (192 KiB)
   static constexpr int TILE_B = 128 * D * 2;  // one K or V tile: 128 rows of 256 bytes
   static constexpr int HALF_B = 128 * 128;    // one 64-column half of a tile
+  // Where the 64-column half h of the 8-row group a of a tile starts:
+  // head-major a * 1024 + h * HALF_B; token-major a * 2048 + h * 1024.
+  static constexpr int GRP_B = TM ? 2048 : 1024;    // between 8-row groups
+  static constexpr int HSTEP_B = TM ? 1024 : HALF_B;  // between the halves
   static constexpr int QTILE_B = N * D * 2;
   static constexpr int QHALF_B = N * 128;
   static constexpr int PTILE_B = N * 128 * 2;  // P^T: N rows of 128 bf16
@@ -97,6 +102,10 @@ struct Cfg {
   // TMEM: S[2] then O[2], N columns each
   static constexpr int TMEM_COLS = 4 * N <= 64 ? 64 : 128;
   static constexpr int NTHREADS = 256;
+  // rescale-factor buffers: three when the factors are published before the
+  // per-chunk barrier (head-major), two when after it (token-major)
+  static constexpr int NALPHA = TM ? 2 : 3;
+  static constexpr int TAB_IDS = TM ? TT : 1;  // block ids per chunk in the id ring
 
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NST * TILE_B;
@@ -112,17 +121,20 @@ struct Cfg {
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
   static constexpr int OFF_SQ = OFF_ABORT + 4;      // [3] ints: sequences of the range's ends, first
   static constexpr int OFF_FLAG = OFF_SQ + 12;      // softmax warps' broadcast word
-  static constexpr int OFF_ALPHA = OFF_FLAG + 4;    // [3][N] floats: per-chunk rescale factors
-  static constexpr int OFF_ML = OFF_ALPHA + 3 * N * 4;  // [N] float2: a piece's (m, l)
-  static constexpr int OFF_CP = OFF_ML + N * 8;          // chunk prefix per sequence, [S+1]
+  static constexpr int OFF_ALPHA = OFF_FLAG + 4;    // [NALPHA][N] floats: per-chunk rescale factors
+  static constexpr int OFF_ML = OFF_ALPHA + NALPHA * N * 4;  // [N] float2: a piece's (m, l)
+  // token-major: [2][4 warps][N] floats, each warp's chunk maxima (and, in
+  // an epilogue, its share of the column sums)
+  static constexpr int OFF_CMX = OFF_ML + N * 8;
+  static constexpr int OFF_CP = OFF_CMX + (TM ? 2 * 4 * N * 4 : 0);  // chunk prefix per sequence, [S+1]
   static constexpr int OFF_NLEN = OFF_CP + (kMaxSeqs + 1) * 4;  // clamped context lengths
   static constexpr int OFF_TAB = OFF_NLEN + kMaxSeqs * 4;       // block-id ring
-  static constexpr int SMEM_BYTES = OFF_TAB + TAB_SLOTS * 4 + 1024;  // + alignment slack
+  static constexpr int SMEM_BYTES = OFF_TAB + TAB_SLOTS * TAB_IDS * 4 + 1024;  // + alignment slack
   static_assert(N % 16 == 0 && N <= 32, "MMA N");
   static_assert(TT <= 32, "a KV head's rows stay in one warp");
   static_assert(OFF_BAR % 1024 == 0 && PHALF_B % 1024 == 0 && QHALF_B % 1024 == 0,
                 "swizzled tiles stay 1024-byte aligned");
-  static_assert(OFF_ALPHA % 16 == 0 && OFF_ML % 8 == 0, "alignment");
+  static_assert(OFF_ALPHA % 16 == 0 && OFF_ML % 8 == 0 && OFF_CMX % 16 == 0, "alignment");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
@@ -172,20 +184,22 @@ __device__ __forceinline__ void merge_step4(float& M, float& L, float4& a, float
   a.w = merge_fold(a.w, rs, w, o.w);
 }
 
-template <int G>
-__global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
+template <int G, bool TM>
+__global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
     decode_hp_kernel(const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_q, const Params p) {
-  using Cf = Cfg<G>;
+  using Cf = Cfg<G, TM>;
   constexpr int HB = Cf::HB, TT = Cf::TT, N = Cf::N, NW = Cf::NW, NST = Cf::NST;
+  constexpr int NALPHA = Cf::NALPHA, TAB_IDS = Cf::TAB_IDS, GRP_B = Cf::GRP_B,
+                HSTEP_B = Cf::HSTEP_B;
   constexpr int TILE_B = Cf::TILE_B, HALF_B = Cf::HALF_B, QTILE_B = Cf::QTILE_B,
                 QHALF_B = Cf::QHALF_B, PTILE_B = Cf::PTILE_B, PHALF_B = Cf::PHALF_B,
                 TMEM_COLS = Cf::TMEM_COLS, NTHREADS = Cf::NTHREADS;
   constexpr int OFF_K = Cf::OFF_K, OFF_V = Cf::OFF_V, OFF_Q = Cf::OFF_Q, OFF_P = Cf::OFF_P,
                 OFF_TMEM = Cf::OFF_TMEM, OFF_SQ = Cf::OFF_SQ, OFF_FLAG = Cf::OFF_FLAG,
                 OFF_ALPHA = Cf::OFF_ALPHA, OFF_ML = Cf::OFF_ML, OFF_CP = Cf::OFF_CP,
-                OFF_NLEN = Cf::OFF_NLEN, OFF_TAB = Cf::OFF_TAB;
+                OFF_NLEN = Cf::OFF_NLEN, OFF_TAB = Cf::OFF_TAB, OFF_CMX = Cf::OFF_CMX;
   constexpr int B_FULL_K = Cf::B_FULL_K, B_FULL_V = Cf::B_FULL_V, B_EMPTY = Cf::B_EMPTY,
                 B_S_FULL = Cf::B_S_FULL, B_S_EMPTY = Cf::B_S_EMPTY, B_P_FULL = Cf::B_P_FULL,
                 B_P_EMPTY = Cf::B_P_EMPTY, B_O_FULL = Cf::B_O_FULL, B_O_EMPTY = Cf::B_O_EMPTY,
@@ -310,13 +324,23 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
 
   if (warp == 4) {
     // ================= producer =================
+    // Head-major: one block id per chunk (lane 0) and four copies, each a
+    // box {64 of d, TT tokens, HB heads} of one block.  Token-major: a chunk
+    // spans TT / block_size blocks; lane i fetches the id of the chunk's
+    // block i and copies that block's rows of the HB heads, both halves of
+    // d, as one box {64 of d, 8 heads, 2 halves, HB / 8, block_size tokens},
+    // for K and for V.  Blocks wholly past the context end are not copied.
     const uint32_t tab = sm.base_u32 + OFF_TAB;
     const int* tab_s = reinterpret_cast<const int*>(sm.base + OFF_TAB);
-    // lane 0 copies the block id of a chunk TAB_AHEAD chunks ahead
+    const int bs = p.block_size;
+    // boxes (blocks) of chunk w that hold context tokens
+    auto nboxes = [&](const Walk& w) { return TM ? (w.valid() + bs - 1) >> p.log2_bs : 1; };
+    // lanes copy the block ids of a chunk TAB_AHEAD chunks ahead
     auto fetch_id = [&](const Walk& w, int slot) {
-      if (lane == 0)
-        cp_async_4(tab + slot * 4, p.block_tables + (int64_t)w.seq * p.max_blocks +
-                                       ((w.j * TT) >> p.log2_bs));
+      if (lane < nboxes(w))
+        cp_async_4(tab + (slot * TAB_IDS + lane) * 4,
+                   p.block_tables + (int64_t)w.seq * p.max_blocks + ((w.j * TT) >> p.log2_bs) +
+                       lane);
     };
     walk.init(lo, hi, seq_lo, seq_hi);
     Walk ahead = walk;
@@ -332,29 +356,48 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     for (; !walk.done(); walk.next(), ++local) {
       const int s = local % NST;
       const uint32_t ph = (local / NST) & 1;
-      cp_async_wait<TAB_AHEAD - 1>();  // this chunk's id has landed (lane 0's copy)
-      int phys = lane == 0 ? tab_s[local % TAB_SLOTS] : 0;
-      phys = __shfl_sync(0xffffffffu, phys, 0);
+      cp_async_wait<TAB_AHEAD - 1>();  // this chunk's ids have landed (each lane's own copy)
+      const int nb = nboxes(walk);
+      int phys = lane < nb ? tab_s[(local % TAB_SLOTS) * TAB_IDS + lane] : 0;
+      if (!TM) phys = __shfl_sync(0xffffffffu, phys, 0);
       if (!wait_bar(sm, sm.bar(B_EMPTY + s), ph ^ 1, p.err, 1)) break;
       if (p.early_meta && local == 0) ptx::grid_dependency_wait();
-      if ((unsigned)phys >= (unsigned)p.num_blocks) {
-        if (lane == 0) atomicExch(p.err, 3);  // bad block id: load block 0 instead of faulting
+      if ((!TM || lane < nb) && (unsigned)phys >= (unsigned)p.num_blocks) {
+        if (TM || lane == 0) atomicExch(p.err, 3);  // bad block id: load block 0 instead of faulting
         phys = 0;
       }
-      const int tok = (walk.j * TT) & (p.block_size - 1);
-      if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_K + s), (uint32_t)TILE_B);
-        ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_V + s), (uint32_t)TILE_B);
-      }
-      __syncwarp();
-      if (lane < 4) {
-        // lanes 0, 1: K halves; lanes 2, 3: V halves.  Box {64 of d, TT
-        // tokens, HB heads} at (d, token in block, first head, block).
-        const bool isk = lane < 2;
-        const int hf = lane & 1;
-        const uint32_t dst = sm.base_u32 + (isk ? OFF_K : OFF_V) + s * TILE_B + hf * HALF_B;
-        ptx::tma_load_4d(dst, isk ? (const void*)&tm_k : (const void*)&tm_v,
-                         sm.bar((isk ? B_FULL_K : B_FULL_V) + s), hf * 64, tok, walk.g * HB, phys);
+      if constexpr (TM) {
+        const uint32_t box_b = (uint32_t)bs * HB * 256;  // one block's rows of the HB heads
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_K + s), (uint32_t)nb * box_b);
+          ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_V + s), (uint32_t)nb * box_b);
+        }
+        __syncwarp();
+        if (lane < nb) {
+          const uint32_t off = s * TILE_B + lane * box_b;
+          const int slot0 = phys << p.log2_bs;  // < num_blocks * block_size <= 2^31 - 1
+          ptx::tma_load_5d(sm.base_u32 + OFF_K + off, &tm_k, sm.bar(B_FULL_K + s), 0, 0, 0,
+                           walk.g * (HB / 8), slot0);
+          ptx::tma_load_5d(sm.base_u32 + OFF_V + off, &tm_v, sm.bar(B_FULL_V + s), 0, 0, 0,
+                           walk.g * (HB / 8), slot0);
+        }
+      } else {
+        const int tok = (walk.j * TT) & (bs - 1);
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_K + s), (uint32_t)TILE_B);
+          ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_V + s), (uint32_t)TILE_B);
+        }
+        __syncwarp();
+        if (lane < 4) {
+          // lanes 0, 1: K halves; lanes 2, 3: V halves.  Box {64 of d, TT
+          // tokens, HB heads} at (d, token in block, first head, block).
+          const bool isk = lane < 2;
+          const int hf = lane & 1;
+          const uint32_t dst = sm.base_u32 + (isk ? OFF_K : OFF_V) + s * TILE_B + hf * HALF_B;
+          ptx::tma_load_4d(dst, isk ? (const void*)&tm_k : (const void*)&tm_v,
+                           sm.bar((isk ? B_FULL_K : B_FULL_V) + s), hf * 64, tok, walk.g * HB,
+                           phys);
+        }
       }
       if (!ahead.done()) {
         fetch_id(ahead, (local + TAB_AHEAD) % TAB_SLOTS);
@@ -416,7 +459,7 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint64_t da =
-                  ptx::smem_desc_sw128(kbase + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
+                  ptx::smem_desc_sw128(kbase + (kk >> 2) * HSTEP_B + (kk & 3) * 32, 16, GRP_B);
               const uint64_t db =
                   ptx::smem_desc_sw128(qbase + (kk >> 2) * QHALF_B + (kk & 3) * 32, 16, 1024);
               ptx::tc_mma_f16(tmem + N * b, da, db, IDESC_QK, kk > 0);
@@ -442,11 +485,12 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
             ptx::tc_fence_after();
             const uint32_t vbase = sm.base_u32 + OFF_V + s * TILE_B;
             const uint32_t pbase = sm.base_u32 + OFF_P + b * PTILE_B;
-            // A = V^T read MN-major from the TMA layout (16 rows per MMA);
+            // A = V^T read MN-major from the TMA layout (16 rows, two 8-row
+            // groups, per MMA; the halves of d HSTEP_B apart);
             // B = P^T, K-major, 64 rows per 128-byte swizzled half
 #pragma unroll
             for (int kk = 0; kk < 128 / 16; ++kk) {
-              const uint64_t da = ptx::smem_desc_sw128(vbase + kk * 2048, HALF_B, 1024);
+              const uint64_t da = ptx::smem_desc_sw128(vbase + kk * 2 * GRP_B, HSTEP_B, GRP_B);
               const uint64_t db =
                   ptx::smem_desc_sw128(pbase + (kk >> 2) * PHALF_B + (kk & 3) * 32, 16, 1024);
               ptx::tc_mma_f16(tmem + 2 * N + N * b, da, db, IDESC_PV, kk > 0);
@@ -552,12 +596,14 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
   } else if (warp < 4) {
     // ================= softmax + epilogue (warps 0-3) =================
     const int t = tid;           // TMEM lane: row (hh, tt) of S; element d of O
-    const int hh = t / TT;       // the row's KV head within the tile
-    const int tt = t % TT;       // the row's token within the chunk
-    const int sel = lane / TT;   // which of this warp's heads
+    const int hh = TM ? t % HB : t / TT;  // the row's KV head within the tile
+    const int tt = TM ? t / HB : t % TT;  // the row's token within the chunk
+    const int sel = lane / TT;   // head-major: which of this warp's heads
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     float* abuf = reinterpret_cast<float*>(sm.base + OFF_ALPHA);
     float2* mlb = reinterpret_cast<float2*>(sm.base + OFF_ML);
+    // token-major: [2][4][N] per-warp chunk maxima, by chunk parity
+    float* cmx = reinterpret_cast<float*>(sm.base + OFF_CMX);
     volatile int* flag = reinterpret_cast<volatile int*>(sm.base + OFF_FLAG);
     // running max per column (the same in all TT lanes of a head) and this
     // row's share of the column sums; dm, dl: those of a just-finished piece
@@ -582,24 +628,50 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     // A piece of unit `in` is done: its (m, l) per column, then the output
     // (whole unit), a partial for the merge warp, or -- the CTA's final
     // piece of a split unit -- the merge itself.
-    auto epilogue = [&](const Info& in, const float* ms, const float* ls, bool final_piece) {
-#pragma unroll
-      for (int i = 0; i < G; ++i) {
-        float v = ls[i];
-#pragma unroll
-        for (int off = TT / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (tt == 0) mlb[hh * G + i] = make_float2(ms[i], v);
-      }
-      ptx::bar_sync_named(2, 128);
+    // lsum (token-major): [4][N] floats free during the call, for the warps'
+    // shares of the column sums
+    auto epilogue = [&](const Info& in, const float* ms, const float* ls, bool final_piece,
+                        float* lsum) {
       float M[N], L[N];
+      float2 own_ml;
+      if constexpr (TM) {
+        // a column's rows are spread over the four warps: each warp sums its
+        // own, then the four shares are added in warp order
 #pragma unroll
-      for (int c = 0; c < N; ++c) {
-        const float2 v = mlb[c];
-        M[c] = v.x;
-        L[c] = v.y;
+        for (int i = 0; i < G; ++i) {
+          float v = ls[i];
+#pragma unroll
+          for (int off = HB; off < 32; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+          if (lane < HB) lsum[warp * N + hh * G + i] = v;
+          if (t < HB) mlb[hh * G + i] = make_float2(ms[i], 0.f);
+        }
+        ptx::bar_sync_named(2, 128);
+#pragma unroll
+        for (int c = 0; c < N; ++c) {
+          M[c] = mlb[c].x;
+          L[c] = ((lsum[c] + lsum[N + c]) + lsum[2 * N + c]) + lsum[3 * N + c];
+        }
+        const int oc = t < N ? t : 0;
+        own_ml = make_float2(mlb[oc].x,
+                             ((lsum[oc] + lsum[N + oc]) + lsum[2 * N + oc]) + lsum[3 * N + oc]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          float v = ls[i];
+#pragma unroll
+          for (int off = TT / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+          if (tt == 0) mlb[hh * G + i] = make_float2(ms[i], v);
+        }
+        ptx::bar_sync_named(2, 128);
+#pragma unroll
+        for (int c = 0; c < N; ++c) {
+          const float2 v = mlb[c];
+          M[c] = v.x;
+          L[c] = v.y;
+        }
+        own_ml = mlb[t < N ? t : 0];
       }
-      const float2 own_ml = mlb[t < N ? t : 0];
-      ptx::bar_sync_named(2, 128);  // all have read mlb before it is rewritten
+      ptx::bar_sync_named(2, 128);  // all have read mlb (and lsum) before they are rewritten
       const long long first = in.k - in.j;
       const long long last = first + in.nch - 1;
       const int c0 = cta_of(first, Ktot, C);
@@ -672,7 +744,7 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
     };
 
     // fold chunk L's PV result into acc with that chunk's rescale factors
-    auto acc_o = [&](int L, const Info& in, bool use_done, bool final_piece) {
+    auto acc_o = [&](int L, const Info& in, bool use_done, bool final_piece, float* lsum) {
       const int b = L & 1;
       const uint32_t bph = (L >> 1) & 1;
       float ov[N];
@@ -686,12 +758,12 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
       ptx::tmem_ld_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(sm.bar(B_O_EMPTY + b));
-      const float* al = abuf + (L % 3) * N;
+      const float* al = abuf + (L % NALPHA) * N;
 #pragma unroll
       for (int c = 0; c < N; ++c) acc[c] = acc[c] * al[c] + (good ? ov[c] : 0.f);
       if (in.last) {
-        if (use_done) epilogue(in, dm, dl, final_piece);
-        else epilogue(in, m, l, final_piece);
+        if (use_done) epilogue(in, dm, dl, final_piece, lsum);
+        else epilogue(in, m, l, final_piece, lsum);
 #pragma unroll
         for (int c = 0; c < N; ++c) acc[c] = 0.f;
       }
@@ -705,10 +777,18 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
       const int b = local & 1;
       const uint32_t bph = (local >> 1) & 1;
       // ---- logits of this chunk: this warp's heads' columns ----
-      float sl[NW];
+      // head-major: a warp's rows are whole heads, so it loads only those
+      // heads' columns; token-major: every warp holds all HB heads and each
+      // thread picks its head's G of the N columns
+      constexpr int NL = TM ? N : NW;
+      float sl[NL];
       bool good = wait_bar(sm, sm.bar(B_S_FULL + b), bph, p.err, 11);
       ptx::tc_fence_after();
-      if constexpr (NW == 8) {
+      if constexpr (NL == 32) {
+        ptx::tmem_ld_x32(tmem + lane_base + N * b, sl);
+      } else if constexpr (NL == 16) {
+        ptx::tmem_ld_x16(tmem + lane_base + N * b, sl);
+      } else if constexpr (NL == 8) {
         ptx::tmem_ld_x8(tmem + lane_base + N * b + warp * NW, sl);
       } else {
         ptx::tmem_ld_x4(tmem + lane_base + N * b + warp * NW, sl);
@@ -721,9 +801,15 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
 #pragma unroll
       for (int i = 0; i < G; ++i) {
         float v = sl[i];
+        if constexpr (TM) {
 #pragma unroll
-        for (int k = 1; k < 32 / TT; ++k)
-          if (sel == k) v = sl[k * G + i];
+          for (int k = 1; k < HB; ++k)
+            if (hh == k) v = sl[k * G + i];
+        } else {
+#pragma unroll
+          for (int k = 1; k < 32 / TT; ++k)
+            if (sel == k) v = sl[k * G + i];
+        }
         x[i] = (good && tt < valid) ? v * p.scale_log2 : -INFINITY;
       }
       // ---- chunk max per column over its head's TT rows ----
@@ -731,9 +817,30 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
 #pragma unroll
       for (int i = 0; i < G; ++i) {
         cm[i] = x[i];
+        if constexpr (TM) {
 #pragma unroll
-        for (int off = TT / 2; off > 0; off >>= 1)
-          cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], off));
+          for (int off = HB; off < 32; off <<= 1)
+            cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], off));
+        } else {
+#pragma unroll
+          for (int off = TT / 2; off > 0; off >>= 1)
+            cm[i] = fmaxf(cm[i], __shfl_xor_sync(0xffffffffu, cm[i], off));
+        }
+      }
+      if constexpr (TM) {
+        // the other warps' rows of the same heads: one exchange per chunk.
+        // This barrier also publishes the previous chunk's rescale factors.
+        float* cw = cmx + (local & 1) * 4 * N;
+        if (lane < HB) {
+#pragma unroll
+          for (int i = 0; i < G; ++i) cw[warp * N + hh * G + i] = cm[i];
+        }
+        ptx::bar_sync_named(1, 128);
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          const int c = hh * G + i;
+          cm[i] = fmaxf(fmaxf(cw[c], cw[N + c]), fmaxf(cw[2 * N + c], cw[3 * N + c]));
+        }
       }
       if (walk.first_of_segment()) {
 #pragma unroll
@@ -757,19 +864,20 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
       }
       if (tt == 0) {
 #pragma unroll
-        for (int i = 0; i < G; ++i) abuf[(local % 3) * N + hh * G + i] = alpha[i];
+        for (int i = 0; i < G; ++i) abuf[(local % NALPHA) * N + hh * G + i] = alpha[i];
       }
       // ---- P tile (and the V rows past the context end) ----
       wait_bar(sm, sm.bar(B_P_EMPTY + b), bph ^ 1, p.err, 12);
       if (valid < TT) {
         wait_bar(sm, sm.bar(B_FULL_V + s), ph, p.err, 13);
         if (tt >= valid) {
-          unsigned char* vrow = sm.base + OFF_V + s * TILE_B + t * 128;
+          // row t's two halves: group t / 8, row t % 8 within it
+          unsigned char* vrow = sm.base + OFF_V + s * TILE_B + (t >> 3) * GRP_B + (t & 7) * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const int cc = (c + t) & 7;
             *reinterpret_cast<uint4*>(vrow + cc * 16) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(vrow + HALF_B + cc * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vrow + HSTEP_B + cc * 16) = make_uint4(0, 0, 0, 0);
           }
         }
       }
@@ -786,12 +894,16 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
       }
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(sm.bar(B_P_FULL + b));
-      ptx::bar_sync_named(1, 128);  // this chunk's rescale factors are visible
+      // head-major: this chunk's rescale factors are visible after this
+      // barrier; token-major: the previous chunk's were at the max exchange
+      if (!TM) ptx::bar_sync_named(1, 128);
       // ---- fold the previous chunk's PV result ----
-      if (local > 0) acc_o(local - 1, prev, walk.first_of_segment(), false);
+      if (local > 0)
+        acc_o(local - 1, prev, walk.first_of_segment(), false, cmx + ((local + 1) & 1) * 4 * N);
       prev = Info{walk.seq, walk.g, walk.nch, walk.j, walk.k, walk.last_of_segment()};
     }
-    if (local > 0) acc_o(local - 1, prev, false, true);
+    if (TM) ptx::bar_sync_named(1, 128);  // the last chunk's rescale factors
+    if (local > 0) acc_o(local - 1, prev, false, true, cmx + ((local + 1) & 1) * 4 * N);
   }
 
   // ---------------- teardown ----------------
@@ -805,21 +917,21 @@ __global__ void __launch_bounds__(Cfg<G>::NTHREADS, 1)
 
 // ---------------- host side ----------------
 
-template <int G>
+template <int G, bool TM>
 cudaError_t launch_g(const Params& prm, const CUtensorMap& mk, const CUtensorMap& mv,
                      const CUtensorMap& mq, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_hp_kernel<G>,
+    cudaError_t e = cudaFuncSetAttribute(decode_hp_kernel<G, TM>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<G>::SMEM_BYTES);
+                                         Cfg<G, TM>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(prm.num_ctas);
-  cfg.blockDim = dim3(Cfg<G>::NTHREADS);
-  cfg.dynamicSmemBytes = Cfg<G>::SMEM_BYTES;
+  cfg.blockDim = dim3(Cfg<G, TM>::NTHREADS);
+  cfg.dynamicSmemBytes = Cfg<G, TM>::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   // programmatic dependent launch: the prologue may overlap the previous
@@ -828,7 +940,7 @@ cudaError_t launch_g(const Params& prm, const CUtensorMap& mk, const CUtensorMap
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_hp_kernel<G>, mk, mv, mq, prm);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_hp_kernel<G, TM>, mk, mv, mq, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -848,12 +960,13 @@ size_t hp_workspace_bytes(int64_t num_seqs, int64_t num_heads, int num_ctas) {
 
 bool hp_supported(int head_dim, int group, bool fp8, int num_seqs, int num_kv_heads,
                   int block_size, int tokens_per_seq) {
-  // a tile holds HB KV heads x TT tokens of one block: H_kv must be a
-  // multiple of HB and a chunk must not cross a block (TT <= block_size)
+  // a tile holds HB KV heads x TT tokens: H_kv must be a multiple of HB.
+  // Blocks of at least TT tokens give head-major tiles (a chunk inside one
+  // block), smaller blocks token-major tiles (a chunk of whole blocks).
   if (fp8 || head_dim != hp::D || tokens_per_seq != 1) return false;
   if (group != 1 && group != 2 && group != 4) return false;
   const int hb = hp::heads_per_tile(group);
-  return num_kv_heads % hb == 0 && block_size >= 128 / hb && num_seqs <= hp::kMaxSeqs &&
+  return num_kv_heads % hb == 0 && block_size >= 1 && num_seqs <= hp::kMaxSeqs &&
          tc::encode_fn() != nullptr;
 }
 
@@ -865,8 +978,9 @@ cudaError_t launch_decode_hp(const TcLaunch& a, cudaStream_t stream) {
   const int hb = heads_per_tile(group);
   const int tt = 128 / hb;
   const int ncol = hb * group;
+  const bool tm = a.block_size < tt;  // token-major tiles
   CUtensorMap mk, mv, mq;
-  {
+  if (!tm) {
     // [blocks, block_size, H_kv, d] listed as (d, token, head, block) so that
     // a box {64, TT, HB, 1} lands head-major: row = head * TT + token
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)a.block_size, (cuuint64_t)a.num_kv_heads,
@@ -880,6 +994,25 @@ cudaError_t launch_decode_hp(const TcLaunch& a, cudaStream_t stream) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
     if (enc(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.v_cache), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  } else {
+    // The same cache viewed as (d in 64s, head mod 8, half of d, head / 8,
+    // slot = block * block_size + token); a box {64, 8, 2, HB / 8, block_size}
+    // is one block's rows of HB heads and lands token-major: for each token,
+    // for each 8 heads, an 8-row (1024-byte) group per half of d.
+    cuuint64_t dims[5] = {64, 8, 2, (cuuint64_t)a.num_kv_heads / 8,
+                          (cuuint64_t)a.num_blocks * a.block_size};
+    cuuint64_t strides[4] = {(cuuint64_t)D * 2, 128, 8 * (cuuint64_t)D * 2,
+                             (cuuint64_t)a.num_kv_heads * D * 2};
+    cuuint32_t box[5] = {64, 8, 2, (cuuint32_t)hb / 8, (cuuint32_t)a.block_size};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    if (enc(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(a.k_cache), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    if (enc(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(a.v_cache), dims, strides,
             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -922,10 +1055,13 @@ cudaError_t launch_decode_hp(const TcLaunch& a, cudaStream_t stream) {
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   prm.early_meta = a.early_meta ? 1 : 0;
   prm.epoch = tc::next_call_epoch();
-  switch (group) {
-    case 1: return launch_g<1>(prm, mk, mv, mq, stream);
-    case 2: return launch_g<2>(prm, mk, mv, mq, stream);
-    case 4: return launch_g<4>(prm, mk, mv, mq, stream);
+  switch (group * 2 + (tm ? 1 : 0)) {
+    case 2: return launch_g<1, false>(prm, mk, mv, mq, stream);
+    case 3: return launch_g<1, true>(prm, mk, mv, mq, stream);
+    case 4: return launch_g<2, false>(prm, mk, mv, mq, stream);
+    case 5: return launch_g<2, true>(prm, mk, mv, mq, stream);
+    case 8: return launch_g<4, false>(prm, mk, mv, mq, stream);
+    case 9: return launch_g<4, true>(prm, mk, mv, mq, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -71,7 +71,8 @@ size_t tc_workspace_bytes(int64_t num_seqs, int64_t num_heads, int64_t max_ctx, 
 cudaError_t launch_decode_tc(const TcLaunch& a, cudaStream_t stream);
 // The head-packed tensor-core kernel (decode_hp.cu): a bf16 cache, one token
 // per sequence, GQA group 1, 2 or 4, H_kv a multiple of its heads per tile
-// (16 for group 1, else 8) and blocks of at least 128 / that many tokens.
+// (16 for group 1, else 8); any block size (head-major tiles for blocks of
+// at least 128 / that many tokens, token-major below).
 // Takes the same TcLaunch (fp8, tokens_per_seq and non_causal unused).
 // Causal varlen attention for prefill chunks on the tensor cores
 // (prefill_tc.cu): bf16 cache, head_dim 128, GQA group 1, 2, 4 or 8, at most

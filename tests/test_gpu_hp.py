@@ -7,7 +7,9 @@ word 0: an expired bounded wait or an out-of-range block id) must stay zero.
 The cases cover several tiles and ragged tails per unit, units split over
 many CTAs (long contexts: merges of dozens of pieces), both tile shapes
 (8 heads x 16 tokens for GQA groups 2 and 4, 16 heads x 8 tokens for MHA),
-block sizes that hold one or several chunks, and empty sequences."""
+block sizes that hold one or several chunks, blocks smaller than a chunk
+(token-major tiles: a chunk of whole blocks, one copy per block, blocks past
+the context end not copied), and empty sequences."""
 import numpy as np
 import pytest
 import torch
@@ -137,11 +139,63 @@ def test_hp_workspace_shared_across_shapes_and_repeated_calls():
 
 
 @requires_gpu
-@pytest.mark.parametrize("hq,hkv,bs,kv", [(64, 8, 16, "bf16"), (32, 8, 8, "bf16"),
-                                          (8, 8, 16, "bf16"), (32, 8, 16, "fp8")])
+@pytest.mark.parametrize("block_size", [1, 2, 4, 8])
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (16, 8), (32, 32), (64, 16)])
+def test_hp_blocks_smaller_than_a_chunk(block_size, hq, hkv):
+    # token-major tiles (8 heads x 16 tokens for groups 2 and 4, 16 x 8 for
+    # MHA, so MHA at block size 8 is head-major); lengths around block,
+    # chunk and CTA boundaries
+    lens = [1, 2, 3, 5, 7, 8, 9, 15, 16, 17, 31, 33, 127, 129, 700, 2000, 4]
+    w = synth.make(f"hp-small-blocks-{hq}-{hkv}-{block_size}", lens, hq, hkv, 128, block_size,
+                   seed=171 + block_size)
+    _check(w)
+
+
+@requires_gpu
+def test_hp_block1_llama8b_and_automatic_choice():
+    # the batch-64 layer at block size 1 (121,416 single-token blocks): the
+    # automatic choice is the head-packed kernel, bit-identical to forcing it
+    w = synth.sweep(1, "bf16")
+    _, forced, _ = _check(w)
+    auto = harness.product_step(w, kernel=0)
+    assert auto["err"] == 0
+    assert np.array_equal(auto["out"], forced["out"])
+
+
+@requires_gpu
+def test_hp_block1_long_contexts():
+    # units split over many CTAs with one-token blocks
+    lens = [70000, 5000, 1, 23000, 0, 999]
+    w = synth.make("hp-b1-long", lens, 32, 8, 128, 1, seed=181, heavy_frac=0.01, heavy_mult=3.0)
+    _check(w)
+
+
+@requires_gpu
+@pytest.mark.parametrize("block_size", [1, 4])
+def test_hp_small_blocks_permutation_invariant(block_size):
+    lens = synth.llama8b_lengths(8)
+    nb = sum(-(-n // block_size) for n in lens) + 500
+    a = synth.make("hp-sb-perm-a", lens, 32, 8, 128, block_size, seed=183, num_blocks=nb)
+    b = synth.make("hp-sb-perm-b", lens, 32, 8, 128, block_size, seed=183, num_blocks=nb)
+    rng = np.random.default_rng(185)
+    perm = rng.permutation(nb).astype(np.int32)
+    mask = np.zeros_like(a.block_tables, dtype=bool)
+    for i, n in enumerate(lens):
+        mask[i, :-(-n // block_size)] = True
+    b.block_tables = np.where(mask, perm[a.block_tables], 0).astype(np.int32)
+    oa = harness.product_step(a, kernel=HP)
+    ob = harness.product_step(b, kernel=HP)
+    assert oa["err"] == 0 and ob["err"] == 0
+    assert np.array_equal(oa["out"], ob["out"])
+    harness.assert_close(oa["out"], harness.oracle_step(a)["out"], False)
+
+
+@requires_gpu
+@pytest.mark.parametrize("hq,hkv,bs,kv", [(64, 8, 16, "bf16"), (8, 8, 16, "bf16"),
+                                          (32, 8, 16, "fp8"), (32, 8, 1, "fp8")])
 def test_hp_unsupported_shapes_are_refused(hq, hkv, bs, kv):
-    # group 8, blocks shorter than a chunk, H_kv not a multiple of the tile's
-    # heads, e4m3 cache: kernel 3 refuses instead of launching
+    # group 8, H_kv not a multiple of the tile's heads, e4m3 cache: kernel 3
+    # refuses instead of launching
     w = synth.make("hp-refuse", [20, 40], hq, hkv, 128, bs, kv_dtype=kv, seed=157)
     from paged_kv_cache_108_gb300._lib import PaError
     with pytest.raises(PaError, match="head-packed"):
