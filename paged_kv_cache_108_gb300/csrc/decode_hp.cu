@@ -548,13 +548,16 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
       if (c0 == c1) continue;  // whole unit: the softmax warps wrote the output
       const bool good = wait_bar(sm, sm.bar(B_EPI + (e++ & 1)), 0, p.err, 14);
       if (!good) continue;
-      __threadfence();  // the partial written by this CTA is visible before the count
       const int u = walk.seq * HG + walk.g;
       int lst = 0;
-      if (lane == 0) lst = (arrive(&p.counters[u], p.epoch) == c1 - c0 + 1);
+      if (lane == 0) {
+        ptx::fence_acq_rel_gpu();  // the partial the softmax warps wrote precedes the count
+        lst = (arrive(&p.counters[u], p.epoch) == c1 - c0 + 1);
+        if (lst) ptx::fence_acq_rel_gpu();  // every other piece's partial is visible
+      }
       lst = __shfl_sync(0xffffffffu, lst, 0);
+      __syncwarp();
       if (!lst) continue;
-      __threadfence();  // see every other piece's partial
       const int64_t row0 = (int64_t)walk.seq * H + (int64_t)walk.g * N;
 #pragma unroll 1
       for (int cb = 0; cb < N; cb += 8) {
@@ -701,21 +704,21 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
       // CTA merges without counting; else it counts like the others and
       // merges only if it was last.  Either way the merge reads all pieces
       // from the slots in CTA order with the merge warp's arithmetic, so the
-      // result does not depend on which CTA merges.
+      // result does not depend on which CTA merges.  One thread fences for
+      // the CTA, after a barrier that orders the other threads' stores.
+      ptx::bar_sync_named(2, 128);  // every thread's partial stores precede the fence
       if (t == 0) {
         const unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(&p.counters[u]);
-        *flag = ((v >> 16) == p.epoch && (int)(v & 0xFFFFull) == nseg - 1) ? 1 : 0;
+        int f = ((v >> 16) == p.epoch && (int)(v & 0xFFFFull) == nseg - 1) ? 1 : 0;
+        if (!f) {
+          ptx::fence_acq_rel_gpu();  // this CTA's partial precedes its count
+          f = (arrive(&p.counters[u], p.epoch) == nseg) ? 1 : 0;
+        }
+        if (f) ptx::fence_acq_rel_gpu();  // every other piece's partial is visible
+        *flag = f;
       }
-      __threadfence();
-      ptx::bar_sync_named(2, 128);  // own partial complete; flag visible
-      const bool fast = *flag != 0;
       ptx::bar_sync_named(2, 128);
-      if (!fast) {
-        if (t == 0) *flag = (arrive(&p.counters[u], p.epoch) == nseg) ? 1 : 0;
-        ptx::bar_sync_named(2, 128);
-        if (*flag == 0) return;
-      }
-      __threadfence();  // see every other piece's partial
+      if (*flag == 0) return;
 #pragma unroll
       for (int c = 0; c < N; ++c) {
         M[c] = -INFINITY;

@@ -613,14 +613,17 @@ __global__ void __launch_bounds__(Cfg<FP8, GATHER>::NTHREADS, 1)
       if (c0 == c1) continue;  // whole unit: the softmax warps wrote the output
       const bool good = wait_bar(sm, sm.bar(B_EPI + (e++ & 1)), 0, p.err, 14);
       if (!good) continue;
-      __threadfence();  // the partial written by this CTA is visible before the count
       const int u = walk.seq * Hkv + walk.g;
       const int nseg = c1 - c0 + 1;
       int last = 0;
-      if (lane == 0) last = (arrive(&p.counters[u], p.epoch) == nseg);
+      if (lane == 0) {
+        ptx::fence_acq_rel_gpu();  // the partial the softmax warps wrote precedes the count
+        last = (arrive(&p.counters[u], p.epoch) == nseg);
+        if (last) ptx::fence_acq_rel_gpu();  // every other piece's partial is visible
+      }
       last = __shfl_sync(0xffffffffu, last, 0);
+      __syncwarp();
       if (!last) continue;
-      __threadfence();  // see every other piece's partial
       float M[G], Ls[G], a[G][4];
 #pragma unroll
       for (int h = 0; h < G; ++h) {

@@ -53,6 +53,13 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 
 // ---- async-proxy fences -------------------------------------------------------
 
+// Release/acquire fence at GPU scope.  One thread of a CTA fences on behalf
+// of the others after a CTA barrier (the barrier orders their accesses before
+// the fence), so a partial hand-off costs one fence, not one per thread.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;\n" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
