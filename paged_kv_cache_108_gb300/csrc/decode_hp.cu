@@ -69,6 +69,7 @@ namespace hp {
 using tc::ChunkWalk;
 using tc::Smem;
 using tc::arrive;
+using tc::arrive_expect_last;
 using tc::cta_of;
 using tc::drain_bar;
 using tc::kWaitClocks;
@@ -79,6 +80,7 @@ using tc::wait_bar;
 constexpr int D = 128;
 constexpr int kMaxSeqs = 1024;
 constexpr int TAB_SLOTS = 4, TAB_AHEAD = 3;  // block-id ring: one id per chunk
+constexpr int kMaxPieces = 160;  // pieces of one split unit: at most the persistent CTAs
 
 // G query heads per KV head (1, 2 or 4).  TM: token-major tiles, for blocks
 // of fewer than TT tokens (see the tile note above the kernel).
@@ -154,35 +156,16 @@ struct Params {
   int early_meta;                // previous kernel wrote only the cache
 };
 
-// One piece (m, l, o) folded into a running merge (M, L, a).  Both merge
-// paths (merge warp, softmax warps) use exactly these roundings, so a unit's
-// output does not depend on which CTA merges it.  A piece may hold no
-// visible key for a column (m = -inf).
-__device__ __forceinline__ void merge_weights(float& M, float m, float& rs, float& w) {
-  const float mn = fmaxf(M, m);
-  const float msafe = mn == -INFINITY ? 0.f : mn;
-  rs = fast_exp2(M - msafe);  // 0 for the first piece
-  w = fast_exp2(m - msafe);
-  M = mn;
-}
-__device__ __forceinline__ float merge_fold(float a, float rs, float w, float o) {
-  return __fmaf_rn(a, rs, __fmul_rn(w, o));
-}
-__device__ __forceinline__ void merge_step(float& M, float& L, float& a, float2 ml, float o) {
-  float rs, w;
-  merge_weights(M, ml.x, rs, w);
-  L = merge_fold(L, rs, w, ml.y);
-  a = merge_fold(a, rs, w, o);
-}
-__device__ __forceinline__ void merge_step4(float& M, float& L, float4& a, float2 ml, float4 o) {
-  float rs, w;
-  merge_weights(M, ml.x, rs, w);
-  L = merge_fold(L, rs, w, ml.y);
-  a.x = merge_fold(a.x, rs, w, o.x);
-  a.y = merge_fold(a.y, rs, w, o.y);
-  a.z = merge_fold(a.z, rs, w, o.z);
-  a.w = merge_fold(a.w, rs, w, o.w);
-}
+// The merge of a split unit's pieces (m_p, l_p, o_p), p in CTA order:
+//   M = max_p m_p,  w_p = 2^(m_p - M),  L = sum_p w_p l_p,  a = sum_p w_p o_p,
+//   out = a * (1 / L),
+// each sum in CTA order with explicit roundings.  Both merge paths (merge
+// warp, softmax warps) use exactly these, so a unit's output does not depend
+// on which CTA merges it.  A piece may hold no visible key for a column
+// (m = -inf, w = 0).
+__device__ __forceinline__ float merge_ref(float M) { return M == -INFINITY ? 0.f : M; }
+__device__ __forceinline__ float merge_w(float m, float mref) { return fast_exp2(m - mref); }
+__device__ __forceinline__ float merge_fold(float a, float w, float o) { return __fmaf_rn(w, o, a); }
 
 template <int G, bool TM>
 __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
@@ -569,6 +552,12 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
           Ls[k] = 0.f;
           a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
+#pragma unroll 4
+        for (int cc = c0; cc <= c1; ++cc) {
+          const int64_t base = ((int64_t)cc * 2 + piece_slot(cc, last, Ktot, C)) * N + cb;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) M[k] = fmaxf(M[k], __ldcg(&p.ws_ml[base + k]).x);
+        }
 #pragma unroll 2
         for (int cc = c0; cc <= c1; ++cc) {
           const int64_t base = ((int64_t)cc * 2 + piece_slot(cc, last, Ktot, C)) * N + cb;
@@ -580,12 +569,20 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
             ov[k] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (base + k) * D) + lane);
           }
 #pragma unroll
-          for (int k = 0; k < 8; ++k) merge_step4(M[k], Ls[k], a[k], ml[k], ov[k]);
+          for (int k = 0; k < 8; ++k) {
+            const float w = merge_w(ml[k].x, merge_ref(M[k]));
+            Ls[k] = merge_fold(Ls[k], w, ml[k].y);
+            a[k].x = merge_fold(a[k].x, w, ov[k].x);
+            a[k].y = merge_fold(a[k].y, w, ov[k].y);
+            a[k].z = merge_fold(a[k].z, w, ov[k].z);
+            a[k].w = merge_fold(a[k].w, w, ov[k].w);
+          }
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          __nv_bfloat162 lo2 = __floats2bfloat162_rn(a[k].x / Ls[k], a[k].y / Ls[k]);
-          __nv_bfloat162 hi2 = __floats2bfloat162_rn(a[k].z / Ls[k], a[k].w / Ls[k]);
+          const float inv = __frcp_rn(Ls[k]);
+          __nv_bfloat162 lo2 = __floats2bfloat162_rn(a[k].x * inv, a[k].y * inv);
+          __nv_bfloat162 hi2 = __floats2bfloat162_rn(a[k].z * inv, a[k].w * inv);
           uint2 w2;
           w2.x = *reinterpret_cast<uint32_t*>(&lo2);
           w2.y = *reinterpret_cast<uint32_t*>(&hi2);
@@ -683,7 +680,8 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
       __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + t;
       if (c0 == c1) {
 #pragma unroll
-        for (int c = 0; c < N; ++c) o[(row0 + c) * D] = __float2bfloat16_rn(acc[c] / L[c]);
+        for (int c = 0; c < N; ++c)
+          o[(row0 + c) * D] = __float2bfloat16_rn(acc[c] * __fdividef(1.f, L[c]));
         if (p.lse && t < N) p.lse[row0 + t] = own_ml.x + __log2f(own_ml.y);
         return;
       }
@@ -700,49 +698,110 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
         ptx::mbar_arrive(sm.bar(B_EPI + (split_epi++ & 1)));
         return;
       }
-      // The CTA's final piece.  If every other piece has already arrived this
-      // CTA merges without counting; else it counts like the others and
-      // merges only if it was last.  Either way the merge reads all pieces
-      // from the slots in CTA order with the merge warp's arithmetic, so the
-      // result does not depend on which CTA merges.  One thread fences for
-      // the CTA, after a barrier that orders the other threads' stores.
+      // The CTA's final piece: it counts like the others (one fence for the
+      // CTA, after a barrier that orders the other threads' stores) and
+      // merges if it was last.  At the kernel's end each global round trip
+      // costs ~1.5 us, so the count assumes it is last (one atomic) and the
+      // merge fetches the pieces' partials with cp.async into the idle K/V
+      // rings, KB pieces per round trip.  The fold reads the pieces in CTA
+      // order with the merge warp's arithmetic, so the result does not
+      // depend on which CTA merges.
       ptx::bar_sync_named(2, 128);  // every thread's partial stores precede the fence
       if (t == 0) {
-        const unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(&p.counters[u]);
-        int f = ((v >> 16) == p.epoch && (int)(v & 0xFFFFull) == nseg - 1) ? 1 : 0;
-        if (!f) {
-          ptx::fence_acq_rel_gpu();  // this CTA's partial precedes its count
-          f = (arrive(&p.counters[u], p.epoch) == nseg) ? 1 : 0;
-        }
+        ptx::fence_acq_rel_gpu();  // this CTA's partial precedes its count
+        const int f = arrive_expect_last(&p.counters[u], p.epoch, nseg) == nseg ? 1 : 0;
         if (f) ptx::fence_acq_rel_gpu();  // every other piece's partial is visible
         *flag = f;
       }
       ptx::bar_sync_named(2, 128);
       if (*flag == 0) return;
-#pragma unroll
-      for (int c = 0; c < N; ++c) {
-        M[c] = -INFINITY;
-        L[c] = 0.f;
-        acc[c] = 0.f;
-      }
+      // Staging in the idle K/V rings: every piece's (m, l), then the
+      // weights w_p per column, (M, L) per column, the output tile, and KB
+      // pieces' o per round trip.  One round trip brings all (m, l) and the
+      // first KB pieces; threads t < N then take column t's M, weights and
+      // L, and every thread folds its element d = t of every column.
+      constexpr int PMAX = kMaxPieces;
+      constexpr int OFF_SML = 0;                              // [PMAX][N] float2
+      constexpr int OFF_SW = OFF_SML + PMAX * N * 8;          // [PMAX][N] float
+      constexpr int OFF_SC = OFF_SW + PMAX * N * 4;           // [N] float2 (M, L)
+      constexpr int OFF_SOT = OFF_SC + N * 8;                 // [N][D] bf16 output tile
+      constexpr int OFF_SPO = (OFF_SOT + N * D * 2 + 1023) / 1024 * 1024;  // [KB][N][D] float
+      constexpr int KB = (2 * NST * TILE_B - OFF_SPO) / (N * D * 4);
+      static_assert(KB >= 1, "staging room for one piece");
+      const uint32_t stg = sm.base_u32 + OFF_K;
+      const float2* sml = reinterpret_cast<const float2*>(sm.base + OFF_K + OFF_SML);
+      float* sw = reinterpret_cast<float*>(sm.base + OFF_K + OFF_SW);
+      float2* sc = reinterpret_cast<float2*>(sm.base + OFF_K + OFF_SC);
+      __nv_bfloat16* sot = reinterpret_cast<__nv_bfloat16*>(sm.base + OFF_K + OFF_SOT);
+      const float* spo = reinterpret_cast<const float*>(sm.base + OFF_K + OFF_SPO);
+      auto slot_base = [&](int q) {
+        const int cc = c0 + q;
+        return ((int64_t)cc * 2 + piece_slot(cc, last, Ktot, C)) * N;
+      };
+      // o of pieces q0 .. q0 + nb - 1: N * D floats each, 16 bytes per copy
+      auto fetch_o = [&](int q0, int nb) {
 #pragma unroll 1
-      for (int cc = c0; cc <= c1; ++cc) {
-        const int64_t base = ((int64_t)cc * 2 + piece_slot(cc, last, Ktot, C)) * N;
-        float2 ml[N];
-        float ov[N];
+        for (int q = 0; q < nb; ++q) {
+          const char* so = reinterpret_cast<const char*>(p.ws_o + slot_base(q0 + q) * D);
 #pragma unroll
-        for (int c = 0; c < N; ++c) {
-          ml[c] = __ldcg(&p.ws_ml[base + c]);
-          ov[c] = __ldcg(&p.ws_o[(base + c) * D + t]);
+          for (int i = t; i < N * D / 4; i += 128)
+            cp_async_16(stg + OFF_SPO + (q * N * D + i * 4) * 4, so + i * 16, 16);
         }
-#pragma unroll
-        for (int c = 0; c < N; ++c) merge_step(M[c], L[c], acc[c], ml[c], ov[c]);
+      };
+#pragma unroll 1
+      for (int i = t; i < nseg * (N / 2); i += 128) {
+        const int q = i / (N / 2), j = i - q * (N / 2);
+        cp_async_16(stg + OFF_SML + (q * N + 2 * j) * 8,
+                    reinterpret_cast<const char*>(p.ws_ml + slot_base(q)) + j * 16, 16);
       }
-#pragma unroll
-      for (int c = 0; c < N; ++c) {
-        o[(row0 + c) * D] = __float2bfloat16_rn(acc[c] / L[c]);
-        if (p.lse && t == c) p.lse[row0 + c] = M[c] + __log2f(L[c]);
+      fetch_o(0, min(KB, nseg));
+      cp_async_commit();
+      cp_async_wait<0>();
+      ptx::bar_sync_named(2, 128);  // every thread's copies have landed
+      if (t < N) {
+        float Mx = -INFINITY;
+#pragma unroll 1
+        for (int q = 0; q < nseg; ++q) Mx = fmaxf(Mx, sml[q * N + t].x);
+        const float mref = merge_ref(Mx);
+        float Lt = 0.f;
+#pragma unroll 1
+        for (int q = 0; q < nseg; ++q) {
+          const float2 ml = sml[q * N + t];
+          const float w = merge_w(ml.x, mref);
+          sw[q * N + t] = w;
+          Lt = merge_fold(Lt, w, ml.y);
+        }
+        sc[t] = make_float2(Mx, Lt);
       }
+      ptx::bar_sync_named(2, 128);  // weights and (M, L) visible
+#pragma unroll
+      for (int c = 0; c < N; ++c) acc[c] = 0.f;
+#pragma unroll 1
+      for (int q0 = 0; q0 < nseg; q0 += KB) {
+        const int nb = min(KB, nseg - q0);
+        if (q0 > 0) {
+          ptx::bar_sync_named(2, 128);  // the previous batch has been read
+          fetch_o(q0, nb);
+          cp_async_commit();
+          cp_async_wait<0>();
+          ptx::bar_sync_named(2, 128);
+        }
+#pragma unroll 1
+        for (int q = 0; q < nb; ++q) {
+#pragma unroll
+          for (int c = 0; c < N; ++c)
+            acc[c] = merge_fold(acc[c], sw[(q0 + q) * N + c], spo[(q * N + c) * D + t]);
+        }
+      }
+      // output: element d = t of each column into the tile, then 16-byte rows
+#pragma unroll
+      for (int c = 0; c < N; ++c) sot[c * D + t] = __float2bfloat16_rn(acc[c] * __frcp_rn(sc[c].y));
+      if (p.lse && t < N) p.lse[row0 + t] = sc[t].x + __log2f(sc[t].y);
+      ptx::bar_sync_named(2, 128);
+#pragma unroll
+      for (int i = t; i < N * D / 8; i += 128)
+        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + row0 * D + i * 8) =
+            *reinterpret_cast<const uint4*>(sot + i * 8);
       if (t == 0) p.counters[u] = p.epoch << 16;  // count 0: a replay starts afresh
     };
 
@@ -982,6 +1041,7 @@ cudaError_t launch_decode_hp(const TcLaunch& a, cudaStream_t stream) {
   const int tt = 128 / hb;
   const int ncol = hb * group;
   const bool tm = a.block_size < tt;  // token-major tiles
+  if (a.num_ctas > kMaxPieces) return cudaErrorInvalidValue;  // a unit's pieces must fit the merge staging
   CUtensorMap mk, mv, mq;
   if (!tm) {
     // [blocks, block_size, H_kv, d] listed as (d, token, head, block) so that

@@ -61,6 +61,22 @@ __device__ __forceinline__ int arrive(unsigned long long* cnt, unsigned long lon
   }
 }
 
+// arrive() for a piece that expects to be its unit's last: the first
+// exchange assumes the other nseg - 1 pieces have counted, so the usual
+// last arrival costs one atomic round trip instead of a read and an atomic.
+__device__ __forceinline__ int arrive_expect_last(unsigned long long* cnt, unsigned long long epoch,
+                                                  int nseg) {
+  const unsigned long long guess = (epoch << 16) | (unsigned long long)(nseg - 1);
+  unsigned long long v = atomicCAS(cnt, guess, guess + 1);
+  if (v == guess) return nseg;
+  while (true) {
+    const unsigned long long nv = ((v >> 16) == epoch) ? v + 1 : ((epoch << 16) | 1ull);
+    const unsigned long long old = atomicCAS(cnt, v, nv);
+    if (old == v) return (int)(nv & 0xFFFFull);
+    v = old;
+  }
+}
+
 // First chunk index owned by CTA c when K chunks are split over C CTAs.
 __device__ __forceinline__ long long range_lo(long long c, long long K, long long C) {
   return c * K / C;
