@@ -572,10 +572,12 @@ def run_ours(args, rank, world, local_rank):
         roofline = {"bound": "hbm", "kernel": "pa_decode alone (tcgen05 paged decode; split "
                     "units merged in-kernel)", "achieved": round(achieved, 2), "peak": peak,
                     "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                    # the ncu record covers the headline decode at block 16 only
+                    # the ncu record covers the headline decode (per-head kernel,
+                    # block 16) only
                     "traffic": (recorded_traffic(dbytes, args.kv_dtype)
                                 if args.workload == "llama8b" and args.block_size == 16
-                                and step.new_tokens == 1 and not step.group else None),
+                                and args.kernel in (0, 2) and step.new_tokens == 1
+                                and not step.group else None),
                     "algorithmic_bytes": dbytes}
     value = job_throughput(world, sbytes, mean_step * 1e-3) / 1e9
     w = step.w
