@@ -126,17 +126,19 @@ size_t pa_decode_workspace_size_ex(int32_t num_seqs, int32_t num_heads,
  *            columns are those heads' query heads, and each column keeps only
  *            its own KV head's rows.  Blocks smaller than 128 / heads per
  *            tile tokens are copied whole (every token's rows of those heads,
- *            2 or 4 KiB per token).  Needs a bf16 cache, head_dim 128, GQA
- *            group 1, 2 or 4, num_kv_heads a multiple of those heads per
- *            tile, at most 1024 sequences, one token per sequence, else
- *            PA_ERR_UNSUPPORTED.  Error word as kernel 2.
+ *            1 to 4 KiB per token).  An e4m3 cache is read as it is, with q
+ *            and the softmax weights split into e4m3 parts as in kernel 2.
+ *            Needs head_dim 128, GQA group 1, 2 or 4, num_kv_heads a
+ *            multiple of those heads per tile, at most 1024 sequences, one
+ *            token per sequence, else PA_ERR_UNSUPPORTED.  Error word as
+ *            kernel 2.
  *  kernel 0: kernel 3 where it applies and either the blocks hold fewer
- *            than 8 tokens or the batch has many units (per unit: a sequence
- *            and its 8 or 16 KV heads; at least twice the SM count, or half
- *            of it for GQA group 1); else kernel 2 where it applies (below 8
- *            tokens per block only for several tokens per sequence: its
- *            gathered loads stream slower than the SIMT kernel); else
- *            kernel 1. */
+ *            than 8 tokens or (bf16 cache) the batch has many units (per
+ *            unit: a sequence and its 8 or 16 KV heads; at least twice the
+ *            SM count, or half of it for GQA group 1); else kernel 2 where it
+ *            applies (below 8 tokens per block only for several tokens per
+ *            sequence: its gathered loads stream slower than the SIMT
+ *            kernel); else kernel 1. */
 typedef struct {
   int32_t partition_tokens; /* split-K partition length: power of two >= 64 */
   int32_t kernel;           /* 0 auto, 1 SIMT, 2 tensor-core, 3 head-packed tensor-core */

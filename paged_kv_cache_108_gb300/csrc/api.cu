@@ -223,7 +223,7 @@ int pa_decode_auto_kernel(const pa_cache_desc& cache, int32_t num_heads, int32_t
     // or 16 heads (2 or 4 KiB per token) with one TMA box.
     if (cache.block_size < 8) return 3;
     const int64_t hp_units = (int64_t)num_seqs * (cache.num_kv_heads / (group >= 2 ? 8 : 16));
-    if (group == 1 ? 2 * hp_units >= num_sms() : hp_units >= 2 * num_sms()) return 3;
+    if (!fp8 && (group == 1 ? 2 * hp_units >= num_sms() : hp_units >= 2 * num_sms())) return 3;
   }
   // Below 8 tokens per block the tensor-core kernel gathers rows with cp.async
   // and publishes a stage only once its own copies have landed; measured on
@@ -290,9 +290,9 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
                                       cache.block_size, tokens_per_seq);
   if (kernel == 3 && !hp_ok)
     return pa_fail(PA_ERR_UNSUPPORTED,
-                   "pa_decode: head-packed kernel needs a bf16 cache, head_dim 128, GQA group "
-                   "1, 2 or 4, num_kv_heads a multiple of 16 (group 1) or 8, at most 1024 "
-                   "sequences and one token per sequence");
+                   "pa_decode: head-packed kernel needs head_dim 128, GQA group 1, 2 or 4, "
+                   "num_kv_heads a multiple of 16 (group 1) or 8, at most 1024 sequences and "
+                   "one token per sequence");
   if (hp_ok) {
     const int nsm = num_sms();
     const size_t need = pa::hp_workspace_bytes(num_seqs, num_heads, nsm);
@@ -306,6 +306,9 @@ static pa_status decode_impl(void* out, const void* q, const void* k_cache, cons
     a.q = q;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
+    a.fp8 = fp8;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.workspace = workspace;

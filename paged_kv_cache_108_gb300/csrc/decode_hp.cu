@@ -83,26 +83,38 @@ constexpr int TAB_SLOTS = 4, TAB_AHEAD = 3;  // block-id ring: one id per chunk
 constexpr int kMaxPieces = 160;  // pieces of one split unit: at most the persistent CTAs
 
 // G query heads per KV head (1, 2 or 4).  TM: token-major tiles, for blocks
-// of fewer than TT tokens (see the tile note above the kernel).
-template <int G, bool TM>
+// of fewer than TT tokens (see the tile note above the kernel).  FP8: an
+// e4m3 cache (see the e4m3 note above the kernel).
+template <int G, bool TM, bool FP8>
 struct Cfg {
   static constexpr int HB = G >= 2 ? 8 : 16;  // KV heads per tile
   static constexpr int TT = 128 / HB;         // tokens per chunk
-  static constexpr int N = HB * G;            // MMA columns: the tile's query heads
+  static constexpr int N = HB * G;            // the tile's query heads
   static constexpr int NW = N / 4;            // columns of one softmax warp's heads
-  static constexpr int NST = 3;               // K/V ring stages (192 KiB)
-  static constexpr int TILE_B = 128 * D * 2;  // one K or V tile: 128 rows of 256 bytes
-  static constexpr int HALF_B = 128 * 128;    // one 64-column half of a tile
-  // Where the 64-column half h of the 8-row group a of a tile starts:
+  static constexpr int ELT = FP8 ? 1 : 2;     // bytes per K/V element
+  // K/V ring stages: 3 x 64 KiB (bf16) or 5 x 32 KiB (e4m3)
+  static constexpr int NST = FP8 ? 5 : 3;
+  static constexpr int TILE_B = 128 * D * ELT;  // one K or V tile: 128 rows of d
+  static constexpr int HALF_B = 128 * 128;      // bf16: one 64-column half of a tile
+  // bf16: where the 64-column half h of the 8-row group a of a tile starts:
   // head-major a * 1024 + h * HALF_B; token-major a * 2048 + h * 1024.
-  static constexpr int GRP_B = TM ? 2048 : 1024;    // between 8-row groups
-  static constexpr int HSTEP_B = TM ? 1024 : HALF_B;  // between the halves
-  static constexpr int QTILE_B = N * D * 2;
+  // e4m3: a 128-byte row is all of d; group a starts at a * 1024.
+  static constexpr int GRP_B = (TM && !FP8) ? 2048 : 1024;  // between 8-row groups
+  static constexpr int HSTEP_B = TM ? 1024 : HALF_B;         // bf16: between the halves
+  // e4m3: q as three e4m3 parts (operand rows part * N + c) and P as two
+  // (rows part * N + c); the MMA N of the logits and of P V
+  static constexpr int NQP = FP8 ? 3 : 1, NPP = FP8 ? 2 : 1;
+  static constexpr int NS = N * NQP, NO = N * NPP;
+  static constexpr int QTILE_B = FP8 ? NS * 128 : N * D * 2;
+  static constexpr int NQBUF = FP8 ? 2 : 1;   // q tiles (e4m3: written by the q warp)
   static constexpr int QHALF_B = N * 128;
-  static constexpr int PTILE_B = N * 128 * 2;  // P^T: N rows of 128 bf16
+  static constexpr int PTILE_B = FP8 ? NO * 128 : N * 128 * 2;  // P^T: rows of 128 tile rows
   static constexpr int PHALF_B = N * 128;
-  // TMEM: S[2] then O[2], N columns each
-  static constexpr int TMEM_COLS = 4 * N <= 64 ? 64 : 128;
+  // TMEM: S[2] of NS columns, then O[2] of NO
+  static constexpr int TMEM_NEED = 2 * (NS + NO);
+  static constexpr int TMEM_COLS =
+      TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
+  static constexpr int O_COL = 2 * NS;
   static constexpr int NTHREADS = 256;
   // rescale-factor buffers: three when the factors are published before the
   // per-chunk barrier (head-major), two when after it (token-major)
@@ -112,18 +124,20 @@ struct Cfg {
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NST * TILE_B;
   static constexpr int OFF_Q = OFF_V + NST * TILE_B;
-  static constexpr int OFF_P = OFF_Q + QTILE_B;
+  static constexpr int OFF_P = OFF_Q + NQBUF * QTILE_B;
   static constexpr int OFF_BAR = OFF_P + 2 * PTILE_B;
   static constexpr int B_FULL_K = 0, B_FULL_V = NST, B_EMPTY = 2 * NST, B_S_FULL = 3 * NST,
                        B_S_EMPTY = B_S_FULL + 2, B_P_FULL = B_S_EMPTY + 2,
                        B_P_EMPTY = B_P_FULL + 2, B_O_FULL = B_P_EMPTY + 2,
                        B_O_EMPTY = B_O_FULL + 2, B_Q_FULL = B_O_EMPTY + 2,
-                       B_Q_EMPTY = B_Q_FULL + 1, B_EPI = B_Q_EMPTY + 1, NBARS = B_EPI + 2;
+                       B_Q_EMPTY = B_Q_FULL + NQBUF, B_EPI = B_Q_EMPTY + NQBUF,
+                       NBARS = B_EPI + 2;
   static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
   static constexpr int OFF_SQ = OFF_ABORT + 4;      // [3] ints: sequences of the range's ends, first
   static constexpr int OFF_FLAG = OFF_SQ + 12;      // softmax warps' broadcast word
-  static constexpr int OFF_ALPHA = OFF_FLAG + 4;    // [NALPHA][N] floats: per-chunk rescale factors
+  static constexpr int OFF_QEXP = OFF_FLAG + 4;     // e4m3: [2] floats, 2^-e of each q tile
+  static constexpr int OFF_ALPHA = (OFF_QEXP + 8 + 15) / 16 * 16;  // [NALPHA][N] floats: rescale factors
   static constexpr int OFF_ML = OFF_ALPHA + NALPHA * N * 4;  // [N] float2: a piece's (m, l)
   // token-major: [2][4 warps][N] floats, each warp's chunk maxima (and, in
   // an epilogue, its share of the column sums)
@@ -133,8 +147,11 @@ struct Cfg {
   static constexpr int OFF_TAB = OFF_NLEN + kMaxSeqs * 4;       // block-id ring
   static constexpr int SMEM_BYTES = OFF_TAB + TAB_SLOTS * TAB_IDS * 4 + 1024;  // + alignment slack
   static_assert(N % 16 == 0 && N <= 32, "MMA N");
+  static_assert(NS <= 256 && NS % 16 == 0 && NO % 16 == 0, "MMA N");
+  static_assert(TMEM_NEED <= 512, "tensor memory columns");
   static_assert(TT <= 32, "a KV head's rows stay in one warp");
-  static_assert(OFF_BAR % 1024 == 0 && PHALF_B % 1024 == 0 && QHALF_B % 1024 == 0,
+  static_assert(OFF_BAR % 1024 == 0 && PHALF_B % 1024 == 0 && QHALF_B % 1024 == 0 &&
+                    QTILE_B % 1024 == 0 && PTILE_B % 1024 == 0 && TILE_B % 1024 == 0,
                 "swizzled tiles stay 1024-byte aligned");
   static_assert(OFF_ALPHA % 16 == 0 && OFF_ML % 8 == 0 && OFF_CMX % 16 == 0, "alignment");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
@@ -149,6 +166,9 @@ struct Params {
   float2* ws_ml;                 // [num_ctas][2][N] (m, l) of a piece
   float* ws_o;                   // [num_ctas][2][N][D] unnormalised o of a piece
   float* lse;                    // optional [S * H]: log2-sum-exp of each output row
+  const void* q;                 // e4m3: [S * H, D] bf16 q, read by the q warp
+  const float* k_scale;          // e4m3: device scalars
+  const float* v_scale;
   int num_seqs, num_heads, num_groups, max_blocks, num_blocks, block_size, log2_bs;
   int num_ctas;
   float scale_log2;
@@ -167,15 +187,16 @@ __device__ __forceinline__ float merge_ref(float M) { return M == -INFINITY ? 0.
 __device__ __forceinline__ float merge_w(float m, float mref) { return fast_exp2(m - mref); }
 __device__ __forceinline__ float merge_fold(float a, float w, float o) { return __fmaf_rn(w, o, a); }
 
-template <int G, bool TM>
-__global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
+template <int G, bool TM, bool FP8>
+__global__ void __launch_bounds__(Cfg<G, TM, FP8>::NTHREADS, 1)
     decode_hp_kernel(const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_q, const Params p) {
-  using Cf = Cfg<G, TM>;
+  using Cf = Cfg<G, TM, FP8>;
   constexpr int HB = Cf::HB, TT = Cf::TT, N = Cf::N, NW = Cf::NW, NST = Cf::NST;
   constexpr int NALPHA = Cf::NALPHA, TAB_IDS = Cf::TAB_IDS, GRP_B = Cf::GRP_B,
-                HSTEP_B = Cf::HSTEP_B;
+                HSTEP_B = Cf::HSTEP_B, NS = Cf::NS, NO = Cf::NO, O_COL = Cf::O_COL,
+                NQBUF = Cf::NQBUF, OFF_QEXP = Cf::OFF_QEXP;
   constexpr int TILE_B = Cf::TILE_B, HALF_B = Cf::HALF_B, QTILE_B = Cf::QTILE_B,
                 QHALF_B = Cf::QHALF_B, PTILE_B = Cf::PTILE_B, PHALF_B = Cf::PHALF_B,
                 TMEM_COLS = Cf::TMEM_COLS, NTHREADS = Cf::NTHREADS;
@@ -223,6 +244,10 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
       if ((i >= B_S_EMPTY && i < B_S_EMPTY + 2) || (i >= B_P_FULL && i < B_P_FULL + 2) ||
           (i >= B_O_EMPTY && i < B_O_EMPTY + 2) || (i >= B_EPI && i < B_EPI + 2))
         cnt = 128;
+      // e4m3: the q warp's lanes fill a q tile; the segment's last logits
+      // MMA and the softmax threads (which read its scale) release it
+      if (FP8 && i >= B_Q_FULL && i < B_Q_FULL + NQBUF) cnt = 32;
+      if (FP8 && i >= B_Q_EMPTY && i < B_Q_EMPTY + NQBUF) cnt = 1 + 128;
       ptx::mbar_init(sm.bar(i), cnt);
     }
     *sm.abort_flag() = 0;
@@ -232,7 +257,7 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
     ptx::prefetch_tmap(&tm_k);
     ptx::prefetch_tmap(&tm_v);
   }
-  if (warp == 5 && lane == 0) ptx::prefetch_tmap(&tm_q);
+  if (!FP8 && warp == 5 && lane == 0) ptx::prefetch_tmap(&tm_q);
   if (warp < 4) {
     // zero both P tiles once: a thread only ever writes its own KV head's
     // columns of its own row, so the off-diagonal blocks stay zero
@@ -350,7 +375,8 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
         phys = 0;
       }
       if constexpr (TM) {
-        const uint32_t box_b = (uint32_t)bs * HB * 256;  // one block's rows of the HB heads
+        // one block's rows of the HB heads
+        const uint32_t box_b = (uint32_t)bs * HB * D * Cf::ELT;
         if (lane == 0) {
           ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_K + s), (uint32_t)nb * box_b);
           ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_V + s), (uint32_t)nb * box_b);
@@ -359,11 +385,32 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
         if (lane < nb) {
           const uint32_t off = s * TILE_B + lane * box_b;
           const int slot0 = phys << p.log2_bs;  // < num_blocks * block_size <= 2^31 - 1
-          ptx::tma_load_5d(sm.base_u32 + OFF_K + off, &tm_k, sm.bar(B_FULL_K + s), 0, 0, 0,
-                           walk.g * (HB / 8), slot0);
-          ptx::tma_load_5d(sm.base_u32 + OFF_V + off, &tm_v, sm.bar(B_FULL_V + s), 0, 0, 0,
-                           walk.g * (HB / 8), slot0);
+          if constexpr (FP8) {
+            // box {128 bytes of d, 8 heads, HB / 8, block_size tokens}
+            ptx::tma_load_4d(sm.base_u32 + OFF_K + off, &tm_k, sm.bar(B_FULL_K + s), 0, 0,
+                             walk.g * (HB / 8), slot0);
+            ptx::tma_load_4d(sm.base_u32 + OFF_V + off, &tm_v, sm.bar(B_FULL_V + s), 0, 0,
+                             walk.g * (HB / 8), slot0);
+          } else {
+            ptx::tma_load_5d(sm.base_u32 + OFF_K + off, &tm_k, sm.bar(B_FULL_K + s), 0, 0, 0,
+                             walk.g * (HB / 8), slot0);
+            ptx::tma_load_5d(sm.base_u32 + OFF_V + off, &tm_v, sm.bar(B_FULL_V + s), 0, 0, 0,
+                             walk.g * (HB / 8), slot0);
+          }
         }
+      } else if constexpr (FP8) {
+        // lane 0: K, lane 1: V; box {128 bytes of d, TT tokens, HB heads}
+        const int tok = (walk.j * TT) & (bs - 1);
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_K + s), (uint32_t)TILE_B);
+          ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_V + s), (uint32_t)TILE_B);
+        }
+        __syncwarp();
+        if (lane < 2)
+          ptx::tma_load_4d(sm.base_u32 + (lane == 0 ? OFF_K : OFF_V) + s * TILE_B,
+                           lane == 0 ? (const void*)&tm_k : (const void*)&tm_v,
+                           sm.bar((lane == 0 ? B_FULL_K : B_FULL_V) + s), 0, tok, walk.g * HB,
+                           phys);
       } else {
         const int tok = (walk.j * TT) & (bs - 1);
         if (lane == 0) {
@@ -404,19 +451,29 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
     // ready.  The q tile has one buffer: when a segment (a unit's piece)
     // starts, its load is issued once the previous segment's last logits
     // MMA has completed, and that segment's first logits MMA waits for it.
+    // e4m3: the q warp fills two q tiles in turn; the MMA thread waits for
+    // the segment's tile and releases it after the segment's last logits MMA.
     if (lane == 0) {
-      constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(128, N, false);
-      constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, N, true);
-      const uint32_t qbase = sm.base_u32 + OFF_Q;
+      constexpr uint32_t IDESC_QK =
+          FP8 ? ptx::idesc_e4m3_f32(128, NS, false) : ptx::idesc_bf16_f32(128, N, false);
+      constexpr uint32_t IDESC_PV =
+          FP8 ? ptx::idesc_e4m3_f32(128, NO, true) : ptx::idesc_bf16_f32(128, N, true);
       walk.init(lo, hi, seq_lo, seq_hi);
-      int nq = 0, npv = 0, seg = 0;
+      int nq = 0, npv = 0, seg = 0, cur_q = 0;
       bool q_loading = false, q_ready = false;
       long long t_idle = clock64();
       while (true) {
         bool progress = false;
         if (!walk.done()) {
           const bool first = walk.first_of_segment();
-          if (first && !q_ready) {
+          if (FP8 && first && !q_ready) {
+            if (ptx::mbar_test_wait(sm.bar(B_Q_FULL + (seg & 1)), (seg >> 1) & 1)) {
+              q_ready = true;
+              cur_q = seg & 1;
+              progress = true;
+            }
+          } else if (!FP8 && first && !q_ready) {
+            const uint32_t qbase = sm.base_u32 + OFF_Q;
             if (!q_loading) {
               if (seg == 0 || ptx::mbar_test_wait(sm.bar(B_Q_EMPTY), (seg - 1) & 1)) {
                 // the unit's query heads g*N .. g*N+N-1: rows of q as [S*H, d]
@@ -439,17 +496,28 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
               ptx::mbar_test_wait(sm.bar(B_S_EMPTY + b), ((nq >> 1) & 1) ^ 1)) {
             ptx::tc_fence_after();
             const uint32_t kbase = sm.base_u32 + OFF_K + s * TILE_B;
+            const uint32_t qbase = sm.base_u32 + OFF_Q + cur_q * QTILE_B;
+            if constexpr (FP8) {
+              // K and q-part rows are 128 bytes (all of d), 32 per MMA
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t da =
-                  ptx::smem_desc_sw128(kbase + (kk >> 2) * HSTEP_B + (kk & 3) * 32, 16, GRP_B);
-              const uint64_t db =
-                  ptx::smem_desc_sw128(qbase + (kk >> 2) * QHALF_B + (kk & 3) * 32, 16, 1024);
-              ptx::tc_mma_f16(tmem + N * b, da, db, IDESC_QK, kk > 0);
+              for (int kk = 0; kk < D / 32; ++kk) {
+                const uint64_t da = ptx::smem_desc_sw128(kbase + kk * 32, 16, 1024);
+                const uint64_t db = ptx::smem_desc_sw128(qbase + kk * 32, 16, 1024);
+                ptx::tc_mma_f8(tmem + NS * b, da, db, IDESC_QK, kk > 0);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t da =
+                    ptx::smem_desc_sw128(kbase + (kk >> 2) * HSTEP_B + (kk & 3) * 32, 16, GRP_B);
+                const uint64_t db =
+                    ptx::smem_desc_sw128(qbase + (kk >> 2) * QHALF_B + (kk & 3) * 32, 16, 1024);
+                ptx::tc_mma_f16(tmem + NS * b, da, db, IDESC_QK, kk > 0);
+              }
             }
             ptx::tc_commit(sm.bar(B_S_FULL + b));
             if (walk.last_of_segment()) {
-              ptx::tc_commit(sm.bar(B_Q_EMPTY));
+              ptx::tc_commit(sm.bar(B_Q_EMPTY + cur_q));
               ++seg;
               q_ready = false;
             }
@@ -468,15 +536,27 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
             ptx::tc_fence_after();
             const uint32_t vbase = sm.base_u32 + OFF_V + s * TILE_B;
             const uint32_t pbase = sm.base_u32 + OFF_P + b * PTILE_B;
-            // A = V^T read MN-major from the TMA layout (16 rows, two 8-row
-            // groups, per MMA; the halves of d HSTEP_B apart);
-            // B = P^T, K-major, 64 rows per 128-byte swizzled half
+            if constexpr (FP8) {
+              // A = V^T MN-major: a 128-byte row is all of d for one tile
+              // row, so one swizzle atom spans M; 32 rows (4 groups) per MMA.
+              // B = P^T, K-major: rows of 128 tile rows, 32 per MMA.
 #pragma unroll
-            for (int kk = 0; kk < 128 / 16; ++kk) {
-              const uint64_t da = ptx::smem_desc_sw128(vbase + kk * 2 * GRP_B, HSTEP_B, GRP_B);
-              const uint64_t db =
-                  ptx::smem_desc_sw128(pbase + (kk >> 2) * PHALF_B + (kk & 3) * 32, 16, 1024);
-              ptx::tc_mma_f16(tmem + 2 * N + N * b, da, db, IDESC_PV, kk > 0);
+              for (int kk = 0; kk < 128 / 32; ++kk) {
+                const uint64_t da = ptx::smem_desc_sw128(vbase + kk * 4 * GRP_B, TILE_B, GRP_B);
+                const uint64_t db = ptx::smem_desc_sw128(pbase + kk * 32, 16, 1024);
+                ptx::tc_mma_f8(tmem + O_COL + NO * b, da, db, IDESC_PV, kk > 0);
+              }
+            } else {
+              // A = V^T read MN-major from the TMA layout (16 rows, two 8-row
+              // groups, per MMA; the halves of d HSTEP_B apart);
+              // B = P^T, K-major, 64 rows per 128-byte swizzled half
+#pragma unroll
+              for (int kk = 0; kk < 128 / 16; ++kk) {
+                const uint64_t da = ptx::smem_desc_sw128(vbase + kk * 2 * GRP_B, HSTEP_B, GRP_B);
+                const uint64_t db =
+                    ptx::smem_desc_sw128(pbase + (kk >> 2) * PHALF_B + (kk & 3) * 32, 16, 1024);
+                ptx::tc_mma_f16(tmem + O_COL + NO * b, da, db, IDESC_PV, kk > 0);
+              }
             }
             ptx::tc_commit(sm.bar(B_O_FULL + b));
             ptx::tc_commit(sm.bar(B_P_EMPTY + b));
@@ -500,7 +580,10 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
       }
       // drain: every copy and commit this thread issued must land before exit
       if (q_loading) drain_bar(sm.bar(B_Q_FULL), seg & 1);
-      if (seg > 0) drain_bar(sm.bar(B_Q_EMPTY), (seg - 1) & 1);
+      if (seg > 0) {
+        if (FP8) drain_bar(sm.bar(B_Q_EMPTY + ((seg - 1) & 1)), ((seg - 1) >> 1) & 1);
+        else drain_bar(sm.bar(B_Q_EMPTY), (seg - 1) & 1);
+      }
       if (nq > 0) drain_bar(sm.bar(B_S_FULL + ((nq - 1) & 1)), ((nq - 1) >> 1) & 1);
       if (npv > 0) {
         const int L = npv - 1;
@@ -578,9 +661,12 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
             a[k].w = merge_fold(a[k].w, w, ov[k].w);
           }
         }
+        // e4m3: o and l carry the factor 256 of P's encoding (it cancels);
+        // v_scale multiplies the output and the log-sum-exp drops the 2^8
+        const float vsc = FP8 ? __ldg(p.v_scale) : 1.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const float inv = __frcp_rn(Ls[k]);
+          const float inv = FP8 ? __frcp_rn(Ls[k]) * vsc : __frcp_rn(Ls[k]);
           __nv_bfloat162 lo2 = __floats2bfloat162_rn(a[k].x * inv, a[k].y * inv);
           __nv_bfloat162 hi2 = __floats2bfloat162_rn(a[k].z * inv, a[k].w * inv);
           uint2 w2;
@@ -588,10 +674,78 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
           w2.y = *reinterpret_cast<uint32_t*>(&hi2);
           *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
                                     (row0 + cb + k) * D + 4 * lane) = w2;
-          if (p.lse && lane == k) p.lse[row0 + cb + k] = M[k] + __log2f(Ls[k]);
+          if (p.lse && lane == k) p.lse[row0 + cb + k] = M[k] + __log2f(Ls[k]) - (FP8 ? 8.f : 0.f);
         }
       }
       if (lane == 0) p.counters[u] = p.epoch << 16;  // count 0: a replay starts afresh
+    }
+  } else if (warp == 7) {
+    // ================= q warp (e4m3 cache only) =================
+    // Per segment, the unit's N bf16 query rows become three e4m3 parts:
+    // q * 2^e ~= hi + mid + lo, with 2^e the power of two that puts max |q|
+    // in [128, 256); each part is the round-to-nearest of what the previous
+    // ones leave (exact fp32 residuals), so the sum holds q to ~2^-12
+    // relative.  Part pp of column c is operand row pp * N + c.
+    if constexpr (FP8) {
+      float* qx = reinterpret_cast<float*>(sm.base + OFF_QEXP);
+      constexpr int NPIECE = N * D / 8;  // 16-byte pieces of the unit's bf16 q rows
+      constexpr int NV = NPIECE / 32;    // per lane
+      walk.init(lo, hi, seq_lo, seq_hi);
+      int seg = 0;
+      for (; !walk.done(); walk.next()) {
+        if (!walk.first_of_segment()) continue;
+        const int qs = seg & 1;
+        if (!wait_bar(sm, sm.bar(B_Q_EMPTY + qs), ((seg >> 1) & 1) ^ 1, p.err, 2)) break;
+        ++seg;
+        // the unit's query heads g*N .. g*N+N-1 are consecutive rows of q
+        const uint4* src = reinterpret_cast<const uint4*>(p.q) +
+                           ((int64_t)walk.seq * H + (int64_t)walk.g * N) * (D / 8);
+        uint4 v[NV];
+        uint32_t amax = 0;  // bit pattern of max |q| (orders like the float)
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+          v[i] = __ldg(src + i * 32 + lane);
+          const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            amax = max(amax, max((w[c] << 16) & 0x7fffffffu, w[c] & 0x7fff0000u));
+        }
+        amax = __reduce_max_sync(0xffffffffu, amax);
+        const int eb = (int)(amax >> 23);  // biased exponent; 0 for zero / subnormal
+        int e = eb == 0 ? 0 : 134 - eb;   // max |q| * 2^e in [128, 256)
+        e = max(-126, min(126, e));
+        const float mul = __int_as_float((127 + e) << 23);
+        if (lane == 0) qx[qs] = __int_as_float((127 - e) << 23);
+        unsigned char* qt = sm.base + OFF_Q + qs * QTILE_B;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+          const int idx = i * 32 + lane;
+          const int c = idx >> 4, d0 = (idx & 15) * 8;
+          const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+          uint32_t pw[3][2] = {{0, 0}, {0, 0}, {0, 0}};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float a = bf16_lo(w[k]) * mul, b2 = bf16_hi(w[k]) * mul;
+#pragma unroll
+            for (int part = 0; part < 3; ++part) {
+              const uint16_t code = pack_e4m3x2_rn(a, b2);
+              const float2 v2 = e4m3x2_to_float2(code);
+              a -= v2.x;
+              b2 -= v2.y;
+              pw[part][k >> 1] |= (uint32_t)code << (16 * (k & 1));
+            }
+          }
+#pragma unroll
+          for (int part = 0; part < 3; ++part) {
+            // 128-byte swizzle: 16-byte piece index XOR (row & 7)
+            const int r = part * N + c;
+            const int o = (r >> 3) * 1024 + (r & 7) * 128 + ((((d0 >> 4) ^ (r & 7)) << 4) | (d0 & 8));
+            *reinterpret_cast<uint2*>(qt + o) = make_uint2(pw[part][0], pw[part][1]);
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(sm.bar(B_Q_FULL + qs));
+      }
     }
   } else if (warp < 4) {
     // ================= softmax + epilogue (warps 0-3) =================
@@ -605,6 +759,15 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
     // token-major: [2][4][N] per-warp chunk maxima, by chunk parity
     float* cmx = reinterpret_cast<float*>(sm.base + OFF_CMX);
     volatile int* flag = reinterpret_cast<volatile int*>(sm.base + OFF_FLAG);
+    // e4m3: logits are (S_c + S_{N+c} + S_{2N+c}) * 2^-e * k_scale * scale *
+    // log2(e), with 2^-e the q tile's prescale; P carries 256 p, which
+    // cancels in o / l; v_scale multiplies the output
+    const float ksc = FP8 ? __ldg(p.k_scale) : 1.f;
+    const float vsc = FP8 ? __ldg(p.v_scale) : 1.f;
+    const float lse_off = FP8 ? 8.f : 0.f;
+    const float* qexp = reinterpret_cast<const float*>(sm.base + OFF_QEXP);
+    float sscale = p.scale_log2;
+    int qseg = 0;
     // running max per column (the same in all TT lanes of a head) and this
     // row's share of the column sums; dm, dl: those of a just-finished piece
     float m[G], l[G], dm[G], dl[G];
@@ -681,8 +844,8 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
       if (c0 == c1) {
 #pragma unroll
         for (int c = 0; c < N; ++c)
-          o[(row0 + c) * D] = __float2bfloat16_rn(acc[c] * __fdividef(1.f, L[c]));
-        if (p.lse && t < N) p.lse[row0 + t] = own_ml.x + __log2f(own_ml.y);
+          o[(row0 + c) * D] = __float2bfloat16_rn(acc[c] * (__fdividef(1.f, L[c]) * vsc));
+        if (p.lse && t < N) p.lse[row0 + t] = own_ml.x + __log2f(own_ml.y) - lse_off;
         return;
       }
       const int u = in.seq * HG + in.g;
@@ -795,8 +958,12 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
       }
       // output: element d = t of each column into the tile, then 16-byte rows
 #pragma unroll
-      for (int c = 0; c < N; ++c) sot[c * D + t] = __float2bfloat16_rn(acc[c] * __frcp_rn(sc[c].y));
-      if (p.lse && t < N) p.lse[row0 + t] = sc[t].x + __log2f(sc[t].y);
+      for (int c = 0; c < N; ++c) {
+        // the merge warp's rounding: a * (1 / L), times v_scale for e4m3
+        const float inv = FP8 ? __frcp_rn(sc[c].y) * vsc : __frcp_rn(sc[c].y);
+        sot[c * D + t] = __float2bfloat16_rn(acc[c] * inv);
+      }
+      if (p.lse && t < N) p.lse[row0 + t] = sc[t].x + __log2f(sc[t].y) - lse_off;
       ptx::bar_sync_named(2, 128);
 #pragma unroll
       for (int i = t; i < N * D / 8; i += 128)
@@ -813,9 +980,21 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
       const bool good = wait_bar(sm, sm.bar(B_O_FULL + b), bph, p.err, 10);
       ptx::tc_fence_after();
       if constexpr (N == 32) {
-        ptx::tmem_ld_x32(tmem + lane_base + 2 * N + N * b, ov);
+        ptx::tmem_ld_x32(tmem + lane_base + O_COL + NO * b, ov);
       } else {
-        ptx::tmem_ld_x16(tmem + lane_base + 2 * N + N * b, ov);
+        ptx::tmem_ld_x16(tmem + lane_base + O_COL + NO * b, ov);
+      }
+      if constexpr (FP8) {
+        // columns N + c hold the contribution of P's low parts
+        float ol[N];
+        if constexpr (N == 32) {
+          ptx::tmem_ld_x32(tmem + lane_base + O_COL + NO * b + N, ol);
+        } else {
+          ptx::tmem_ld_x16(tmem + lane_base + O_COL + NO * b + N, ol);
+        }
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < N; ++c) ov[c] += ol[c];
       }
       ptx::tmem_ld_wait();
       ptx::tc_fence_before();
@@ -846,18 +1025,37 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
       float sl[NL];
       bool good = wait_bar(sm, sm.bar(B_S_FULL + b), bph, p.err, 11);
       ptx::tc_fence_after();
-      if constexpr (NL == 32) {
-        ptx::tmem_ld_x32(tmem + lane_base + N * b, sl);
-      } else if constexpr (NL == 16) {
-        ptx::tmem_ld_x16(tmem + lane_base + N * b, sl);
-      } else if constexpr (NL == 8) {
-        ptx::tmem_ld_x8(tmem + lane_base + N * b + warp * NW, sl);
-      } else {
-        ptx::tmem_ld_x4(tmem + lane_base + N * b + warp * NW, sl);
+      // e4m3: the logits of q's three parts, columns pp * N + c, are added
+#pragma unroll
+      for (int pp = 0; pp < Cf::NQP; ++pp) {
+        float sp[NL];
+        const uint32_t col = tmem + lane_base + NS * b + pp * N + (TM ? 0 : warp * NW);
+        if constexpr (NL == 32) {
+          ptx::tmem_ld_x32(col, sp);
+        } else if constexpr (NL == 16) {
+          ptx::tmem_ld_x16(col, sp);
+        } else if constexpr (NL == 8) {
+          ptx::tmem_ld_x8(col, sp);
+        } else {
+          ptx::tmem_ld_x4(col, sp);
+        }
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < NL; ++k) sl[k] = pp == 0 ? sp[k] : sl[k] + sp[k];
       }
-      ptx::tmem_ld_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(sm.bar(B_S_EMPTY + b));
+      if constexpr (FP8) {
+        if (walk.first_of_segment()) {
+          // the q tile's prescale; the q warp may refill the tile once every
+          // softmax thread has read it (and the segment's last MMA is done)
+          const int qs = qseg & 1;
+          good = wait_bar(sm, sm.bar(B_Q_FULL + qs), (qseg >> 1) & 1, p.err, 15) && good;
+          sscale = p.scale_log2 * ksc * qexp[qs];
+          ptx::mbar_arrive(sm.bar(B_Q_EMPTY + qs));
+          ++qseg;
+        }
+      }
       const int valid = walk.valid();
       float x[G];
 #pragma unroll
@@ -872,7 +1070,7 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
           for (int k = 1; k < 32 / TT; ++k)
             if (sel == k) v = sl[k * G + i];
         }
-        x[i] = (good && tt < valid) ? v * p.scale_log2 : -INFINITY;
+        x[i] = (good && tt < valid) ? v * sscale : -INFINITY;
       }
       // ---- chunk max per column over its head's TT rows ----
       float cm[G];
@@ -914,15 +1112,42 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
         }
       }
       float alpha[G];
-      __nv_bfloat16 pb[G];
+      __nv_bfloat16 pb[G];   // bf16: p rounded for the MMA
+      uint8_t phi[G], plo[G];  // e4m3: 256 p ~= hi + lo, two e4m3 codes
+      float pv[G];
 #pragma unroll
       for (int i = 0; i < G; ++i) {
         const float m_new = fmaxf(m[i], cm[i]);
         const float msafe = m_new == -INFINITY ? 0.f : m_new;
         alpha[i] = fast_exp2(m[i] - msafe);
         m[i] = m_new;
-        pb[i] = __float2bfloat16_rn(fast_exp2(x[i] - msafe));  // 0 for masked rows
-        l[i] = l[i] * alpha[i] + __bfloat162float(pb[i]);
+        pv[i] = fast_exp2(x[i] - msafe);  // 0 for masked rows
+      }
+      if constexpr (FP8) {
+        // 256 p in [0, 256] keeps e4m3's range; l carries the same factor,
+        // so it cancels in o / l.  The residual is exact (Sterbenz).
+#pragma unroll
+        for (int i = 0; i < G; i += 2) {
+          const float a = pv[i] * 256.f, bq = (i + 1 < G ? pv[i + 1] : 0.f) * 256.f;
+          const uint16_t ch = pack_e4m3x2_rn(a, bq);
+          const float2 hv = e4m3x2_to_float2(ch);
+          const uint16_t cl = pack_e4m3x2_rn(a - hv.x, bq - hv.y);
+          const float2 lv = e4m3x2_to_float2(cl);
+          phi[i] = (uint8_t)(ch & 0xff);
+          plo[i] = (uint8_t)(cl & 0xff);
+          l[i] = l[i] * alpha[i] + (hv.x + lv.x);
+          if (i + 1 < G) {
+            phi[i + 1] = (uint8_t)(ch >> 8);
+            plo[i + 1] = (uint8_t)(cl >> 8);
+            l[i + 1] = l[i + 1] * alpha[i + 1] + (hv.y + lv.y);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          pb[i] = __float2bfloat16_rn(pv[i]);
+          l[i] = l[i] * alpha[i] + __bfloat162float(pb[i]);
+        }
       }
       if (tt == 0) {
 #pragma unroll
@@ -933,17 +1158,27 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
       if (valid < TT) {
         wait_bar(sm, sm.bar(B_FULL_V + s), ph, p.err, 13);
         if (tt >= valid) {
-          // row t's two halves: group t / 8, row t % 8 within it
+          // row t (bf16: its two halves): group t / 8, row t % 8 within it
           unsigned char* vrow = sm.base + OFF_V + s * TILE_B + (t >> 3) * GRP_B + (t & 7) * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const int cc = (c + t) & 7;
             *reinterpret_cast<uint4*>(vrow + cc * 16) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(vrow + HSTEP_B + cc * 16) = make_uint4(0, 0, 0, 0);
+            if (!FP8) *reinterpret_cast<uint4*>(vrow + HSTEP_B + cc * 16) = make_uint4(0, 0, 0, 0);
           }
         }
       }
-      {
+      if constexpr (FP8) {
+        // P^T rows c (hi) and N + c (lo): 128 bytes, tile row t at byte t
+        unsigned char* pt = sm.base + OFF_P + b * PTILE_B;
+        const int chunk = t >> 4, byte = t & 15;
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          const int c = hh * G + i, cl = N + c;
+          pt[(c >> 3) * 1024 + (c & 7) * 128 + (((chunk ^ (c & 7)) << 4) | byte)] = phi[i];
+          pt[(cl >> 3) * 1024 + (cl & 7) * 128 + (((chunk ^ (cl & 7)) << 4) | byte)] = plo[i];
+        }
+      } else {
         // P^T[c][r]: row c of 128 bf16, 64 per 128-byte swizzled half
         unsigned char* pt = sm.base + OFF_P + b * PTILE_B + (t >> 6) * PHALF_B;
         const int chunk = (t & 63) >> 3;
@@ -979,21 +1214,22 @@ __global__ void __launch_bounds__(Cfg<G, TM>::NTHREADS, 1)
 
 // ---------------- host side ----------------
 
-template <int G, bool TM>
+template <int G, bool TM, bool FP8>
 cudaError_t launch_g(const Params& prm, const CUtensorMap& mk, const CUtensorMap& mv,
                      const CUtensorMap& mq, cudaStream_t stream) {
+  using Cf = Cfg<G, TM, FP8>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_hp_kernel<G, TM>,
+    cudaError_t e = cudaFuncSetAttribute(decode_hp_kernel<G, TM, FP8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<G, TM>::SMEM_BYTES);
+                                         Cf::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(prm.num_ctas);
-  cfg.blockDim = dim3(Cfg<G, TM>::NTHREADS);
-  cfg.dynamicSmemBytes = Cfg<G, TM>::SMEM_BYTES;
+  cfg.blockDim = dim3(Cf::NTHREADS);
+  cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   // programmatic dependent launch: the prologue may overlap the previous
@@ -1002,7 +1238,7 @@ cudaError_t launch_g(const Params& prm, const CUtensorMap& mk, const CUtensorMap
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_hp_kernel<G, TM>, mk, mv, mq, prm);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_hp_kernel<G, TM, FP8>, mk, mv, mq, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1025,7 +1261,8 @@ bool hp_supported(int head_dim, int group, bool fp8, int num_seqs, int num_kv_he
   // a tile holds HB KV heads x TT tokens: H_kv must be a multiple of HB.
   // Blocks of at least TT tokens give head-major tiles (a chunk inside one
   // block), smaller blocks token-major tiles (a chunk of whole blocks).
-  if (fp8 || head_dim != hp::D || tokens_per_seq != 1) return false;
+  (void)fp8;  // bf16 or e4m3
+  if (head_dim != hp::D || tokens_per_seq != 1) return false;
   if (group != 1 && group != 2 && group != 4) return false;
   const int hb = hp::heads_per_tile(group);
   return num_kv_heads % hb == 0 && block_size >= 1 && num_seqs <= hp::kMaxSeqs &&
@@ -1041,9 +1278,41 @@ cudaError_t launch_decode_hp(const TcLaunch& a, cudaStream_t stream) {
   const int tt = 128 / hb;
   const int ncol = hb * group;
   const bool tm = a.block_size < tt;  // token-major tiles
+  const bool fp8 = a.fp8;
   if (a.num_ctas > kMaxPieces) return cudaErrorInvalidValue;  // a unit's pieces must fit the merge staging
   CUtensorMap mk, mv, mq;
-  if (!tm) {
+  if (fp8) {
+    // e4m3: a row (one token of one head) is 128 bytes, all of d.
+    // Head-major: (d, token, head, block), box {128, TT, HB, 1}; token-major:
+    // (d, head mod 8, head / 8, slot = block * block_size + token), box
+    // {128, 8, HB / 8, block_size}: one block's rows of HB heads, 8-row
+    // (1024-byte) groups per token.
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4];
+    if (!tm) {
+      dims[0] = D; dims[1] = a.block_size; dims[2] = a.num_kv_heads; dims[3] = a.num_blocks;
+      strides[0] = (cuuint64_t)a.num_kv_heads * D;
+      strides[1] = D;
+      strides[2] = (cuuint64_t)a.block_size * a.num_kv_heads * D;
+      box[0] = 128; box[1] = tt; box[2] = hb; box[3] = 1;
+    } else {
+      dims[0] = D; dims[1] = 8; dims[2] = a.num_kv_heads / 8;
+      dims[3] = (cuuint64_t)a.num_blocks * a.block_size;
+      strides[0] = D;
+      strides[1] = 8 * (cuuint64_t)D;
+      strides[2] = (cuuint64_t)a.num_kv_heads * D;
+      box[0] = 128; box[1] = 8; box[2] = hb / 8; box[3] = a.block_size;
+    }
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (enc(&mk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(a.k_cache), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    if (enc(&mv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(a.v_cache), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  } else if (!tm) {
     // [blocks, block_size, H_kv, d] listed as (d, token, head, block) so that
     // a box {64, TT, HB, 1} lands head-major: row = head * TT + token
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)a.block_size, (cuuint64_t)a.num_kv_heads,
@@ -1096,6 +1365,9 @@ cudaError_t launch_decode_hp(const TcLaunch& a, cudaStream_t stream) {
   prm.block_tables = a.block_tables;
   prm.context_lens = a.context_lens;
   prm.lse = a.lse;
+  prm.q = a.q;
+  prm.k_scale = a.k_scale;
+  prm.v_scale = a.v_scale;
   char* ws = static_cast<char*>(a.workspace);
   size_t off = 0;
   prm.err = reinterpret_cast<int*>(ws + off);
@@ -1118,13 +1390,19 @@ cudaError_t launch_decode_hp(const TcLaunch& a, cudaStream_t stream) {
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   prm.early_meta = a.early_meta ? 1 : 0;
   prm.epoch = tc::next_call_epoch();
-  switch (group * 2 + (tm ? 1 : 0)) {
-    case 2: return launch_g<1, false>(prm, mk, mv, mq, stream);
-    case 3: return launch_g<1, true>(prm, mk, mv, mq, stream);
-    case 4: return launch_g<2, false>(prm, mk, mv, mq, stream);
-    case 5: return launch_g<2, true>(prm, mk, mv, mq, stream);
-    case 8: return launch_g<4, false>(prm, mk, mv, mq, stream);
-    case 9: return launch_g<4, true>(prm, mk, mv, mq, stream);
+  switch (group * 4 + (tm ? 2 : 0) + (fp8 ? 1 : 0)) {
+    case 4: return launch_g<1, false, false>(prm, mk, mv, mq, stream);
+    case 5: return launch_g<1, false, true>(prm, mk, mv, mq, stream);
+    case 6: return launch_g<1, true, false>(prm, mk, mv, mq, stream);
+    case 7: return launch_g<1, true, true>(prm, mk, mv, mq, stream);
+    case 8: return launch_g<2, false, false>(prm, mk, mv, mq, stream);
+    case 9: return launch_g<2, false, true>(prm, mk, mv, mq, stream);
+    case 10: return launch_g<2, true, false>(prm, mk, mv, mq, stream);
+    case 11: return launch_g<2, true, true>(prm, mk, mv, mq, stream);
+    case 16: return launch_g<4, false, false>(prm, mk, mv, mq, stream);
+    case 17: return launch_g<4, false, true>(prm, mk, mv, mq, stream);
+    case 18: return launch_g<4, true, false>(prm, mk, mv, mq, stream);
+    case 19: return launch_g<4, true, true>(prm, mk, mv, mq, stream);
     default: return cudaErrorInvalidValue;
   }
 }
