@@ -234,7 +234,8 @@ pa_status pa_write_and_decode(const void* key, const void* value,
  *
  *  - Output and numerics are those of pa_decode with the automatic kernel
  *    choice.  When that choice is the SIMT kernel (head_dim other than 128,
- *    block_size below 8, ...), its split-K partition length is the shortest
+ *    or a head layout the tensor-core kernels do not take), its split-K
+ *    partition length is the shortest
  *    power of two from 256 tokens whose partials fit; the tensor-core
  *    kernels ignore partition lengths and use their fixed per-CTA slots.
  *  - PA_ERR_UNSUPPORTED, with nothing launched, when the sizes need more
