@@ -120,6 +120,13 @@ struct Cfg {
   // per-chunk barrier (head-major), two when after it (token-major)
   static constexpr int NALPHA = TM ? 2 : 3;
   static constexpr int TAB_IDS = TM ? TT : 1;  // block ids per chunk in the id ring
+  // e4m3 token-major tiles of 8 heads are loaded by row gathers (see the
+  // producer): a token's 8 heads land as one unswizzled 1 KiB group, which
+  // the MMAs read through their 128-byte-swizzle descriptors, so row hh of
+  // the group sees its 16-byte pieces of d in the order j ^ hh.  The q warp
+  // stores the columns of head hh with the same order, and every output
+  // element of column c is written back to d ^ (16 * (c / G)).
+  static constexpr bool G4 = FP8 && TM && HB == 8;
 
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NST * TILE_B;
@@ -375,14 +382,37 @@ __global__ void __launch_bounds__(Cfg<G, TM, FP8>::NTHREADS, 1)
         phys = 0;
       }
       if constexpr (TM) {
-        // one block's rows of the HB heads
+        // one block's rows of the HB heads (gathers: always the whole tile)
         const uint32_t box_b = (uint32_t)bs * HB * D * Cf::ELT;
+        const uint32_t tile_tx = Cf::G4 ? (uint32_t)TILE_B : (uint32_t)nb * box_b;
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_K + s), (uint32_t)nb * box_b);
-          ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_V + s), (uint32_t)nb * box_b);
+          ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_K + s), tile_tx);
+          ptx::mbar_arrive_expect_tx(sm.bar(B_FULL_V + s), tile_tx);
         }
         __syncwarp();
-        if (lane < nb) {
+        if constexpr (Cf::G4) {
+          // Four gathers of four tokens each, for K and for V: a token's rows
+          // of the 8 heads are one 1 KiB row of the cache seen as (slot, d of
+          // all heads).  Token tk's slot is the id of block tk / B (held by
+          // lane tk / B) times B plus tk % B; tokens past the context end
+          // repeat the chunk's first token and are masked later.
+          int sl[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int tk = 4 * (lane & 3) + i;
+            const int tkc = tk < walk.valid() ? tk : 0;
+            const int pb = __shfl_sync(0xffffffffu, phys, tkc >> p.log2_bs);
+            sl[i] = (pb << p.log2_bs) + (tkc & (bs - 1));
+          }
+          if (lane < 4) {
+            const uint32_t off = s * TILE_B + lane * 4096;
+            const int col = walk.g * (HB * D / 4);
+            ptx::tma_gather4(sm.base_u32 + OFF_K + off, &tm_k, sm.bar(B_FULL_K + s), col, sl[0],
+                             sl[1], sl[2], sl[3]);
+            ptx::tma_gather4(sm.base_u32 + OFF_V + off, &tm_v, sm.bar(B_FULL_V + s), col, sl[0],
+                             sl[1], sl[2], sl[3]);
+          }
+        } else if (lane < nb) {
           const uint32_t off = s * TILE_B + lane * box_b;
           const int slot0 = phys << p.log2_bs;  // < num_blocks * block_size <= 2^31 - 1
           if constexpr (FP8) {
@@ -672,8 +702,9 @@ __global__ void __launch_bounds__(Cfg<G, TM, FP8>::NTHREADS, 1)
           uint2 w2;
           w2.x = *reinterpret_cast<uint32_t*>(&lo2);
           w2.y = *reinterpret_cast<uint32_t*>(&hi2);
+          const int dq = Cf::G4 ? ((4 * lane) ^ (((cb + k) / G) << 4)) : 4 * lane;
           *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                    (row0 + cb + k) * D + 4 * lane) = w2;
+                                    (row0 + cb + k) * D + dq) = w2;
           if (p.lse && lane == k) p.lse[row0 + cb + k] = M[k] + __log2f(Ls[k]) - (FP8 ? 8.f : 0.f);
         }
       }
@@ -737,9 +768,12 @@ __global__ void __launch_bounds__(Cfg<G, TM, FP8>::NTHREADS, 1)
           }
 #pragma unroll
           for (int part = 0; part < 3; ++part) {
-            // 128-byte swizzle: 16-byte piece index XOR (row & 7)
+            // 128-byte swizzle: 16-byte piece index XOR (row & 7); gathered
+            // tiles also XOR the piece index with the column's head
             const int r = part * N + c;
-            const int o = (r >> 3) * 1024 + (r & 7) * 128 + ((((d0 >> 4) ^ (r & 7)) << 4) | (d0 & 8));
+            const int xq = Cf::G4 ? c / G : 0;
+            const int o = (r >> 3) * 1024 + (r & 7) * 128 +
+                          (((((d0 >> 4) ^ xq) ^ (r & 7)) << 4) | (d0 & 8));
             *reinterpret_cast<uint2*>(qt + o) = make_uint2(pw[part][0], pw[part][1]);
           }
         }
@@ -844,7 +878,8 @@ __global__ void __launch_bounds__(Cfg<G, TM, FP8>::NTHREADS, 1)
       if (c0 == c1) {
 #pragma unroll
         for (int c = 0; c < N; ++c)
-          o[(row0 + c) * D] = __float2bfloat16_rn(acc[c] * (__fdividef(1.f, L[c]) * vsc));
+          o[(row0 + c) * D + (Cf::G4 ? (t ^ ((c / G) << 4)) - t : 0)] =
+              __float2bfloat16_rn(acc[c] * (__fdividef(1.f, L[c]) * vsc));
         if (p.lse && t < N) p.lse[row0 + t] = own_ml.x + __log2f(own_ml.y) - lse_off;
         return;
       }
@@ -961,7 +996,7 @@ __global__ void __launch_bounds__(Cfg<G, TM, FP8>::NTHREADS, 1)
       for (int c = 0; c < N; ++c) {
         // the merge warp's rounding: a * (1 / L), times v_scale for e4m3
         const float inv = FP8 ? __frcp_rn(sc[c].y) * vsc : __frcp_rn(sc[c].y);
-        sot[c * D + t] = __float2bfloat16_rn(acc[c] * inv);
+        sot[c * D + (Cf::G4 ? t ^ ((c / G) << 4) : t)] = __float2bfloat16_rn(acc[c] * inv);
       }
       if (p.lse && t < N) p.lse[row0 + t] = sc[t].x + __log2f(sc[t].y) - lse_off;
       ptx::bar_sync_named(2, 128);
@@ -1304,6 +1339,24 @@ cudaError_t launch_decode_hp(const TcLaunch& a, cudaStream_t stream) {
       box[0] = 128; box[1] = 8; box[2] = hb / 8; box[3] = a.block_size;
     }
     cuuint32_t es[4] = {1, 1, 1, 1};
+    if (tm && hb == 8) {
+      // row gathers: the cache as (32-bit words of d over all heads, slot);
+      // a gathered row is one token's 8 heads of group g (256 words, 1 KiB),
+      // copied without swizzle
+      cuuint64_t gd[2] = {(cuuint64_t)a.num_kv_heads * D / 4,
+                          (cuuint64_t)a.num_blocks * a.block_size};
+      cuuint64_t gs[1] = {(cuuint64_t)a.num_kv_heads * D};
+      cuuint32_t gb[2] = {(cuuint32_t)hb * D / 4, 1};
+      cuuint32_t ge[2] = {1, 1};
+      if (enc(&mk, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(a.k_cache), gd, gs, gb,
+              ge, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+      if (enc(&mv, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(a.v_cache), gd, gs, gb,
+              ge, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    } else {
     if (enc(&mk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(a.k_cache), dims, strides,
             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -1312,6 +1365,7 @@ cudaError_t launch_decode_hp(const TcLaunch& a, cudaStream_t stream) {
             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
+    }
   } else if (!tm) {
     // [blocks, block_size, H_kv, d] listed as (d, token, head, block) so that
     // a box {64, TT, HB, 1} lands head-major: row = head * TT + token
