@@ -63,6 +63,28 @@ using tc::wait_bar;
 
 constexpr int D = 128;
 constexpr int CHK = 128;                  // keys per chunk
+
+// Paired fp32 arithmetic (one instruction for two lanes of work): the
+// softmax of a prefill tile is bound by instruction issue.
+__device__ __forceinline__ float2 fma_x2(float2 a, float2 b, float2 c) {
+  unsigned long long ra, rb, rc, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
+__device__ __forceinline__ float2 add_x2(float2 a, float2 b) {
+  unsigned long long ra, rb, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
 // K and V rings: a K chunk is free once its logits MMA completes, a V chunk
 // only after its PV MMA, so K runs one stage further ahead
 constexpr int NSTK = 3, NSTV = 2;
@@ -779,22 +801,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         } else {
           // keys half * 64 ..: the row's 128-byte half `half` of the P tile
           unsigned char* prow = sm.base + OFF_P + half * HALF_B + row * 128;
+          float2 l2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
+          const float2 rs2 = make_float2(rs, rs), nm2 = make_float2(-msafe, -msafe);
 #pragma unroll
           for (int c8 = 0; c8 < 8; ++c8) {
             uint32_t w[4];
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
               const int e = (c8 & 3) * 8 + 2 * e2;
-              // p = 2^(s * scale - m): one FMA per logit (masked logits are -inf)
-              const float p0 = fast_exp2(fmaf(sv[c8 >> 2][e], rs, -msafe));
-              const float p1 = fast_exp2(fmaf(sv[c8 >> 2][e + 1], rs, -msafe));
-              l4[e2] += p0 + p1;  // before the bf16 rounding the MMA sees: within its error
-              const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+              // p = 2^(s * scale - m): one paired FMA per two logits (masked
+              // logits are -inf)
+              const float2 x2 =
+                  fma_x2(make_float2(sv[c8 >> 2][e], sv[c8 >> 2][e + 1]), rs2, nm2);
+              const float2 p2 = make_float2(fast_exp2(x2.x), fast_exp2(x2.y));
+              l2[e2] = add_x2(l2[e2], p2);  // before the bf16 rounding the MMA sees
+              const __nv_bfloat162 pb = __floats2bfloat162_rn(p2.x, p2.y);
               w[e2] = *reinterpret_cast<const uint32_t*>(&pb);
             }
             *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) =
                 make_uint4(w[0], w[1], w[2], w[3]);
           }
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) l4[e2] = l2[e2].x + l2[e2].y;
         }
         l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         ptx::fence_proxy_async_smem();
