@@ -31,9 +31,8 @@ def test_serving_mix(prefix):
     harness.assert_close(got["out"], ref["out"], False)
 
 
-def _grouped(group, n_groups, prefix_blocks, suffix_lens, H, Hkv, kv_dtype, seed):
+def _grouped(group, n_groups, prefix_blocks, suffix_lens, H, Hkv, kv_dtype, seed, B=16):
     """Tables where each group's members share their first prefix_blocks blocks."""
-    B = 16
     rng = np.random.default_rng(seed)
     S = group * n_groups
     lens = np.array([prefix_blocks * B + int(s) for s in suffix_lens], dtype=np.int32)
@@ -92,6 +91,19 @@ def test_groups_gqa_and_e4m3(group, H, Hkv, kv):
     suffix = rng.integers(1, 900, size=group * 6)
     c = _grouped(group, 6, 40, suffix, H, Hkv, kv, seed=group * 3 + H)
     _run_and_check(c, group, kv == "fp8")
+
+
+@requires_gpu
+@pytest.mark.parametrize("B", [1, 4])
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_small_blocks(B, kv):
+    # blocks of fewer than 8 tokens: the suffix pass runs on the head-packed
+    # kernel's token-major tiles (e4m3: row gathers) and hands its log2-sum-
+    # exp to the merge; the prefix pass gathers rows on the per-head kernel
+    rng = np.random.default_rng(11 + B)
+    suffix = rng.integers(1, 700, size=4 * 5)
+    c = _grouped(4, 5, 480 // B, suffix, 32, 8, kv, seed=13 + B, B=B)
+    _run_and_check(c, 4, kv == "fp8")
 
 
 @requires_gpu
