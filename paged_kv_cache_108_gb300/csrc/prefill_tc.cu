@@ -138,6 +138,7 @@ struct PCfg {
   // small weights above e4m3's 2^-9 floor
   static constexpr float kRescaleLog2 = FP8 ? 3.f : 8.f;
   static constexpr float kPScale = FP8 ? 32.f : 1.f;  // 2^(8 - R)
+  static constexpr float kPScaleLog2 = FP8 ? 5.f : 0.f;  // 8 - R
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
   static_assert(OFF_BAR % 1024 == 0, "tiles stay 1024-byte aligned");
 };
@@ -775,22 +776,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           // of the row's 128-byte row in each part; the sum adds the parts, so
           // the factor and the rounding cancel in O / l
           unsigned char* prow = sm.base + OFF_P + row * 128;
+          // 2^(8 - R) p = 2^(s * scale - m + 8 - R): the factor folds into the
+          // FMA's bias; logits and sums go two to an instruction
+          const float2 rs2 = make_float2(rs, rs);
+          const float bias = C::kPScaleLog2 - msafe;
+          const float2 nb2 = make_float2(bias, bias);
+          float2 l2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
             uint32_t hw[4], lw[4];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               const int e = c4 * 16 + q4 * 4;  // key among this thread's 64
-              float x[4];
-#pragma unroll
-              for (int t4 = 0; t4 < 4; ++t4)
-                x[t4] = fast_exp2(fmaf(sv[(e + t4) >> 5][(e + t4) & 31], rs, -msafe)) * C::kPScale;
+              const float2 a01 = fma_x2(make_float2(sv[e >> 5][e & 31], sv[(e + 1) >> 5][(e + 1) & 31]),
+                                        rs2, nb2);
+              const float2 a23 = fma_x2(make_float2(sv[(e + 2) >> 5][(e + 2) & 31],
+                                                    sv[(e + 3) >> 5][(e + 3) & 31]), rs2, nb2);
+              const float x[4] = {fast_exp2(a01.x), fast_exp2(a01.y), fast_exp2(a23.x),
+                                  fast_exp2(a23.y)};
               const uint16_t h01 = pack_e4m3x2_rn(x[0], x[1]), h23 = pack_e4m3x2_rn(x[2], x[3]);
               const float2 f01 = e4m3x2_to_float2(h01), f23 = e4m3x2_to_float2(h23);
               const uint16_t g01 = pack_e4m3x2_rn(x[0] - f01.x, x[1] - f01.y);
               const uint16_t g23 = pack_e4m3x2_rn(x[2] - f23.x, x[3] - f23.y);
               const float2 r01 = e4m3x2_to_float2(g01), r23 = e4m3x2_to_float2(g23);
-              l4[q4] += ((f01.x + r01.x) + (f01.y + r01.y)) + ((f23.x + r23.x) + (f23.y + r23.y));
+              l2[q4] = add_x2(add_x2(l2[q4], add_x2(f01, r01)), add_x2(f23, r23));
               hw[q4] = (uint32_t)h01 | ((uint32_t)h23 << 16);
               lw[q4] = (uint32_t)g01 | ((uint32_t)g23 << 16);
             }
@@ -798,6 +808,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             *reinterpret_cast<uint4*>(prow + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             *reinterpret_cast<uint4*>(prow + PPART_B + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) l4[q4] = l2[q4].x + l2[q4].y;
         } else {
           // keys half * 64 ..: the row's 128-byte half `half` of the P tile
           unsigned char* prow = sm.base + OFF_P + half * HALF_B + row * 128;
