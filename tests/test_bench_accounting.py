@@ -38,3 +38,33 @@ def test_llama8b_decode_bytes_match_the_stated_figure():
     qo = 2 * 64 * 32 * 128 * 2
     table = sum(-(-int(n) // 16) for n in w.context_lens) * 4
     assert kv + qo + table + 64 * 4 == 498_399_248
+
+
+def test_traffic_record_applies_only_to_the_source_it_was_taken_on(tmp_path, monkeypatch):
+    # a record carries the sha-256 of the kernel sources it was captured on;
+    # once one of them changes, the bench reports no traffic rather than a
+    # figure taken on other code
+    import hashlib
+    import json
+    src = tmp_path / "k.cu"
+    src.write_bytes(b"kernel v1")
+    (tmp_path / "profiles").mkdir()
+    rec = {"sources": ["k.cu"], "sources_sha256": hashlib.sha256(b"kernel v1").hexdigest(),
+           "dram_bytes_per_call": 123}
+    (tmp_path / "profiles" / "decode_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic(0) == 123
+    assert bench.recorded_traffic(0, "fp8") is None  # no record for that cache type
+    src.write_bytes(b"kernel v2")
+    assert bench.recorded_traffic(0) is None
+
+
+def test_committed_traffic_records_are_well_formed():
+    import json
+    import os
+    for name in ("decode_traffic.json", "decode_traffic_fp8.json"):
+        with open(os.path.join(bench.ROOT, "profiles", name)) as f:
+            rec = json.load(f)
+        assert all(os.path.exists(os.path.join(bench.ROOT, s)) for s in rec["sources"])
+        assert rec["dram_bytes_per_call"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
+        assert "--clock-control none" in rec["command"]
