@@ -37,16 +37,35 @@
 // shared units first).  Both read all pieces from the slots in CTA order
 // with the same roundings, so the output does not depend on who merges.
 //
+// Token-major tiles (blocks of fewer than TT tokens).  A chunk is TT
+// tokens of whole blocks; its rows are (token, head), r = tt * HB + hh, so
+// one copy per block brings that block's rows of all HB heads (the cache
+// rows of one token's heads are contiguous).  A column's rows then span the
+// four softmax warps: the chunk maximum takes one shared-memory exchange,
+// and each thread picks its own head's G columns of the logits.
+//
+// e4m3 caches.  The MMAs take the cache bytes as they are (kind::f8f6f4):
+// the q warp writes each unit's bf16 q, scaled by a power of two, as three
+// e4m3 parts (operand rows part * N + c) whose logits add up to q . k; the
+// softmax writes 256 p as two e4m3 parts (P rows c and N + c).  The factor
+// 256 cancels in o / l, k_scale and the power of two fold into the logit
+// scale, v_scale multiplies the output.  Token-major e4m3 tiles of 8 heads
+// are loaded by row gathers (four tokens' 1 KiB rows per copy) that land
+// unswizzled; the q parts and the outputs are permuted to match (see G4 in
+// Cfg).
+//
 // Warp roles (256 threads):
 //   warps 0-3  softmax + epilogue: thread t owns TMEM lane t (row t of the
 //              logits tile; element d = t of the output tile);
-//   warp 4     producer: per chunk one block id (a cp.async ring a few chunks
-//              ahead) and four TMA copies (K and V, two 64-column halves)
-//              into a 3-stage ring;
-//   warp 5     TMEM allocation; one thread issues the MMAs and the q tile's
-//              loads (one buffer, reloaded when a unit starts);
+//   warp 4     producer: per chunk the block ids (a cp.async ring a few
+//              chunks ahead) and the chunk's TMA copies (head-major: K and V
+//              boxes; token-major: one box per block, or row gathers) into a
+//              3-stage (bf16) or 5-stage (e4m3) ring;
+//   warp 5     TMEM allocation; one thread issues the MMAs and, for bf16,
+//              the q tile's loads (one buffer, reloaded when a unit starts);
 //   warp 6     merge warp;
-//   warp 7     no role after the prologue.
+//   warp 7     e4m3: the q warp (q parts, two buffers); bf16: no role after
+//              the prologue.
 //
 // Every mbarrier wait gives up after ~2^31 clocks: the thread records an
 // error code in the workspace's first word and marks the CTA aborted, so the
@@ -83,8 +102,8 @@ constexpr int TAB_SLOTS = 4, TAB_AHEAD = 3;  // block-id ring: one id per chunk
 constexpr int kMaxPieces = 160;  // pieces of one split unit: at most the persistent CTAs
 
 // G query heads per KV head (1, 2 or 4).  TM: token-major tiles, for blocks
-// of fewer than TT tokens (see the tile note above the kernel).  FP8: an
-// e4m3 cache (see the e4m3 note above the kernel).
+// of fewer than TT tokens.  FP8: an e4m3 cache.  (Both are described at the
+// top of this file.)
 template <int G, bool TM, bool FP8>
 struct Cfg {
   static constexpr int HB = G >= 2 ? 8 : 16;  // KV heads per tile
