@@ -1,6 +1,6 @@
 // Causal paged attention for prefill chunks on the 5th-generation tensor
-// cores, for a bf16 cache with head_dim 128: the tensor-core path of
-// pa_varlen_attention.
+// cores, for a bf16 or e4m3 cache with head_dim 128: the tensor-core path
+// of pa_varlen_attention.
 //
 // What it computes is the varlen paged attention of "Paged attention"
 // (query_start_loc, seq_lens, causal limit): request r's new tokens are
@@ -31,6 +31,19 @@
 // folded into one FMA per logit).  Keys past a row's causal limit get p = 0 (a select,
 // so stale cache bytes never reach the result); V rows past the item's last
 // key are zeroed in smem.
+//
+// e4m3 caches (PCfg<true>).  The MMAs take the cache bytes as they are
+// (kind::f8f6f4; K and V chunks of 128 keys x 128-byte rows).  At an item's
+// start the softmax threads split the staged bf16 q rows, each scaled by
+// the power of two that puts its max |q| in [128, 256), into three e4m3
+// parts (three operand tiles; the logits are the sum of three MMAs).  P
+// holds 2^(8 - R) p as two e4m3 parts, with the rescale threshold R = 3 so
+// that it stays inside e4m3's range; the factor and the rounding cancel in
+// O / l.  P V is computed as its transpose, O^T = V^T P^T (V the MN-major A
+// operand, P's rows the K-major B operand), so a row of O is a column of
+// the tensor-memory tile: a row's rescale is collective (each row publishes
+// its factor and one reduction barrier tells every thread whether any row
+// rescales), and the epilogue writes each thread's element d of 64 rows.
 //
 // Warp roles (352 threads): warps 0-7 softmax and epilogue, two threads per
 // row (64 keys and 64 output columns each); warp 8 producer of the q tiles
